@@ -1,0 +1,155 @@
+"""Exact attention for one GB300 (sm_103a): Python binding of libfa.
+
+The functions named like the C ABI (``fa_fwd``, ``fa_bwd``, ``fa_get_status``,
+``fa_status_string``, ``fa_debug_set``, ``fa_debug_exp2``) only marshal
+arguments: pointers may be given as ints or as CUDA tensors, the stream as an
+int, a ``torch.cuda.Stream`` or None (the current stream). They return the
+library's integer status. ``forward`` and ``backward`` allocate outputs with
+torch, call the C ABI and raise ``FAError`` on a non-zero status.
+
+Every computation runs in the CUDA kernels of libfa.so; there is no fallback.
+If the library is missing the import of this module still succeeds (so it can
+be built), but every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+__all__ = ["FAError", "lib", "fa_fwd", "fa_bwd", "fa_get_status", "fa_status_string", "fa_debug_set",
+           "fa_debug_exp2", "forward", "backward", "STATUS"]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfa.so")
+
+STATUS = {
+    0: "FA_OK",
+    1: "FA_ERR_INVALID_ARG",
+    2: "FA_ERR_UNSUPPORTED",
+    3: "FA_ERR_ALLOC",
+    4: "FA_ERR_LAUNCH",
+    5: "FA_ERR_TIMEOUT",
+    6: "FA_ERR_NO_DEVICE",
+}
+
+
+class FAError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {STATUS.get(status, status)}")
+        self.status = status
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libfa.so (built in-tree). Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libfa.so is not built ({LIB_PATH}); run exact_attention_99_gb300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i, f, ull = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_ulonglong
+        L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp]
+        L.fa_fwd.restype = i
+        L.fa_bwd.argtypes = [vp] * 9 + [i, i, i, i, i, i, f, i, vp]
+        L.fa_bwd.restype = i
+        L.fa_get_status.argtypes = [vp]
+        L.fa_get_status.restype = i
+        L.fa_status_string.argtypes = [i]
+        L.fa_status_string.restype = ctypes.c_char_p
+        L.fa_debug_set.argtypes = [ull, i]
+        L.fa_debug_set.restype = i
+        L.fa_debug_exp2.argtypes = [vp, vp, i, i, vp]
+        L.fa_debug_exp2.restype = i
+        _lib = L
+    return _lib
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(s):
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def fa_fwd(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, stream=None) -> int:
+    return lib().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Nq, Nk, d, float(scale),
+                        int(causal), _stream(stream))
+
+
+def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Nq, Nk, d, scale, causal, stream=None) -> int:
+    return lib().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
+                        B, Hq, Hkv, Nq, Nk, d, float(scale), int(causal), _stream(stream))
+
+
+def fa_get_status(stream=None) -> int:
+    return lib().fa_get_status(_stream(stream))
+
+
+def fa_status_string(status: int) -> str:
+    return lib().fa_status_string(int(status)).decode()
+
+
+def fa_debug_set(wait_limit_ns: int = 0, inject: int = 0) -> int:
+    return lib().fa_debug_set(int(wait_limit_ns), int(inject))
+
+
+def fa_debug_exp2(x, y, n, mode, stream=None) -> int:
+    return lib().fa_debug_exp2(_ptr(x), _ptr(y), int(n), int(mode), _stream(stream))
+
+
+def _check_bshd(name, t, B, N, H, d):
+    import torch
+    if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or tuple(t.shape) != (B, N, H, d):
+        raise ValueError(f"{name} must be a contiguous CUDA bf16 tensor of shape {(B, N, H, d)}")
+
+
+def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None, stream=None):
+    """O, LSE for q [B,Nq,Hq,d], k/v [B,Nk,Hkv,d] (bf16, CUDA, contiguous)."""
+    import torch
+    B, Nq, Hq, d = q.shape
+    _, Nk, Hkv, _ = k.shape
+    _check_bshd("q", q, B, Nq, Hq, d)
+    _check_bshd("k", k, B, Nk, Hkv, d)
+    _check_bshd("v", v, B, Nk, Hkv, d)
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    if out is None:
+        o = torch.empty_like(q)
+        lse = torch.empty((B, Hq, Nq), device=q.device, dtype=torch.float32)
+    else:
+        o, lse = out
+    st = fa_fwd(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, stream)
+    if st != 0:
+        raise FAError(st, "fa_fwd")
+    return o, lse
+
+
+def backward(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None, out=None, stream=None):
+    """dQ, dK, dV for the forward that produced o and lse."""
+    import torch
+    B, Nq, Hq, d = q.shape
+    _, Nk, Hkv, _ = k.shape
+    for name, t, N, H in (("q", q, Nq, Hq), ("k", k, Nk, Hkv), ("v", v, Nk, Hkv), ("o", o, Nq, Hq),
+                          ("dout", dout, Nq, Hq)):
+        _check_bshd(name, t, B, N, H, d)
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    if out is None:
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    else:
+        dq, dk, dv = out
+    st = fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Nq, Nk, d, scale, causal, stream)
+    if st != 0:
+        raise FAError(st, "fa_bwd")
+    return dq, dk, dv

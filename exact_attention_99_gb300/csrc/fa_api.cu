@@ -1,0 +1,219 @@
+// C ABI of libfa: argument validation, per-device state, dispatch.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/fa.h"
+#include "fa_internal.h"
+#include "sm103_math.cuh"
+#include "sm103_ptx.cuh"
+
+namespace fa {
+
+// Per-device status word: kernels OR error bits into it; fa_get_status reads
+// and clears it. A file-scope __device__ word (one copy per device).
+__device__ unsigned g_fa_status;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;
+
+std::mutex g_mu;
+int g_sms[kMaxDevices];
+unsigned* g_status_ptr[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+DebugCfg g_debug = {kDefaultWaitNs, 0};
+
+int current_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+  return dev;
+}
+
+bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Argument checks shared by fa_fwd and fa_bwd (pointers checked by callers).
+int check_sizes(int B, int Hq, int Hkv, int Nq, int Nk, int d, float scale, int causal) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Nq < 1 || Nk < 1) return FA_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.0f)) return FA_ERR_INVALID_ARG;
+  if (d < 1) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  // index ranges: sequence coordinates and unit counts stay in int32,
+  // tensor strides stay below the tensor-map limit of 2^40 bytes
+  if (Nq > (1 << 28) || Nk > (1 << 28)) return FA_ERR_UNSUPPORTED;
+  const long long q_elems = 1LL * B * Nq * Hq * d, k_elems = 1LL * B * Nk * Hkv * d;
+  if (q_elems * 2 >= (1LL << 40) || k_elems * 2 >= (1LL << 40)) return FA_ERR_UNSUPPORTED;
+  if (1LL * B * Hq * ((Nq + 255) / 256) >= (1LL << 30)) return FA_ERR_UNSUPPORTED;
+  if (1LL * B * Hkv * ((Nk + 127) / 128) >= (1LL << 30)) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+int check_device() {
+  const int dev = current_device();
+  if (dev < 0) return FA_ERR_NO_DEVICE;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return FA_ERR_NO_DEVICE;
+  if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return FA_ERR_NO_DEVICE;
+  if (major != 10 || minor != 3) return FA_ERR_NO_DEVICE;
+  return FA_OK;
+}
+
+__global__ void debug_exp2_kernel(const float* x, float* y, int n, int mode) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  float a = x[i];
+  if (mode == 0) {
+    y[i] = ex2_mufu(a);
+  } else {
+    float b = a;
+    exp2_poly_pair(a, b);
+    y[i] = a;
+  }
+}
+
+}  // namespace
+
+DebugCfg debug_cfg() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  return g_debug;
+}
+
+int num_sms() {
+  const int dev = current_device();
+  if (dev < 0) return 1;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_sms[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    g_sms[dev] = n > 0 ? n : 1;
+  }
+  return g_sms[dev];
+}
+
+unsigned* status_word() {
+  const int dev = current_device();
+  if (dev < 0) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_fa_status) != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = static_cast<unsigned*>(p);
+  }
+  return g_status_ptr[dev];
+}
+
+bool make_bshd_map(CUtensorMap* m, const void* base, int B, int N, int H, int d, int box_rows) {
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+              cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || !fn)
+        return false;
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+  }
+  cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)N, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2, (cuuint64_t)N * H * d * 2};
+  cuuint32_t box[4] = {64, 1, (cuuint32_t)box_rows, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+cudaError_t launch_debug_exp2(const float* x, float* y, int n, int mode, cudaStream_t stream) {
+  debug_exp2_kernel<<<(n + 255) / 256, 256, 0, stream>>>(x, y, n, mode);
+  return cudaGetLastError();
+}
+
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Nq,
+                      int Nk, int d, float scale, int causal, void* stream) {
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return FA_ERR_INVALID_ARG;
+  int st = check_sizes(B, Hq, Hkv, Nq, Nk, d, scale, causal);
+  if (st != FA_OK) return st;
+  st = check_device();
+  if (st != FA_OK) return st;
+  Problem p{q, k, v, B, Hq, Hkv, Nq, Nk, d, scale, causal};
+  return launch_fwd(p, o, lse, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                      void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Nq, int Nk, int d, float scale,
+                      int causal, void* stream) {
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(dout) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return FA_ERR_INVALID_ARG;
+  int st = check_sizes(B, Hq, Hkv, Nq, Nk, d, scale, causal);
+  if (st != FA_OK) return st;
+  st = check_device();
+  if (st != FA_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t acc_bytes = sizeof(float) * size_t(B) * Nq * Hq * d;
+  const size_t delta_bytes = sizeof(float) * size_t(B) * Hq * Nq;
+  void* ws = nullptr;
+  if (cudaMallocAsync(&ws, acc_bytes + delta_bytes, s) != cudaSuccess) {
+    cudaGetLastError();
+    return FA_ERR_ALLOC;
+  }
+  Problem p{q, k, v, B, Hq, Hkv, Nq, Nk, d, scale, causal};
+  float* dq_acc = static_cast<float*>(ws);
+  float* delta = reinterpret_cast<float*>(static_cast<char*>(ws) + acc_bytes);
+  const cudaError_t e = launch_bwd(p, o, lse, dout, dq, dk, dv, dq_acc, delta, s);
+  const cudaError_t f = cudaFreeAsync(ws, s);
+  if (e != cudaSuccess || f != cudaSuccess) return FA_ERR_LAUNCH;
+  return FA_OK;
+}
+
+extern "C" int fa_get_status(void* stream) {
+  if (check_device() != FA_OK) return FA_ERR_NO_DEVICE;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_LAUNCH;
+  unsigned v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_fa_status, sizeof(v)) != cudaSuccess) return FA_ERR_LAUNCH;
+  const unsigned zero = 0;
+  if (cudaMemcpyToSymbol(g_fa_status, &zero, sizeof(zero)) != cudaSuccess) return FA_ERR_LAUNCH;
+  return (v & kDevTimeout) ? FA_ERR_TIMEOUT : FA_OK;
+}
+
+extern "C" const char* fa_status_string(int status) {
+  switch (status) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+    case FA_ERR_ALLOC: return "FA_ERR_ALLOC";
+    case FA_ERR_LAUNCH: return "FA_ERR_LAUNCH";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
+    case FA_ERR_NO_DEVICE: return "FA_ERR_NO_DEVICE";
+    default: return "FA_ERR_UNKNOWN";
+  }
+}
+
+extern "C" int fa_debug_set(unsigned long long wait_limit_ns, int inject) {
+  if (inject < 0 || inject > 1) return FA_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_debug.wait_limit_ns = wait_limit_ns == 0 ? kDefaultWaitNs : wait_limit_ns;
+  g_debug.inject = inject;
+  return FA_OK;
+}
+
+extern "C" int fa_debug_exp2(const float* x, float* y, int n, int mode, void* stream) {
+  if (!aligned16(x) || !aligned16(y) || n < 0 || (mode != 0 && mode != 1)) return FA_ERR_INVALID_ARG;
+  if (n == 0) return FA_OK;
+  const int st = check_device();
+  if (st != FA_OK) return st;
+  return launch_debug_exp2(x, y, n, mode, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}

@@ -1,0 +1,565 @@
+// Forward pass of exact attention on sm_103a.
+//
+// Method (the post "FlashAttention v1", deep_school #630, sections
+// "Тайлинг (Tiling)" and "Онлайн-Softmax"): Q, K and V are cut into tiles
+// that are staged on chip; each 128-row query tile meets every visible
+// 128-key tile in turn; per row the running max and running sum of
+// exponentials are updated and the accumulated output is rescaled when the
+// max grows, so the score matrix never leaves the chip and the result equals
+// the classical softmax.
+//
+// Blackwell mapping (the FlashAttention-4 article on smntcn.com describes the
+// ingredients: fully asynchronous fifth-generation tensor cores, 256 KB of
+// tensor memory per SM for intermediates, warps specialised into data
+// movers and MMA issuers, and exp computed partly in software because the
+// special-function unit scales slower than the tensor cores):
+//
+//   CTA = 512 threads, persistent (one per SM), one unit of work = one
+//   (batch, query head, 256-row query block) handled as two 128-row stages.
+//     warps 0-3   softmax, stage 0      (one thread per query row)
+//     warps 4-7   softmax, stage 1
+//     warps 8-11  correction + epilogue (rescale O when a row max grows;
+//                                        O / l -> bf16, LSE)
+//     warp 12     TMA producer          (Q per unit, K/V ring)
+//     warp 13     MMA issuer            (tcgen05.mma, one thread)
+//     warps 14-15 idle
+//   TMEM (512 columns x 128 lanes, fp32):
+//     [0,128)   S of stage 0; its first 64 columns are overwritten by P
+//               (bf16 pairs), the A operand of O += P V
+//     [128,256) S / P of stage 1
+//     [256, 256+d)       O of stage 0
+//     [256+d, 256+2d)    O of stage 1
+//   MMA issue order per key tile j (stages interleaved so one stage's
+//   softmax overlaps the other stage's GEMMs):
+//     ... PV0(j), S0(j+1), PV1(j), S1(j+1), PV0(j+1), ...
+//   Every mbarrier wait is bounded; on timeout the CTA stops cleanly and
+//   the per-device status word records it.
+#include <cuda_bf16.h>
+#include <cmath>
+
+#include "fa_internal.h"
+#include "sm103_math.cuh"
+#include "sm103_ptx.cuh"
+
+namespace fa {
+namespace fwd {
+
+constexpr int kThreads = 512;
+constexpr int kMaxSlots = 8;
+
+// Share of exponentials done by the polynomial: one column pair in every
+// kPolyEvery goes to the FMA pipes (0 = all on the special-function unit).
+#ifndef FA_POLY_EVERY
+#define FA_POLY_EVERY 0
+#endif
+constexpr int kPolyEvery = FA_POLY_EVERY;
+
+template <int D>
+struct Cfg {
+  static constexpr int kChunks = D / 64;          // 64-wide swizzle atoms along d
+  static constexpr int kTileBytes = 128 * D * 2;  // one 128-row tile of Q, K or V
+  static constexpr int kSlots = D == 128 ? 4 : 8;
+  static constexpr int kSmemDyn = (2 + kSlots) * kTileBytes + 1024;
+  static constexpr uint32_t kOCol0 = 256;
+};
+
+struct Params {
+  __nv_bfloat16* o;
+  float* lse;
+  int B, Hq, Hkv, Nq, Nk;
+  int group;
+  float scale_log2;
+  int n_mblocks;
+  int n_units;
+  unsigned long long wait_limit_ns;
+  int inject;
+  unsigned* status;
+};
+
+struct __align__(8) Ctl {
+  uint64_t q_full[2];
+  uint64_t q_empty;
+  uint64_t kv_full[kMaxSlots];
+  uint64_t kv_empty[kMaxSlots];
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t alpha_full[2];
+  uint64_t o_ready[2];
+  uint64_t o_full[2];
+  uint64_t stats_full[2];
+  uint64_t stats_empty[2];
+  uint64_t drain;
+  float alpha[2][128];
+  float stat_l[2][128];
+  float stat_m[2][128];
+  uint32_t tmem_base;
+  uint32_t abort;
+};
+
+struct Unit {
+  int b, h, kvh, row0;
+  int n[2];   // key tiles each stage visits
+  int nb;     // max(n[0], n[1])
+  bool rows[2];
+};
+
+template <bool CAUSAL>
+__device__ __forceinline__ Unit decode_unit(const Params& p, int u) {
+  Unit x;
+  const int bh_count = p.B * p.Hq;
+  const int r = u / bh_count;
+  const int bh = u - r * bh_count;
+  // causal: longest units (last query blocks) first
+  const int mb = CAUSAL ? (p.n_mblocks - 1 - r) : r;
+  x.b = bh / p.Hq;
+  x.h = bh - x.b * p.Hq;
+  x.kvh = x.h / p.group;
+  x.row0 = mb * 256;
+  const int off = p.Nk - p.Nq;
+  const int nkb = (p.Nk + 127) >> 7;
+#pragma unroll
+  for (int s = 0; s < 2; ++s) {
+    const int r0 = x.row0 + s * 128;
+    x.rows[s] = r0 < p.Nq;
+    if (!x.rows[s]) {
+      x.n[s] = 0;
+    } else if (!CAUSAL) {
+      x.n[s] = nkb;
+    } else {
+      const int rl = min(r0 + 127, p.Nq - 1);
+      const int kmax = min(rl + off, p.Nk - 1);
+      x.n[s] = kmax < 0 ? 0 : (kmax >> 7) + 1;
+    }
+  }
+  x.nb = max(x.n[0], x.n[1]);
+  return x;
+}
+
+// Static snake order over rounds of gridDim.x units (longest first when
+// causal): CTA c takes unit c in even rounds and G-1-c in odd rounds.
+__device__ __forceinline__ int unit_at(int round, int c) {
+  const int G = gridDim.x;
+  return round * G + ((round & 1) ? (G - 1 - c) : c);
+}
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const Params p) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ Ctl ctl;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;                          // 2 tiles
+  uint8_t* sKV = smem + 2 * C::kTileBytes;     // kSlots tiles
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int wg = warp >> 2;
+  volatile uint32_t* abort_flag = &ctl.abort;
+  const uint64_t LIM = p.wait_limit_ns;
+
+  if (threadIdx.x == 0) {
+    ctl.abort = 0;
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&ctl.q_full[s], 1);
+      mbar_init(&ctl.s_full[s], 1);
+      mbar_init(&ctl.p_full[s], 4);
+      mbar_init(&ctl.alpha_full[s], 4);
+      mbar_init(&ctl.o_ready[s], 4);
+      mbar_init(&ctl.o_full[s], 1);
+      mbar_init(&ctl.stats_full[s], 4);
+      mbar_init(&ctl.stats_empty[s], 4);
+    }
+    mbar_init(&ctl.q_empty, 1);
+    mbar_init(&ctl.drain, 1);
+    for (int i = 0; i < C::kSlots; ++i) {
+      mbar_init(&ctl.kv_full[i], 1);
+      mbar_init(&ctl.kv_empty[i], 1);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 13) {
+    tmem_alloc(&ctl.tmem_base, 512);
+    tmem_relinquish();
+  }
+  if (warp == 12 && lane == 0) {
+    prefetch_tmap(&tmQ);
+    prefetch_tmap(&tmK);
+    prefetch_tmap(&tmV);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl.tmem_base;
+
+  if (wg <= 1) {
+    // ------------------------------------------------------------ softmax
+    setmaxnreg_inc<176>();
+    const int s = wg;
+    const int row = ((warp & 3) << 5) + lane;
+    const uint32_t t_s = tmem + (uint32_t(warp & 3) << 21) + uint32_t(s * 128);  // lane quarter + S columns
+    uint32_t ph_s = 0, ph_se = 0;
+    const float sl = p.scale_log2;
+    bool ok = true;
+    for (int rnd = 0; ok; ++rnd) {
+      const int u = unit_at(rnd, blockIdx.x);
+      if (u >= p.n_units) break;
+      const Unit un = decode_unit<CAUSAL>(p, u);
+      const int n = un.n[s];
+      if (n == 0) continue;
+      const int rg = un.row0 + s * 128 + row;  // global query row
+      const int off = p.Nk - p.Nq;
+      float m_run = -INFINITY, l_run = 0.0f;
+      for (int j = 0; j < n; ++j) {
+        if (!mbar_wait_bounded(&ctl.s_full[s], ph_s, abort_flag, LIM)) { ok = false; break; }
+        ph_s ^= 1;
+        tc_fence_after();
+        uint32_t x[128];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(t_s + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&x[c * 32]));
+        tmem_wait_ld();
+        const int kb = j * 128;
+        const bool need_mask = (kb + 127 >= p.Nk) || (CAUSAL && kb + 127 > un.row0 + s * 128 + off);
+        if (need_mask) {
+          int lim = p.Nk - kb;
+          if (CAUSAL) lim = min(lim, rg + off + 1 - kb);
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (c >= lim) x[c] = f2u(-INFINITY);
+        }
+        float mA = -INFINITY, mB = -INFINITY, mC = -INFINITY, mD = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 128; c += 8) {
+          mA = fmax3(mA, u2f(x[c]), u2f(x[c + 1]));
+          mB = fmax3(mB, u2f(x[c + 2]), u2f(x[c + 3]));
+          mC = fmax3(mC, u2f(x[c + 4]), u2f(x[c + 5]));
+          mD = fmax3(mD, u2f(x[c + 6]), u2f(x[c + 7]));
+        }
+        const float mx = fmaxf(fmaxf(mA, mB), fmaxf(mC, mD));
+        const float m_new = fmaxf(m_run, mx * sl);
+        const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
+        const float alpha = ex2_mufu(m_run - m_use);
+        ctl.alpha[s][row] = alpha;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl.alpha_full[s]);
+
+        const uint64_t sl2 = pack2(sl, sl);
+        const uint64_t nm2 = pack2(-m_use, -m_use);
+        uint64_t acc0 = 0, acc1 = 0, acc2 = 0, acc3 = 0;
+        uint32_t pk[64];
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          uint64_t y = ffma2(pack2(u2f(x[2 * c]), u2f(x[2 * c + 1])), sl2, nm2);
+          float a, b;
+          unpack2(y, a, b);
+          if (kPolyEvery > 0 && (c % (kPolyEvery > 0 ? kPolyEvery : 1)) == (kPolyEvery - 1)) {
+            exp2_poly_pair(a, b);
+          } else {
+            a = ex2_mufu(a);
+            b = ex2_mufu(b);
+          }
+          const uint64_t pr = pack2(a, b);
+          if ((c & 3) == 0) acc0 = c == 0 ? pr : fadd2(acc0, pr);
+          if ((c & 3) == 1) acc1 = c == 1 ? pr : fadd2(acc1, pr);
+          if ((c & 3) == 2) acc2 = c == 2 ? pr : fadd2(acc2, pr);
+          if ((c & 3) == 3) acc3 = c == 3 ? pr : fadd2(acc3, pr);
+          pk[c] = pack_bf16x2(a, b);
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_st16(t_s + c * 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[c * 16]));
+        const uint64_t acc = fadd2(fadd2(acc0, acc1), fadd2(acc2, acc3));
+        float la, lb;
+        unpack2(acc, la, lb);
+        l_run = fmaf(l_run, alpha, la + lb);
+        m_run = m_new;
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl.p_full[s]);
+      }
+      if (!ok) break;
+      // final row statistics for the epilogue
+      if (!mbar_wait_bounded(&ctl.stats_empty[s], ph_se ^ 1, abort_flag, LIM)) { ok = false; break; }
+      ph_se ^= 1;
+      ctl.stat_l[s][row] = l_run;
+      ctl.stat_m[s][row] = m_run;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl.stats_full[s]);
+    }
+  } else if (wg == 2) {
+    // ------------------------------------------------ correction + epilogue
+    setmaxnreg_dec<80>();
+    const int wq = warp & 3;
+    const int row = (wq << 5) + lane;
+    const uint32_t t_lane = tmem + (uint32_t(wq) << 21);
+    uint32_t ph_a[2] = {0, 0}, ph_st[2] = {0, 0}, ph_of[2] = {0, 0};
+    bool ok = true;
+    for (int rnd = 0; ok; ++rnd) {
+      const int u = unit_at(rnd, blockIdx.x);
+      if (u >= p.n_units) break;
+      const Unit un = decode_unit<CAUSAL>(p, u);
+      for (int j = 0; j < un.nb && ok; ++j) {
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+          if (j >= un.n[s]) continue;
+          if (!mbar_wait_bounded(&ctl.alpha_full[s], ph_a[s], abort_flag, LIM)) { ok = false; break; }
+          ph_a[s] ^= 1;
+          const float a = ctl.alpha[s][row];
+          if (j > 0 && __any_sync(0xffffffffu, a < 1.0f)) {
+            tc_fence_after();
+            const uint32_t t_o = t_lane + C::kOCol0 + uint32_t(s * D);
+            const uint64_t a2 = pack2(a, a);
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t v[32];
+              tmem_ld32(t_o + c * 32, v);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; i += 2) {
+                float lo, hi;
+                unpack2(fmul2(pack2(u2f(v[i]), u2f(v[i + 1])), a2), lo, hi);
+                v[i] = f2u(lo);
+                v[i + 1] = f2u(hi);
+              }
+              tmem_st32(t_o + c * 32, v);
+            }
+            tmem_wait_st();
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ctl.o_ready[s]);
+        }
+      }
+      if (!ok) break;
+      // epilogue: O / l -> bf16, LSE
+#pragma unroll 1
+      for (int s = 0; s < 2; ++s) {
+        if (!un.rows[s]) continue;
+        const int rg = un.row0 + s * 128 + row;
+        const bool valid = rg < p.Nq;
+        __nv_bfloat16* dst = p.o + ((size_t(un.b) * p.Nq + rg) * p.Hq + un.h) * D;
+        float* lse_dst = p.lse + (size_t(un.b) * p.Hq + un.h) * p.Nq + rg;
+        if (un.n[s] == 0) {
+          if (valid) {
+            const uint4 z = make_uint4(0, 0, 0, 0);
+            for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4*>(dst)[c] = z;
+            *lse_dst = -INFINITY;
+          }
+          continue;
+        }
+        if (!mbar_wait_bounded(&ctl.stats_full[s], ph_st[s], abort_flag, LIM)) { ok = false; break; }
+        ph_st[s] ^= 1;
+        const float l = ctl.stat_l[s][row];
+        const float m = ctl.stat_m[s][row];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl.stats_empty[s]);
+        if (!mbar_wait_bounded(&ctl.o_full[s], ph_of[s], abort_flag, LIM)) { ok = false; break; }
+        ph_of[s] ^= 1;
+        tc_fence_after();
+        const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+        const uint32_t t_o = t_lane + C::kOCol0 + uint32_t(s * D);
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(t_o + c * 32, v);
+          tmem_wait_ld();
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(u2f(v[2 * i]) * inv, u2f(v[2 * i + 1]) * inv);
+          if (valid) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          }
+        }
+        if (valid) *lse_dst = l > 0.0f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+        tc_fence_before();
+      }
+    }
+  } else {
+    setmaxnreg_dec<80>();
+  }
+  if (warp == 12) {
+    // ------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      uint32_t kv_it = 0, ph_qe = 0;
+      bool first = true, ok = true;
+      bool injected = false;
+      for (int rnd = 0; ok; ++rnd) {
+        const int u = unit_at(rnd, blockIdx.x);
+        if (u >= p.n_units) break;
+        const Unit un = decode_unit<CAUSAL>(p, u);
+        if (un.nb == 0) continue;
+        if (!first) {
+          if (!mbar_wait_bounded(&ctl.q_empty, ph_qe, abort_flag, LIM)) { ok = false; break; }
+          ph_qe ^= 1;
+        }
+        first = false;
+        for (int s = 0; s < 2; ++s) {
+          if (un.n[s] == 0) continue;
+          mbar_arrive_expect_tx(&ctl.q_full[s], C::kTileBytes);
+#pragma unroll
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_load_4d(sQ + s * C::kTileBytes + c * 16384, &tmQ, &ctl.q_full[s], c * 64, un.h, un.row0 + s * 128,
+                        un.b);
+        }
+        for (int j = 0; j < un.nb && ok; ++j) {
+#pragma unroll 1
+          for (int t = 0; t < 2; ++t) {
+            const uint32_t slot = kv_it % C::kSlots;
+            const uint32_t ph = ((kv_it / C::kSlots) & 1) ^ 1;
+            if (!mbar_wait_bounded(&ctl.kv_empty[slot], ph, abort_flag, LIM)) { ok = false; break; }
+            ++kv_it;
+            if (p.inject == 1 && !injected) {  // test hook: never deliver this tile
+              injected = true;
+              continue;
+            }
+            mbar_arrive_expect_tx(&ctl.kv_full[slot], C::kTileBytes);
+            const CUtensorMap* map = t == 0 ? &tmK : &tmV;
+#pragma unroll
+            for (int c = 0; c < C::kChunks; ++c)
+              tma_load_4d(sKV + slot * C::kTileBytes + c * 16384, map, &ctl.kv_full[slot], c * 64, un.kvh, j * 128,
+                          un.b);
+          }
+        }
+      }
+      if (*abort_flag) {
+        // let copies already in flight land before shared memory is released
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 1000000ull) __nanosleep(1000);
+      }
+    }
+  } else if (warp == 13) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16_f32(128, 128, 0, 0);
+      constexpr uint32_t idPV = idesc_bf16_f32(128, D, 0, 1);
+      const uint32_t sQa = smem_u32(sQ), sKVa = smem_u32(sKV);
+      uint32_t kv_it = 0, ph_q[2] = {0, 0}, ph_p[2] = {0, 0}, ph_o[2] = {0, 0};
+      bool ok = true;
+      auto issue_S = [&](int s, uint32_t kslot) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
+          const uint64_t ad = sdesc_sw128(sQa + s * C::kTileBytes + koff, 16, 1024);
+          const uint64_t bd = sdesc_sw128(sKVa + kslot * C::kTileBytes + koff, 16, 1024);
+          mma_ss(tmem + uint32_t(s * 128), ad, bd, idS, kk > 0);
+        }
+      };
+      auto issue_PV = [&](int s, uint32_t vslot, bool acc) {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t bd = sdesc_sw128(sKVa + vslot * C::kTileBytes + kk * 2048, 16384, 1024);
+          mma_ts(tmem + C::kOCol0 + uint32_t(s * D), tmem + uint32_t(s * 128 + kk * 8), bd, idPV,
+                 (acc || kk > 0) ? 1u : 0u);
+        }
+      };
+      auto wait_kv = [&](uint32_t& slot) -> bool {
+        slot = kv_it % C::kSlots;
+        const bool r = mbar_wait_bounded(&ctl.kv_full[slot], (kv_it / C::kSlots) & 1, abort_flag, LIM);
+        ++kv_it;
+        return r;
+      };
+      for (int rnd = 0; ok; ++rnd) {
+        const int u = unit_at(rnd, blockIdx.x);
+        if (u >= p.n_units) break;
+        const Unit un = decode_unit<CAUSAL>(p, u);
+        if (un.nb == 0) continue;
+        for (int s = 0; s < 2 && ok; ++s) {
+          if (un.n[s] == 0) continue;
+          ok = mbar_wait_bounded(&ctl.q_full[s], ph_q[s], abort_flag, LIM);
+          ph_q[s] ^= 1;
+        }
+        uint32_t kslot = 0, vslot = 0;
+        if (!ok || !wait_kv(kslot)) { ok = false; break; }
+        tc_fence_after();
+        for (int s = 0; s < 2; ++s) {
+          if (un.n[s] == 0) continue;
+          issue_S(s, kslot);
+          mma_commit(&ctl.s_full[s]);
+        }
+        mma_commit(&ctl.kv_empty[kslot]);
+        if (un.nb == 1) mma_commit(&ctl.q_empty);
+        for (int j = 0; j < un.nb && ok; ++j) {
+          if (!wait_kv(vslot)) { ok = false; break; }
+          const bool nxt = j + 1 < un.nb;
+          if (nxt && !wait_kv(kslot)) { ok = false; break; }
+          for (int s = 0; s < 2; ++s) {
+            if (j >= un.n[s]) continue;
+            if (!mbar_wait_bounded(&ctl.p_full[s], ph_p[s], abort_flag, LIM)) { ok = false; break; }
+            ph_p[s] ^= 1;
+            if (!mbar_wait_bounded(&ctl.o_ready[s], ph_o[s], abort_flag, LIM)) { ok = false; break; }
+            ph_o[s] ^= 1;
+            tc_fence_after();
+            issue_PV(s, vslot, j > 0);
+            if (j == un.n[s] - 1) mma_commit(&ctl.o_full[s]);
+            if (j + 1 < un.n[s]) {
+              issue_S(s, kslot);
+              mma_commit(&ctl.s_full[s]);
+            }
+          }
+          if (!ok) break;
+          mma_commit(&ctl.kv_empty[vslot]);
+          if (nxt) mma_commit(&ctl.kv_empty[kslot]);
+          if (j + 2 == un.nb) mma_commit(&ctl.q_empty);
+        }
+      }
+      if (*abort_flag) {
+        // drain the tensor pipe before TMEM is released
+        mma_commit(&ctl.drain);
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(smem_u32(&ctl.drain), 0) && globaltimer_ns() - t0 < 100000000ull) {
+        }
+      }
+    }
+  }
+
+  // ------------------------------------------------------------- teardown
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 13) tmem_dealloc(tmem, 512);
+  if (threadIdx.x == 0 && ctl.abort) atomicOr(p.status, kDevTimeout);
+}
+
+template <int D, bool CAUSAL>
+cudaError_t launch_t(const Problem& pb, void* o, float* lse, cudaStream_t stream) {
+  CUtensorMap mq, mk, mv;
+  if (!make_bshd_map(&mq, pb.q, pb.B, pb.Nq, pb.Hq, D, 128) || !make_bshd_map(&mk, pb.k, pb.B, pb.Nk, pb.Hkv, D, 128) ||
+      !make_bshd_map(&mv, pb.v, pb.B, pb.Nk, pb.Hkv, D, 128))
+    return cudaErrorInvalidValue;
+  Params p;
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.B = pb.B;
+  p.Hq = pb.Hq;
+  p.Hkv = pb.Hkv;
+  p.Nq = pb.Nq;
+  p.Nk = pb.Nk;
+  p.group = pb.Hq / pb.Hkv;
+  p.scale_log2 = pb.scale * 1.4426950408889634f;
+  p.n_mblocks = (pb.Nq + 255) / 256;
+  p.n_units = p.n_mblocks * pb.B * pb.Hq;
+  const DebugCfg dc = debug_cfg();
+  p.wait_limit_ns = dc.wait_limit_ns;
+  p.inject = dc.inject;
+  p.status = status_word();
+  if (!p.status) return cudaErrorMemoryAllocation;
+  auto kern = fa_fwd_kernel<D, CAUSAL>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmemDyn);
+  if (e != cudaSuccess) return e;
+  const int grid = p.n_units < num_sms() ? p.n_units : num_sms();
+  kern<<<grid, kThreads, Cfg<D>::kSmemDyn, stream>>>(mq, mk, mv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace fwd
+
+cudaError_t launch_fwd(const Problem& p, void* o, float* lse, cudaStream_t stream) {
+  if (p.d == 128) return p.causal ? fwd::launch_t<128, true>(p, o, lse, stream) : fwd::launch_t<128, false>(p, o, lse, stream);
+  return p.causal ? fwd::launch_t<64, true>(p, o, lse, stream) : fwd::launch_t<64, false>(p, o, lse, stream);
+}
+
+}  // namespace fa

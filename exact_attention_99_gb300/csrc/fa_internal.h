@@ -1,0 +1,43 @@
+// Host-side declarations shared by the translation units of libfa.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace fa {
+
+// Status bits written by kernels into the per-device status word.
+constexpr unsigned kDevTimeout = 1u;
+
+struct Problem {
+  const void* q;
+  const void* k;
+  const void* v;
+  int B, Hq, Hkv, Nq, Nk, d;
+  float scale;
+  int causal;
+};
+
+struct DebugCfg {
+  unsigned long long wait_limit_ns;
+  int inject;
+};
+DebugCfg debug_cfg();
+
+// Device properties cached per device.
+int num_sms();
+
+// Per-device status word (device pointer), created on first use.
+unsigned* status_word();
+
+// 4-D bf16 tensor map over a BSHD tensor [B, N, H, d]: dims {d, H, N, B},
+// box {64, 1, box_rows, 1}, 128-byte swizzle, zero fill out of range.
+bool make_bshd_map(CUtensorMap* m, const void* base, int B, int N, int H, int d, int box_rows);
+
+// Launchers. Return a cudaError_t (cudaSuccess on success).
+cudaError_t launch_fwd(const Problem& p, void* o, float* lse, cudaStream_t stream);
+cudaError_t launch_bwd(const Problem& p, const void* o, const float* lse, const void* dout, void* dq, void* dk,
+                       void* dv, float* dq_acc, float* delta, cudaStream_t stream);
+cudaError_t launch_debug_exp2(const float* x, float* y, int n, int mode, cudaStream_t stream);
+
+}  // namespace fa

@@ -1,0 +1,110 @@
+/*
+ * fa.h — C ABI of the exact-attention library for one NVIDIA GB300 (sm_103a).
+ *
+ * What is computed. Exact scaled-dot-product attention
+ *     O = softmax(scale * Q K^T [+ causal mask]) V
+ * (the post "FlashAttention v1", deep_school #630, section "Проблема
+ * базового attention"), evaluated tile by tile with online softmax so the
+ * Nq x Nk score matrix never reaches device memory (same post, sections
+ * "Тайлинг (Tiling)" and "Онлайн-Softmax"). The result equals the classical
+ * softmax up to floating-point rounding. The backward pass recomputes the
+ * probabilities from the saved log-sum-exp instead of storing them (the
+ * FlashAttention-3 summary on news.hada.io, section "Resumo do
+ * FlashAttention": tiling and recomputation).
+ *
+ * Conventions shared by every call.
+ *   Layout   : contiguous, head dimension innermost ("BSHD").
+ *              q, o, dout, dq : [B, Nq, Hq, d]   bf16
+ *              k, v, dk, dv   : [B, Nk, Hkv, d]  bf16
+ *              lse            : [B, Hq, Nq]      fp32, natural log:
+ *                               lse[b,h,i] = ln sum_j exp(scale * q_i . k_j)
+ *                               over the keys j visible to row i.
+ *   GQA      : query head h reads kv head h / (Hq / Hkv); Hq % Hkv == 0.
+ *   Causal   : causal = 1 hides key j from query i when j > i + (Nk - Nq)
+ *              (bottom-right alignment; with Nq == Nk this is j > i). A row
+ *              that sees no key gets o = 0 and lse = -inf.
+ *   Sizes    : B, Hq, Hkv, Nq, Nk >= 1; d in {64, 128}; scale finite and
+ *              > 0; every element count and B*Hq*Nq*d fit in int32 indices
+ *              per the limits checked below.
+ *   Pointers : device pointers owned by the caller, 16-byte aligned. The
+ *              library keeps no pointer after a call returns.
+ *   Stream   : `stream` is a cudaStream_t (NULL = legacy default stream).
+ *              Calls only enqueue work; outputs are valid once the stream
+ *              has been synchronised. The calls are not re-entrant on one
+ *              stream from several host threads.
+ *   Errors   : argument errors are detected on the host before anything is
+ *              enqueued and return FA_ERR_INVALID_ARG / FA_ERR_UNSUPPORTED.
+ *              A failed launch returns FA_ERR_LAUNCH. Every wait inside the
+ *              kernels is bounded; a wait that runs out stops the kernel and
+ *              records FA_ERR_TIMEOUT in a per-device status word that
+ *              fa_get_status() returns.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size, bad scale or flag */
+  FA_ERR_UNSUPPORTED = 2, /* valid request this build does not serve (e.g. d not in {64,128}) */
+  FA_ERR_ALLOC = 3,       /* device workspace allocation failed */
+  FA_ERR_LAUNCH = 4,      /* a CUDA call or kernel launch failed */
+  FA_ERR_TIMEOUT = 5,     /* a bounded device-side wait ran out (reported by fa_get_status) */
+  FA_ERR_NO_DEVICE = 6    /* no usable sm_103 device is current */
+} fa_status;
+
+/*
+ * fa_fwd — forward pass.
+ *   in : q [B,Nq,Hq,d], k [B,Nk,Hkv,d], v [B,Nk,Hkv,d]   (bf16, device)
+ *   out: o [B,Nq,Hq,d] (bf16), lse [B,Hq,Nq] (fp32)        (device)
+ * Needs no device workspace. All outputs are fully written.
+ */
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Nq, int Nk,
+           int d, float scale, int causal, void* stream);
+
+/*
+ * fa_bwd — backward pass for L = sum(dout * o).
+ *   in : q, k, v, o (bf16), lse (fp32, as written by fa_fwd for the same
+ *        inputs), dout [B,Nq,Hq,d] (bf16)
+ *   out: dq [B,Nq,Hq,d], dk [B,Nk,Hkv,d], dv [B,Nk,Hkv,d] (bf16), fully written.
+ * Allocates its fp32 workspace (dq accumulator, row terms D_i) with the
+ * stream-ordered allocator on `stream` and frees it on the same stream;
+ * returns FA_ERR_ALLOC if that fails. GQA gradients of dk/dv are summed over
+ * the query heads of each group inside the kernel.
+ */
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout, void* dq,
+           void* dk, void* dv, int B, int Hq, int Hkv, int Nq, int Nk, int d, float scale, int causal,
+           void* stream);
+
+/*
+ * fa_get_status — synchronises `stream`, then returns and clears the
+ * current device's status word: FA_OK, or FA_ERR_TIMEOUT if any kernel of
+ * this library gave up on a bounded wait since the last call. A CUDA error
+ * seen while synchronising is returned as FA_ERR_LAUNCH.
+ */
+int fa_get_status(void* stream);
+
+/* fa_status_string — static, human-readable name of a status code. */
+const char* fa_status_string(int status);
+
+/*
+ * Test hooks (not for production use).
+ * fa_debug_set — wait_limit_ns: per-wait time limit of every kernel (0
+ *   restores the default of 2 s). inject: 0 = off; 1 = the forward producer
+ *   never issues its first K-tile load, so the consumer's bounded wait must
+ *   run out and the kernel must report FA_ERR_TIMEOUT and exit cleanly.
+ *   Process-wide; not thread-safe.
+ * fa_debug_exp2 — y[i] = 2^x[i] for n device floats, evaluated by the
+ *   kernels' own device routine: mode 0 = ex2.approx on the special-function
+ *   unit, mode 1 = the fitted polynomial on the FMA pipes.
+ */
+int fa_debug_set(unsigned long long wait_limit_ns, int inject);
+int fa_debug_exp2(const float* x, float* y, int n, int mode, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FA_H_ */

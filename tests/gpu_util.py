@@ -1,0 +1,40 @@
+"""Helpers shared by the GPU parity tests (comparison and tolerances)."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+# Tolerances for bf16 I/O with fp32 accumulation: max-abs 2e-2 and mean-abs
+# 2e-3 on O, dQ, dK, dV; 1e-3 absolute on LSE (natural log).
+TOL_MAX = 2e-2
+TOL_MEAN = 2e-3
+TOL_LSE = 1e-3
+
+
+def to64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().double().cpu().numpy()
+
+
+def rounding_floor(ref: np.ndarray) -> float:
+    """max |bf16(ref) - ref|: the part of the error output rounding alone causes."""
+    r = torch.from_numpy(ref).to(torch.bfloat16).double().numpy()
+    return float(np.abs(r - ref).max()) if ref.size else 0.0
+
+
+def assert_close(name: str, got: np.ndarray, ref: np.ndarray, max_tol=TOL_MAX, mean_tol=TOL_MEAN):
+    assert got.shape == ref.shape, (name, got.shape, ref.shape)
+    if ref.size == 0:
+        return
+    fin = np.isfinite(ref)
+    assert np.array_equal(np.isfinite(got), fin), f"{name}: non-finite pattern differs"
+    diff = np.abs(got[fin] - ref[fin])
+    mx, mean = float(diff.max()) if diff.size else 0.0, float(diff.mean()) if diff.size else 0.0
+    assert mx <= max_tol and mean <= mean_tol, (
+        f"{name}: max-abs {mx:.3e} (tol {max_tol}), mean-abs {mean:.3e} (tol {mean_tol}), "
+        f"bf16 rounding floor {rounding_floor(ref[fin]):.3e}")
+    if not fin.all():
+        assert np.array_equal(got[~fin], ref[~fin]), f"{name}: infinite entries differ"
+
+
+def assert_lse(got: np.ndarray, ref: np.ndarray, tol=TOL_LSE):
+    assert_close("lse", got, ref, max_tol=tol, mean_tol=tol)

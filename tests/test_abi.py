@@ -1,0 +1,100 @@
+"""Host-only checks of the C ABI: the library builds, loads without a GPU,
+exports every function include/fa.h declares, and rejects bad arguments on
+the host before any device work (no GPU needed, nothing is launched)."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def fa():
+    import __graft_entry__
+    __graft_entry__.build()
+    import exact_attention_99_gb300 as m
+    m.lib()
+    return m
+
+
+def declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(fa_\w+)\s*\(", text, flags=re.M))
+    return names
+
+
+def test_header_exports(fa):
+    names = declared_functions()
+    assert {"fa_fwd", "fa_bwd", "fa_get_status", "fa_status_string"} <= names
+    L = ctypes.CDLL(fa.LIB_PATH)
+    for n in sorted(names):
+        assert hasattr(L, n), f"{n} declared in include/ but not exported"
+
+
+def test_status_strings(fa):
+    for code, name in fa.STATUS.items():
+        assert fa.fa_status_string(code) == name
+    assert fa.fa_status_string(99) == "FA_ERR_UNKNOWN"
+
+
+GOOD = dict(B=1, Hq=4, Hkv=2, Nq=64, Nk=64, d=128, scale=0.125, causal=1)
+P16 = 1 << 20  # any 16-byte aligned non-null address: validation fails before it is touched
+
+
+def fwd(fa, ptrs=(P16,) * 5, **kw):
+    a = dict(GOOD, **kw)
+    return fa.fa_fwd(*ptrs, a["B"], a["Hq"], a["Hkv"], a["Nq"], a["Nk"], a["d"], a["scale"], a["causal"], 0)
+
+
+def bwd(fa, ptrs=(P16,) * 9, **kw):
+    a = dict(GOOD, **kw)
+    return fa.fa_bwd(*ptrs, a["B"], a["Hq"], a["Hkv"], a["Nq"], a["Nk"], a["d"], a["scale"], a["causal"], 0)
+
+
+@pytest.mark.parametrize("call", [fwd, bwd])
+@pytest.mark.parametrize("bad,code", [
+    (dict(d=96), 2), (dict(d=256), 2), (dict(d=0), 1), (dict(Hq=3, Hkv=2), 1), (dict(B=0), 1),
+    (dict(Nq=0), 1), (dict(Nk=-5), 1), (dict(Hkv=0), 1), (dict(causal=2), 1), (dict(scale=0.0), 1),
+    (dict(scale=-1.0), 1), (dict(scale=float("nan")), 1), (dict(scale=float("inf")), 1),
+    (dict(Nq=1 << 29), 2),
+])
+def test_bad_sizes_rejected_on_host(fa, call, bad, code):
+    assert call(fa, **bad) == code
+
+
+@pytest.mark.parametrize("which", range(5))
+def test_bad_pointers_fwd(fa, which):
+    for bad in (0, P16 + 8):  # null, misaligned
+        ptrs = [P16] * 5
+        ptrs[which] = bad
+        assert fwd(fa, ptrs=tuple(ptrs)) == 1
+
+
+@pytest.mark.parametrize("which", range(9))
+def test_bad_pointers_bwd(fa, which):
+    for bad in (0, P16 + 2):
+        ptrs = [P16] * 9
+        ptrs[which] = bad
+        assert bwd(fa, ptrs=tuple(ptrs)) == 1
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
+def test_no_device_fails_loudly(fa):
+    # valid arguments without a usable device: an error, never a silent fallback
+    assert fwd(fa) == 6
+    assert bwd(fa) == 6
+    with pytest.raises((RuntimeError, ValueError)):
+        fa.forward(torch.zeros(1, 8, 1, 64, dtype=torch.bfloat16), torch.zeros(1, 8, 1, 64, dtype=torch.bfloat16),
+                   torch.zeros(1, 8, 1, 64, dtype=torch.bfloat16))
+
+
+def test_debug_set_validates(fa):
+    assert fa.fa_debug_set(0, 2) == 1
+    assert fa.fa_debug_set(0, 0) == 0

@@ -1,0 +1,170 @@
+"""Forward parity on a GB300: the CUDA path (through the C ABI) against the
+fp64 CPU oracle on identical seeded bf16 inputs."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from oracle import attn_ref
+from tests.gpu_util import assert_close, assert_lse, to64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fa():
+    import __graft_entry__
+    __graft_entry__.build()
+    import exact_attention_99_gb300 as m
+    assert torch.cuda.is_available(), "GPU tests need a GPU"
+    m.fa_debug_set(0, 0)
+    return m
+
+
+def run_case(fa, B, Hq, Hkv, Nq, Nk, d, causal, seed, sigma_qk=1.0, rows=None):
+    x = workloads.make_inputs(B, Hq, Hkv, Nq, Nk, d, seed, sigma_qk=sigma_qk)
+    q, k, v = (x[n].cuda() for n in ("q", "k", "v"))
+    scale = 1.0 / math.sqrt(d)
+    o, lse = fa.forward(q, k, v, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    assert fa.fa_get_status() == 0
+    qn, kn, vn = (x[n].double().numpy() for n in ("q", "k", "v"))
+    ro, rlse = attn_ref.forward(qn, kn, vn, scale, causal, rows=rows)
+    go, glse = to64(o), to64(lse)
+    if rows is not None:
+        go, glse = go[:, rows], glse[:, :, rows]
+    assert_close("o", go, ro)
+    assert_lse(glse, rlse)
+    return o, lse
+
+
+SMALL = [
+    # B, Hq, Hkv, Nq, Nk, d
+    (1, 2, 2, 1, 1, 64),
+    (1, 2, 1, 17, 17, 128),
+    (2, 3, 3, 128, 128, 64),
+    (1, 4, 2, 129, 129, 128),
+    (1, 2, 2, 255, 255, 64),
+    (2, 2, 2, 256, 256, 128),
+    (1, 4, 1, 300, 300, 128),
+    (1, 2, 2, 513, 513, 64),
+    (1, 2, 2, 100, 700, 128),   # Nq < Nk
+    (1, 2, 2, 700, 100, 128),   # Nq > Nk: causal rows with no visible key
+    (1, 1, 1, 1, 1000, 64),
+]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", SMALL, ids=lambda s: "x".join(map(str, s)))
+def test_small_shapes(fa, shape, causal):
+    B, Hq, Hkv, Nq, Nk, d = shape
+    run_case(fa, B, Hq, Hkv, Nq, Nk, d, causal, seed=hash((shape, causal)) % 10000)
+
+
+def test_workload_small_full(fa):
+    w = workloads.WORKLOADS[0]
+    run_case(fa, w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.d, w.causal, w.seed, w.sigma_qk)
+
+
+@pytest.mark.parametrize("idx", [1, 2, 3])
+def test_workload_full_size_sampled(fa, idx):
+    """Full-size run in the benchmark's launch configuration; the oracle
+    checks sampled rows of a few heads (every row of those heads would take
+    minutes in fp64)."""
+    w = workloads.WORKLOADS[idx]
+    x = workloads.workload_inputs(w)
+    q, k, v = (x[n].cuda() for n in ("q", "k", "v"))
+    o, lse = fa.forward(q, k, v, causal=w.causal, scale=w.scale)
+    torch.cuda.synchronize()
+    assert fa.fa_get_status() == 0
+    rng = np.random.default_rng(w.seed)
+    rows = np.unique(np.concatenate([rng.choice(w.Nq, 96, replace=False), [0, 1, 127, 128, 255, w.Nq - 1]]))
+    heads = [(0, 0), (w.B - 1, w.Hq - 1), (w.B // 2, w.Hq // 2)]
+    go, glse = to64(o), to64(lse)
+    for b, h in heads:
+        kv = h // (w.Hq // w.Hkv)
+        qn = x["q"][b:b + 1, :, h:h + 1].double().numpy()
+        kn = x["k"][b:b + 1, :, kv:kv + 1].double().numpy()
+        vn = x["v"][b:b + 1, :, kv:kv + 1].double().numpy()
+        ro, rlse = attn_ref.forward(qn, kn, vn, w.scale, w.causal, rows=rows)
+        assert_close(f"o[b{b},h{h}]", go[b:b + 1, rows, h:h + 1], ro)
+        assert_lse(glse[b:b + 1, h:h + 1, rows], rlse)
+    # properties that hold at any size
+    assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+
+
+def test_constant_v_identity(fa):
+    B, H, N, d = 1, 2, 333, 128
+    x = workloads.make_inputs(B, H, H, N, N, d, seed=5, sigma_qk=2.0)
+    v0 = torch.randn(d).to(torch.bfloat16)
+    v = v0.expand(B, N, H, d).contiguous()
+    for causal in (False, True):
+        o, _ = fa.forward(x["q"].cuda(), x["k"].cuda(), v.cuda(), causal=causal)
+        torch.cuda.synchronize()
+        err = (o.double().cpu() - v0.double().expand(B, N, H, d)).abs().max().item()
+        assert err <= 2e-2, err
+
+
+def test_zero_q_mean(fa):
+    B, H, N, d = 1, 2, 260, 64
+    x = workloads.make_inputs(B, H, H, N, N, d, seed=6)
+    q = torch.zeros_like(x["q"])
+    o, lse = fa.forward(q.cuda(), x["k"].cuda(), x["v"].cuda(), causal=True)
+    torch.cuda.synchronize()
+    vc = x["v"].double().cumsum(dim=1) / torch.arange(1, N + 1, dtype=torch.float64)[None, :, None, None]
+    assert (o.double().cpu() - vc).abs().max().item() <= 2e-2
+    want = torch.log(torch.arange(1, N + 1, dtype=torch.float64))
+    assert (lse.double().cpu() - want[None, None]).abs().max().item() <= 1e-3
+
+
+def test_deterministic_and_offset_invariant(fa):
+    B, Hq, Hkv, N, d = 2, 4, 2, 384, 128
+    x = workloads.make_inputs(B, Hq, Hkv, N, N, d, seed=9)
+    q, k, v = (x[n].cuda() for n in ("q", "k", "v"))
+    o1, l1 = fa.forward(q, k, v, causal=True)
+    o2, l2 = fa.forward(q, k, v, causal=True)
+    # same tensors placed at a 16-byte-aligned offset inside larger buffers
+    pad = 8
+    bufs = []
+    for t in (q, k, v):
+        big = torch.empty(t.numel() + pad, dtype=t.dtype, device=t.device)
+        big[pad:].copy_(t.reshape(-1))
+        bufs.append(big[pad:].view(t.shape))
+    o3, l3 = fa.forward(*bufs, causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    assert torch.equal(o1, o3) and torch.equal(l1, l3)
+
+
+def test_bounded_wait_reports_timeout(fa):
+    """The producer withholds one tile; the consumer's bounded wait must run
+    out, the kernel must exit and report FA_ERR_TIMEOUT, and the context must
+    stay usable."""
+    B, H, N, d = 1, 1, 256, 64
+    x = workloads.make_inputs(B, H, H, N, N, d, seed=11)
+    q, k, v = (x[n].cuda() for n in ("q", "k", "v"))
+    assert fa.fa_get_status() == 0
+    assert fa.fa_debug_set(20_000_000, 1) == 0
+    try:
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, N), device="cuda", dtype=torch.float32)
+        assert fa.fa_fwd(q, k, v, o, lse, B, H, H, N, N, d, d ** -0.5, 0) == 0
+        assert fa.fa_get_status() == 5
+    finally:
+        fa.fa_debug_set(0, 0)
+    run_case(fa, B, H, H, N, N, d, False, seed=11)
+
+
+def test_debug_exp2(fa):
+    x = torch.linspace(-130.0, 0.0, 1 << 16, device="cuda", dtype=torch.float32)
+    want = torch.exp2(x.double())
+    for mode in (0, 1):
+        y = torch.empty_like(x)
+        assert fa.fa_debug_exp2(x, y, x.numel(), mode) == 0
+        torch.cuda.synchronize()
+        ok = x > -126
+        rel = ((y.double() - want) / want)[ok].abs()
+        assert rel.max().item() < (2e-6 if mode == 0 else 1e-4), (mode, rel.max().item())
+        assert y[x <= -127.5].abs().max().item() < 1e-37
