@@ -163,17 +163,13 @@ extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o
   st = check_device();
   if (st != FA_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const size_t acc_bytes = sizeof(float) * size_t(B) * Nq * Hq * d;
-  const size_t delta_bytes = sizeof(float) * size_t(B) * Hq * Nq;
+  Problem p{q, k, v, B, Hq, Hkv, Nq, Nk, d, scale, causal};
   void* ws = nullptr;
-  if (cudaMallocAsync(&ws, acc_bytes + delta_bytes, s) != cudaSuccess) {
+  if (cudaMallocAsync(&ws, bwd_workspace_bytes(p), s) != cudaSuccess) {
     cudaGetLastError();
     return FA_ERR_ALLOC;
   }
-  Problem p{q, k, v, B, Hq, Hkv, Nq, Nk, d, scale, causal};
-  float* dq_acc = static_cast<float*>(ws);
-  float* delta = reinterpret_cast<float*>(static_cast<char*>(ws) + acc_bytes);
-  const cudaError_t e = launch_bwd(p, o, lse, dout, dq, dk, dv, dq_acc, delta, s);
+  const cudaError_t e = launch_bwd(p, o, lse, dout, dq, dk, dv, static_cast<float*>(ws), s);
   const cudaError_t f = cudaFreeAsync(ws, s);
   if (e != cudaSuccess || f != cudaSuccess) return FA_ERR_LAUNCH;
   return FA_OK;

@@ -1,10 +1,641 @@
-// Backward pass of exact attention on sm_103a (placeholder until the
-// tcgen05 backward lands).
+// Backward pass of exact attention on sm_103a.
+//
+// Method: the probabilities are recomputed tile by tile from the saved
+// log-sum-exp instead of being stored (the FlashAttention-3 summary on
+// news.hada.io, section "Resumo do FlashAttention": tiling and
+// recomputation), and the intermediates of the five GEMMs stay in tensor
+// memory to cut shared-memory traffic (the FlashAttention-4 article on
+// smntcn.com: backward is bound by shared-memory traffic; intermediates are
+// kept in the 256 KB of tensor memory per SM).
+//
+// Gradients of L = sum(dO * O) with P = softmax(scale * Q K^T):
+//   dV = P^T dO,  dP = dO V^T,  D_i = sum_c dO_ic O_ic,  dS = P o (dP - D),
+//   dQ = scale * dS K,  dK = scale * dS^T Q.
+//
+// Kernels:
+//   bwd_pre  : D_i and LSE * log2(e) per query row (padded to whole tiles),
+//              zero the fp32 dQ accumulator.
+//   bwd_main : one CTA per (batch, kv head, 128-key tile); loops over the
+//              query heads of the GQA group x 128-row query tiles.
+//     warps 0-3  compute: one thread per key row; P^T = 2^(S^T*scale*log2e -
+//                LSE*log2e), dS^T = P^T o (dP^T - D)
+//     warps 4-7  dQ drain (TMEM -> fp32 reductions into the accumulator) and
+//                the dK/dV epilogue
+//     warp 8     TMA producer, warp 9 MMA issuer, warps 10-11 idle
+//     TMEM: S^T [0,128) with P^T (bf16) over its first 64 columns;
+//           dP^T [128,256), reused for dQ^T once read; dV [256,256+d);
+//           dK [256+d, 256+2d).
+//     MMA order per query tile i:
+//       dP(i), dV(i) += P^T dO, S(i+1), dK(i) += dS^T Q, dQ^T(i) = K^T dS^T
+//   bwd_post : dQ = bf16(scale * accumulator).
+#include <cuda_bf16.h>
+
+#include <cmath>
+
 #include "fa_internal.h"
+#include "sm103_math.cuh"
+#include "sm103_ptx.cuh"
 
 namespace fa {
-cudaError_t launch_bwd(const Problem&, const void*, const float*, const void*, void*, void*, void*, float*, float*,
-                       cudaStream_t) {
-  return cudaErrorNotSupported;
+namespace bwd {
+
+constexpr int kThreads = 384;
+constexpr int kSlots = 4;
+
+template <int D>
+struct Cfg {
+  static constexpr int kTile = 128 * D * 2;  // K, V, Q or dO tile of 128 rows
+  static constexpr int kDsBytes = 128 * 128 * 2;
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kTile;
+  static constexpr int kOffSlots = 2 * kTile;
+  static constexpr int kOffDs = kOffSlots + kSlots * kTile;
+  static constexpr int kOffVec = kOffDs + kDsBytes;  // [2 stages][lse2 128 | delta 128] fp32
+  static constexpr int kOffCtl = kOffVec + 2 * 2 * 128 * 4;
+  static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
+};
+
+struct __align__(8) Ctl {
+  uint64_t kv_full;
+  uint64_t slot_full[kSlots];
+  uint64_t slot_empty[kSlots];
+  uint64_t vec_full[2];
+  uint64_t vec_empty[2];
+  uint64_t s_full, p_full, dp_full, ds_full, dq_full, dq_empty, acc_full, drain;
+  uint32_t tmem_base;
+  uint32_t abort;
+};
+
+struct Params {
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  float* dq_acc;        // [B, Nq, Hq, D] fp32
+  const float* lse2;    // [B*Hq, Nq_pad]: LSE*log2(e), +inf for padded / empty rows
+  const float* delta;   // [B*Hq, Nq_pad]
+  int B, Hq, Hkv, Nq, Nk, Nq_pad, group, n_ktiles, n_qtiles;
+  float scale, scale_log2;
+  unsigned long long wait_limit_ns;
+  unsigned* status;
+};
+
+struct Work {
+  int b, kvh, j;
+  int i0, nq;   // first query tile, query tiles per head
+  int steps;    // group * nq
+};
+
+template <bool CAUSAL>
+__device__ __forceinline__ Work decode(const Params& p) {
+  Work w;
+  const int bk = p.B * p.Hkv;
+  w.j = blockIdx.x / bk;  // ascending key tile = descending work when causal
+  const int r = blockIdx.x - w.j * bk;
+  w.b = r / p.Hkv;
+  w.kvh = r - w.b * p.Hkv;
+  w.i0 = 0;
+  if (CAUSAL) {
+    const int first_row = w.j * 128 - (p.Nk - p.Nq);  // first query row that sees key j*128
+    w.i0 = first_row <= 0 ? 0 : first_row / 128;
+  }
+  w.nq = p.n_qtiles - w.i0;
+  if (w.nq < 0) w.nq = 0;
+  w.steps = w.nq * p.group;
+  return w;
 }
+
+// swizzled (128-byte) byte offset of element (row, col) in a [128 rows x 128
+// cols] bf16 tile stored as two 64-column atoms
+__device__ __forceinline__ uint32_t sw128_off(int row, int col) {
+  const int chunk = col >> 6, c = col & 63;
+  return chunk * 16384 + (row >> 3) * 1024 + (row & 7) * 128 + ((((c >> 3) ^ (row & 7))) << 4) + ((c & 7) << 1);
+}
+
+__device__ __forceinline__ void red_add_f32(float* addr, float v) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                    const Params p) {
+  using C = Cfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  Ctl& ctl = *reinterpret_cast<Ctl*>(smem + C::kOffCtl);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int wg = warp >> 2;
+  const Work w = decode<CAUSAL>(p);
+  const uint64_t LIM = p.wait_limit_ns;
+  volatile uint32_t* abort_flag = &ctl.abort;
+
+  if ((smem_u32(smem) & 1023u) != 0) {  // the swizzle atoms need a 1024-byte aligned base
+    if (threadIdx.x == 0) atomicOr(p.status, kDevTimeout);
+    return;
+  }
+  if (threadIdx.x == 0) {
+    ctl.abort = 0;
+    mbar_init(&ctl.kv_full, 1);
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(&ctl.slot_full[i], 1);
+      mbar_init(&ctl.slot_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&ctl.vec_full[i], 1);
+      mbar_init(&ctl.vec_empty[i], 4);
+    }
+    mbar_init(&ctl.s_full, 1);
+    mbar_init(&ctl.p_full, 4);
+    mbar_init(&ctl.dp_full, 1);
+    mbar_init(&ctl.ds_full, 4);
+    mbar_init(&ctl.dq_full, 1);
+    mbar_init(&ctl.dq_empty, 4);
+    mbar_init(&ctl.acc_full, 1);
+    mbar_init(&ctl.drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(&ctl.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl.tmem_base;
+  uint8_t* sK = smem + C::kOffK;
+  uint8_t* sV = smem + C::kOffV;
+  uint8_t* sSlots = smem + C::kOffSlots;
+  uint8_t* sDs = smem + C::kOffDs;
+  float* sVec = reinterpret_cast<float*>(smem + C::kOffVec);
+
+  if (wg == 0) {
+    // ------------------------------------------------------------ compute
+    setmaxnreg_inc<232>();
+    const int row = ((warp & 3) << 5) + lane;  // key row within the tile
+    const uint32_t t_lane = tmem + (uint32_t(warp & 3) << 21);
+    const int key = w.j * 128 + row;
+    const bool kvalid = key < p.Nk;  // keys past Nk are zero-filled: give them P = 0
+    const int off = p.Nk - p.Nq;
+    const float sl = p.scale_log2;
+    uint32_t ph_s = 0, ph_dp = 0;
+    bool ok = true;
+    for (int st = 0; st < w.steps && ok; ++st) {
+      const int it = w.i0 + st % w.nq;  // query tile
+      const int vs = st & 1;
+      const float* lse2 = sVec + vs * 256;
+      const float* dlt = lse2 + 128;
+      if (!mbar_wait_bounded(&ctl.vec_full[vs], (st >> 1) & 1, abort_flag, LIM)) { ok = false; break; }
+      if (!mbar_wait_bounded(&ctl.s_full, ph_s, abort_flag, LIM)) { ok = false; break; }
+      ph_s ^= 1;
+      tc_fence_after();
+      uint32_t x[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        tmem_ld32(t_lane + C::kColS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&x[c * 32]));
+      tmem_wait_ld();
+      // causal: query row q sees this key iff q >= key - off
+      const bool need_mask = CAUSAL && (it * 128 < w.j * 128 + 127 - off);
+      const int qlim = key - off - it * 128;  // columns c < qlim are hidden
+      float pv[128];
+#pragma unroll
+      for (int c = 0; c < 128; c += 4) {
+        const float4 l4 = *reinterpret_cast<const float4*>(lse2 + c);
+        const uint64_t y0 = ffma2(pack2(u2f(x[c]), u2f(x[c + 1])), pack2(sl, sl), pack2(-l4.x, -l4.y));
+        const uint64_t y1 = ffma2(pack2(u2f(x[c + 2]), u2f(x[c + 3])), pack2(sl, sl), pack2(-l4.z, -l4.w));
+        float a0, a1, a2, a3;
+        unpack2(y0, a0, a1);
+        unpack2(y1, a2, a3);
+        pv[c] = ex2_mufu(a0);
+        pv[c + 1] = ex2_mufu(a1);
+        pv[c + 2] = ex2_mufu(a2);
+        pv[c + 3] = ex2_mufu(a3);
+        if (!kvalid) {
+          pv[c] = pv[c + 1] = pv[c + 2] = pv[c + 3] = 0.0f;
+        } else if (need_mask) {
+          if (c < qlim) pv[c] = 0.0f;
+          if (c + 1 < qlim) pv[c + 1] = 0.0f;
+          if (c + 2 < qlim) pv[c + 2] = 0.0f;
+          if (c + 3 < qlim) pv[c + 3] = 0.0f;
+        }
+      }
+      {
+        uint32_t pk[64];
+#pragma unroll
+        for (int c = 0; c < 64; ++c) pk[c] = pack_bf16x2(pv[2 * c], pv[2 * c + 1]);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_st16(t_lane + C::kColS + c * 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[c * 16]));
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl.p_full);
+
+      // dS^T = P^T o (dP^T - D)
+      if (!mbar_wait_bounded(&ctl.dp_full, ph_dp, abort_flag, LIM)) { ok = false; break; }
+      ph_dp ^= 1;
+      tc_fence_after();
+#pragma unroll
+      for (int c0 = 0; c0 < 128; c0 += 32) {
+        uint32_t g[32];
+        tmem_ld32(t_lane + C::kColDP + c0, g);
+        tmem_wait_ld();
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {  // 8 columns = one 16-byte unit
+          const int c = c0 + u * 8;
+          const float4 d0 = *reinterpret_cast<const float4*>(dlt + c);
+          const float4 d1 = *reinterpret_cast<const float4*>(dlt + c + 4);
+          const float dd[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+          uint32_t pk[4];
+#pragma unroll
+          for (int e = 0; e < 8; e += 2) {
+            const float s0 = pv[c + e] * (u2f(g[u * 8 + e]) - dd[e]);
+            const float s1 = pv[c + e + 1] * (u2f(g[u * 8 + e + 1]) - dd[e + 1]);
+            pk[e >> 1] = pack_bf16x2(s0, s1);
+          }
+          *reinterpret_cast<uint4*>(sDs + sw128_off(row, c)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&ctl.ds_full);
+        mbar_arrive(&ctl.vec_empty[vs]);
+      }
+    }
+  } else if (wg == 1) {
+    // ------------------------------------------------ dQ drain + epilogue
+    const int wq = warp & 3;
+    const uint32_t t_lane = tmem + (uint32_t(wq) << 21);
+    const int lr = (wq << 5) + lane;  // TMEM lane: d index (D=128) or query row (D=64)
+    uint32_t ph_dq = 0;
+    bool ok = true;
+    for (int st = 0; st < w.steps && ok; ++st) {
+      const int it = w.i0 + st % w.nq;
+      const int h = w.kvh * p.group + st / w.nq;
+      if (!mbar_wait_bounded(&ctl.dq_full, ph_dq, abort_flag, LIM)) { ok = false; break; }
+      ph_dq ^= 1;
+      tc_fence_after();
+      if (D == 128) {
+        uint32_t v[128];
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          tmem_ld32(t_lane + C::kColDP + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&v[c * 32]));
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl.dq_empty);
+        // dQ^T: lane = d index, column = query row of the tile
+        float* base = p.dq_acc + ((size_t(w.b) * p.Nq + it * 128) * p.Hq + h) * D + lr;
+        const size_t rstride = size_t(p.Hq) * D;
+        const int nrows = min(128, p.Nq - it * 128);
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (c < nrows) red_add_f32(base + c * rstride, u2f(v[c]));
+      } else {
+        uint32_t v[64];
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+          tmem_ld32(t_lane + C::kColDP + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&v[c * 32]));
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl.dq_empty);
+        // dQ: lane = query row, 64 columns = d
+        const int q = it * 128 + lr;
+        if (q < p.Nq) {
+          float* dst = p.dq_acc + ((size_t(w.b) * p.Nq + q) * p.Hq + h) * D;
+#pragma unroll
+          for (int c = 0; c < 64; c += 4) red_add_v4(dst + c, u2f(v[c]), u2f(v[c + 1]), u2f(v[c + 2]), u2f(v[c + 3]));
+        }
+      }
+    }
+    // epilogue: dV, dK rows of this key tile (lane = key row)
+    if (ok) {
+      const int key = w.j * 128 + lr;
+      const bool valid = key < p.Nk;
+      __nv_bfloat16* dv = p.dv + ((size_t(w.b) * p.Nk + key) * p.Hkv + w.kvh) * D;
+      __nv_bfloat16* dk = p.dk + ((size_t(w.b) * p.Nk + key) * p.Hkv + w.kvh) * D;
+      if (w.steps == 0) {
+        if (valid) {
+          for (int c = 0; c < D / 8; ++c) {
+            reinterpret_cast<uint4*>(dv)[c] = make_uint4(0, 0, 0, 0);
+            reinterpret_cast<uint4*>(dk)[c] = make_uint4(0, 0, 0, 0);
+          }
+        }
+      } else if (mbar_wait_bounded(&ctl.acc_full, 0, abort_flag, LIM)) {
+        tc_fence_after();
+#pragma unroll 1
+        for (int t = 0; t < 2; ++t) {
+          const uint32_t col = t == 0 ? C::kColDV : C::kColDK;
+          const float mul = t == 0 ? 1.0f : p.scale;
+          __nv_bfloat16* dst = t == 0 ? dv : dk;
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld32(t_lane + col + c * 32, v);
+            tmem_wait_ld();
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(u2f(v[2 * i]) * mul, u2f(v[2 * i + 1]) * mul);
+            if (valid) {
+              uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+            }
+          }
+        }
+      }
+    }
+  } else {
+    setmaxnreg_dec<104>();
+  }
+  if (warp == 8) {
+    // ------------------------------------------------------- TMA producer
+    if (lane == 0 && w.steps > 0) {
+      bool ok = true;
+      mbar_arrive_expect_tx(&ctl.kv_full, 2 * C::kTile);
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        tma_load_4d(sK + c * 16384, &tmK, &ctl.kv_full, c * 64, w.kvh, w.j * 128, w.b);
+        tma_load_4d(sV + c * 16384, &tmV, &ctl.kv_full, c * 64, w.kvh, w.j * 128, w.b);
+      }
+      uint32_t slot_it = 0;
+      for (int st = 0; st < w.steps && ok; ++st) {
+        const int it = w.i0 + st % w.nq;
+        const int h = w.kvh * p.group + st / w.nq;
+#pragma unroll 1
+        for (int t = 0; t < 2; ++t) {  // Q then dO
+          const uint32_t slot = slot_it % kSlots;
+          if (!mbar_wait_bounded(&ctl.slot_empty[slot], ((slot_it / kSlots) & 1) ^ 1, abort_flag, LIM)) {
+            ok = false;
+            break;
+          }
+          ++slot_it;
+          mbar_arrive_expect_tx(&ctl.slot_full[slot], C::kTile);
+          const CUtensorMap* map = t == 0 ? &tmQ : &tmDO;
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_4d(sSlots + slot * C::kTile + c * 16384, map, &ctl.slot_full[slot], c * 64, h, it * 128, w.b);
+        }
+        if (!ok) break;
+        const int vs = st & 1;
+        if (!mbar_wait_bounded(&ctl.vec_empty[vs], ((st >> 1) & 1) ^ 1, abort_flag, LIM)) { ok = false; break; }
+        mbar_arrive_expect_tx(&ctl.vec_full[vs], 1024);
+        const size_t roff = (size_t(w.b) * p.Hq + h) * p.Nq_pad + size_t(it) * 128;
+        bulk_load(sVec + vs * 256, p.lse2 + roff, 512, &ctl.vec_full[vs]);
+        bulk_load(sVec + vs * 256 + 128, p.delta + roff, 512, &ctl.vec_full[vs]);
+      }
+      if (*abort_flag) {
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 1000000ull) __nanosleep(1000);
+      }
+    }
+  } else if (warp == 9) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0 && w.steps > 0) {
+      constexpr uint32_t idSS = idesc_bf16_f32(128, 128, 0, 0);     // S^T, dP^T
+      constexpr uint32_t idAcc = idesc_bf16_f32(128, D, 0, 1);      // dV, dK
+      constexpr uint32_t idDQ = D == 128 ? idesc_bf16_f32(128, 128, 1, 1) : idesc_bf16_f32(128, 64, 1, 1);
+      const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aSl = smem_u32(sSlots), aDs = smem_u32(sDs);
+      bool ok = mbar_wait_bounded(&ctl.kv_full, 0, abort_flag, LIM);
+      uint32_t ph_p = 0, ph_ds = 0, ph_dqe = 0;
+      uint32_t slot_it = 0;
+      auto wait_slot = [&](uint32_t& slot) -> bool {
+        slot = slot_it % kSlots;
+        const bool r = mbar_wait_bounded(&ctl.slot_full[slot], (slot_it / kSlots) & 1, abort_flag, LIM);
+        ++slot_it;
+        return r;
+      };
+      auto issue_kmajor = [&](uint32_t d_col, uint32_t a_base, uint32_t b_base) {  // [128 x 128] += A B^T, K = D
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_ss(tmem + d_col, sdesc_sw128(a_base + ko, 16, 1024), sdesc_sw128(b_base + ko, 16, 1024), idSS, kk > 0);
+        }
+      };
+      uint32_t sq = 0, sdo = 0;
+      if (ok) ok = wait_slot(sq);
+      if (ok) {
+        tc_fence_after();
+        issue_kmajor(C::kColS, aK, aSl + sq * C::kTile);  // S^T(0) = K Q_0^T
+        mma_commit(&ctl.s_full);
+      }
+      for (int st = 0; st < w.steps && ok; ++st) {
+        if (!wait_slot(sdo)) { ok = false; break; }
+        if (st > 0) {
+          if (!mbar_wait_bounded(&ctl.dq_empty, ph_dqe, abort_flag, LIM)) { ok = false; break; }
+          ph_dqe ^= 1;
+        }
+        tc_fence_after();
+        issue_kmajor(C::kColDP, aV, aSl + sdo * C::kTile);  // dP^T = V dO^T
+        mma_commit(&ctl.dp_full);
+        if (!mbar_wait_bounded(&ctl.p_full, ph_p, abort_flag, LIM)) { ok = false; break; }
+        ph_p ^= 1;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)  // dV += P^T dO   (P^T in TMEM, dO MN-major)
+          mma_ts(tmem + C::kColDV, tmem + C::kColS + kk * 8, sdesc_sw128(aSl + sdo * C::kTile + kk * 2048, 16384, 1024),
+                 idAcc, (st > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&ctl.slot_empty[sdo]);
+        uint32_t sq_next = 0;
+        if (st + 1 < w.steps) {
+          if (!wait_slot(sq_next)) { ok = false; break; }
+          tc_fence_after();
+          issue_kmajor(C::kColS, aK, aSl + sq_next * C::kTile);  // S^T(i+1)
+          mma_commit(&ctl.s_full);
+        }
+        if (!mbar_wait_bounded(&ctl.ds_full, ph_ds, abort_flag, LIM)) { ok = false; break; }
+        ph_ds ^= 1;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {  // dK += dS^T Q   (dS^T K-major, Q MN-major)
+          const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_ss(tmem + C::kColDK, sdesc_sw128(aDs + ko, 16, 1024),
+                 sdesc_sw128(aSl + sq * C::kTile + kk * 2048, 16384, 1024), idAcc, (st > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(&ctl.slot_empty[sq]);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          if (D == 128)  // dQ^T = K^T dS^T  (both MN-major)
+            mma_ss(tmem + C::kColDP, sdesc_sw128(aK + kk * 2048, 16384, 1024), sdesc_sw128(aDs + kk * 2048, 16384, 1024),
+                   idDQ, kk > 0);
+          else  // dQ = dS K  (both MN-major)
+            mma_ss(tmem + C::kColDP, sdesc_sw128(aDs + kk * 2048, 16384, 1024), sdesc_sw128(aK + kk * 2048, 16384, 1024),
+                   idDQ, kk > 0);
+        }
+        mma_commit(&ctl.dq_full);
+        sq = sq_next;
+      }
+      if (ok) mma_commit(&ctl.acc_full);
+      if (*abort_flag) {
+        mma_commit(&ctl.drain);
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(smem_u32(&ctl.drain), 0) && globaltimer_ns() - t0 < 100000000ull) {
+        }
+      }
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 9) tmem_dealloc(tmem, 512);
+  if (threadIdx.x == 0 && ctl.abort) atomicOr(p.status, kDevTimeout);
+}
+
+// D_i = sum_c dO_ic O_ic and LSE * log2(e) per row, written to padded
+// [B*Hq, Nq_pad] arrays; padded rows and rows with LSE = -inf get +inf (so
+// their probabilities recompute to 0) and D = 0. Also zeroes the fp32 dQ
+// accumulator.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* o, const __nv_bfloat16* dout,
+                                                      const float* lse, float* lse2, float* delta, float* dq_acc,
+                                                      int B, int Hq, int Nq, int Nq_pad) {
+  constexpr int TPR = D / 8;  // threads per row, 8 elements (16 bytes) each
+  const long long rows = 1LL * B * Nq * Hq;
+  const long long tid = 1LL * blockIdx.x * blockDim.x + threadIdx.x;
+  const long long r = tid / TPR;
+  const int part = int(tid % TPR);
+  float acc = 0.0f;
+  if (r < rows) {
+    const uint4 a = *reinterpret_cast<const uint4*>(o + r * D + part * 8);
+    const uint4 g = *reinterpret_cast<const uint4*>(dout + r * D + part * 8);
+    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+    const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&g);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 fa = __bfloat1622float2(a2[i]), fg = __bfloat1622float2(g2[i]);
+      acc = fmaf(fa.x, fg.x, acc);
+      acc = fmaf(fa.y, fg.y, acc);
+    }
+  }
+#pragma unroll
+  for (int s = TPR / 2; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+  if (r < rows && part == 0) {
+    // r indexes [B, Nq, Hq]
+    const int h = int(r % Hq);
+    const long long bq = r / Hq;
+    const int q = int(bq % Nq);
+    const int b = int(bq / Nq);
+    const size_t dst = (size_t(b) * Hq + h) * Nq_pad + q;
+    const float l = lse[(size_t(b) * Hq + h) * Nq + q];
+    lse2[dst] = l == -INFINITY ? INFINITY : l * 1.4426950408889634f;
+    delta[dst] = acc;
+  }
+  // padded rows
+  const long long pad = 1LL * B * Hq * (Nq_pad - Nq);
+  const long long nthreads = 1LL * gridDim.x * blockDim.x;
+  for (long long i = tid; i < pad; i += nthreads) {
+    const long long bh = i / (Nq_pad - Nq);
+    const int q = Nq + int(i % (Nq_pad - Nq));
+    lse2[bh * Nq_pad + q] = INFINITY;
+    delta[bh * Nq_pad + q] = 0.0f;
+  }
+  // zero the dQ accumulator
+  const long long n4 = 1LL * B * Nq * Hq * D / 4;
+  for (long long i = tid; i < n4; i += nthreads) reinterpret_cast<float4*>(dq_acc)[i] = make_float4(0, 0, 0, 0);
+}
+
+__global__ void __launch_bounds__(256) bwd_post_kernel(const float* dq_acc, __nv_bfloat16* dq, long long n8,
+                                                       float scale) {
+  const long long i = 1LL * blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n8) return;
+  const float4 a = reinterpret_cast<const float4*>(dq_acc)[2 * i];
+  const float4 b = reinterpret_cast<const float4*>(dq_acc)[2 * i + 1];
+  uint4 r;
+  r.x = pack_bf16x2(a.x * scale, a.y * scale);
+  r.y = pack_bf16x2(a.z * scale, a.w * scale);
+  r.z = pack_bf16x2(b.x * scale, b.y * scale);
+  r.w = pack_bf16x2(b.z * scale, b.w * scale);
+  reinterpret_cast<uint4*>(dq)[i] = r;
+}
+
+template <int D, bool CAUSAL>
+cudaError_t launch_t(const Problem& pb, const void* o, const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                     float* ws, cudaStream_t stream) {
+  const int Nq_pad = (pb.Nq + 127) / 128 * 128;
+  const size_t acc_elems = size_t(pb.B) * pb.Nq * pb.Hq * D;
+  float* dq_acc = ws;
+  float* lse2 = ws + acc_elems;
+  float* delta = lse2 + size_t(pb.B) * pb.Hq * Nq_pad;
+  {
+    const long long threads = 1LL * pb.B * pb.Nq * pb.Hq * (D / 8);
+    long long blocks = (threads + 255) / 256;
+    const long long minb = 4LL * num_sms();
+    if (blocks < minb) blocks = minb;
+    bwd_pre_kernel<D><<<unsigned(blocks), 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(o),
+                                                             static_cast<const __nv_bfloat16*>(dout), lse, lse2, delta,
+                                                             dq_acc, pb.B, pb.Hq, pb.Nq, Nq_pad);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  CUtensorMap mq, mk, mv, mdo;
+  if (!make_bshd_map(&mq, pb.q, pb.B, pb.Nq, pb.Hq, D, 128) || !make_bshd_map(&mk, pb.k, pb.B, pb.Nk, pb.Hkv, D, 128) ||
+      !make_bshd_map(&mv, pb.v, pb.B, pb.Nk, pb.Hkv, D, 128) ||
+      !make_bshd_map(&mdo, dout, pb.B, pb.Nq, pb.Hq, D, 128))
+    return cudaErrorInvalidValue;
+  Params p;
+  p.dk = static_cast<__nv_bfloat16*>(dk);
+  p.dv = static_cast<__nv_bfloat16*>(dv);
+  p.dq_acc = dq_acc;
+  p.lse2 = lse2;
+  p.delta = delta;
+  p.B = pb.B;
+  p.Hq = pb.Hq;
+  p.Hkv = pb.Hkv;
+  p.Nq = pb.Nq;
+  p.Nk = pb.Nk;
+  p.Nq_pad = Nq_pad;
+  p.group = pb.Hq / pb.Hkv;
+  p.n_ktiles = (pb.Nk + 127) / 128;
+  p.n_qtiles = Nq_pad / 128;
+  p.scale = pb.scale;
+  p.scale_log2 = pb.scale * 1.4426950408889634f;
+  p.wait_limit_ns = debug_cfg().wait_limit_ns;
+  p.status = status_word();
+  if (!p.status) return cudaErrorMemoryAllocation;
+  using C = Cfg<D>;
+  constexpr int smem = C::kOffCtl + int(sizeof(Ctl));
+  auto kern = bwd_main_kernel<D, CAUSAL>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const unsigned grid = unsigned(pb.B) * pb.Hkv * p.n_ktiles;
+  kern<<<grid, kThreads, smem, stream>>>(mq, mk, mv, mdo, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const long long n8 = (long long)acc_elems / 8;
+  bwd_post_kernel<<<unsigned((n8 + 255) / 256), 256, 0, stream>>>(dq_acc, static_cast<__nv_bfloat16*>(dq), n8,
+                                                                  pb.scale);
+  return cudaGetLastError();
+}
+
+}  // namespace bwd
+
+size_t bwd_workspace_bytes(const Problem& p) {
+  const size_t Nq_pad = size_t(p.Nq + 127) / 128 * 128;
+  return sizeof(float) * (size_t(p.B) * p.Nq * p.Hq * p.d + 2 * size_t(p.B) * p.Hq * Nq_pad);
+}
+
+cudaError_t launch_bwd(const Problem& p, const void* o, const float* lse, const void* dout, void* dq, void* dk,
+                       void* dv, float* ws, cudaStream_t stream) {
+  if (p.d == 128)
+    return p.causal ? bwd::launch_t<128, true>(p, o, lse, dout, dq, dk, dv, ws, stream)
+                    : bwd::launch_t<128, false>(p, o, lse, dout, dq, dk, dv, ws, stream);
+  return p.causal ? bwd::launch_t<64, true>(p, o, lse, dout, dq, dk, dv, ws, stream)
+                  : bwd::launch_t<64, false>(p, o, lse, dout, dq, dk, dv, ws, stream);
+}
+
 }  // namespace fa

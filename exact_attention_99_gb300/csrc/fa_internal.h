@@ -36,8 +36,10 @@ bool make_bshd_map(CUtensorMap* m, const void* base, int B, int N, int H, int d,
 
 // Launchers. Return a cudaError_t (cudaSuccess on success).
 cudaError_t launch_fwd(const Problem& p, void* o, float* lse, cudaStream_t stream);
+// Backward workspace (fp32 dQ accumulator, padded LSE*log2e and D rows).
+size_t bwd_workspace_bytes(const Problem& p);
 cudaError_t launch_bwd(const Problem& p, const void* o, const float* lse, const void* dout, void* dq, void* dk,
-                       void* dv, float* dq_acc, float* delta, cudaStream_t stream);
+                       void* dv, float* ws, cudaStream_t stream);
 cudaError_t launch_debug_exp2(const float* x, float* y, int n, int mode, cudaStream_t stream);
 
 }  // namespace fa
