@@ -1,0 +1,402 @@
+#!/usr/bin/env python
+"""Benchmark of exact attention on GB300: one step = the whole hot path
+(forward: O and LSE; backward: dQ, dK, dV) over one batch of the headline
+workload B=4, H=16, Nq=Nk=2048, d=128, non-causal, bf16, seeded synthetic
+inputs resident in HBM.
+
+Prints ONE JSON line on rank 0. `value` is TFLOP/s over all ranks (forward
+4*B*H*N*N*d plus backward 2.5x that, per step), timed on the device with
+CUDA events over K steps with the L2 flushed (a 256 MB write) before every
+step. Extra keys: `roofline` for the dominant kernel, `cpu_baseline` (the
+fp64 oracle on a bounded sample on the host cores), `e2e` (the same metric
+through the public API with pinned host buffers, copies included), `clocks`
+sampled during the timed region, `gpu_launches`, and `configs` with
+forward/backward TFLOP/s of every headline workload.
+
+--impl reference times the fp64 CPU oracle on the same workload (a bounded
+sample per step) and prints the same kind of line with "impl": "reference".
+Multi-GPU (torchrun): every rank runs the same per-GPU workload (weak
+scaling, no collective in the data path); the timing is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+MAIN = workloads.WORKLOADS[1]
+METRIC = "attention fwd/bwd TFLOP/s at 1 GB300 and fraction of dense BF16 tensor peak"
+FLUSH_BYTES = 256 << 20
+KERNEL_SOURCES = {"fa_fwd_kernel": "fa_fwd.cu", "bwd_main_kernel": "fa_bwd.cu"}
+
+
+def step_flops(w) -> float:
+    return w.fwd_flops() + w.bwd_flops()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops, burst cuBLAS)"
+    return 1900.0, "fallback (1.9 PFLOP/s bf16 burst from an earlier GB300 measurement)"
+
+
+def source_sha(kernel: str) -> str:
+    path = os.path.join(ROOT, "exact_attention_99_gb300", "csrc", KERNEL_SOURCES[kernel])
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, workload: str):
+    """dram bytes per launch from a committed ncu summary, if that summary was
+    taken on the current source of the kernel; else None."""
+    for path in glob.glob(os.path.join(ROOT, "profiles", "*.md")):
+        fields = {}
+        with open(path) as f:
+            for line in f:
+                if ":" in line and line.startswith("- "):
+                    k, v = line[2:].split(":", 1)
+                    fields[k.strip()] = v.strip().strip("`")
+        if fields.get("kernel") == kernel and fields.get("workload") == workload:
+            if fields.get("source_sha256") == source_sha(kernel) and "dram_bytes_per_launch" in fields:
+                return int(float(fields["dram_bytes_per_launch"]))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.lines = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", str(self.dev)], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.3)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, flag in zip(names, parts[5:9]):
+                if flag.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "power_w_max": max(power), "samples": len(sm)}
+
+
+def oracle_sample(w, x, seconds: float, max_heads: int | None = None, first: int = 0):
+    """Time the fp64 oracle (forward + backward) head by head on the main
+    workload, starting at (batch, head) slice `first`, until `seconds` have
+    passed or `max_heads` slices are done. Returns (flops, elapsed, heads)."""
+    from oracle import attn_ref
+    heads = [(b, h) for b in range(w.B) for h in range(w.Hq)]
+    heads = heads[first % len(heads):] + heads[:first % len(heads)]
+    flops_per_head = step_flops(w) / (w.B * w.Hq)
+    done, t0 = 0, time.perf_counter()
+    for b, h in heads:
+        kv = h // (w.Hq // w.Hkv)
+        sl = lambda t, hh: t[b:b + 1, :, hh:hh + 1].double().numpy()
+        q, k, v, do = sl(x["q"], h), sl(x["k"], kv), sl(x["v"], kv), sl(x["do"], h)
+        attn_ref.forward(q, k, v, w.scale, w.causal)
+        attn_ref.backward(q, k, v, do, w.scale, w.causal)
+        done += 1
+        if time.perf_counter() - t0 >= seconds or (max_heads and done >= max_heads):
+            break
+    el = time.perf_counter() - t0
+    return done * flops_per_head, el, done
+
+
+def blas_threads() -> int:
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(var):
+            return int(os.environ[var])
+    return os.cpu_count() or 1
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    w = MAIN
+    x = workloads.workload_inputs(w, with_dout=True)
+    flops_head = step_flops(w) / (w.B * w.Hq)
+    for i in range(args.warmup):
+        oracle_sample(w, x, 0.0, max_heads=1, first=i)
+    times = []
+    for i in range(args.steps):
+        _, el, _ = oracle_sample(w, x, 0.0, max_heads=1, first=args.warmup + i)
+        times.append(el)
+    total = sum(times)
+    value = args.steps * flops_head / total / 1e12
+    sample = f"one (batch, head) slice of {w.name} per step: fp64 forward + backward, N={w.Nq}, d={w.d}"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Nq": w.Nq, "Nk": w.Nk, "d": w.d,
+                   "causal": w.causal, "step": "fwd+bwd of one head (bounded sample)"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def time_one(fn, flush, reps=5, warm=2):
+    import torch
+    for _ in range(warm):
+        fn()
+    ts = []
+    for _ in range(reps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    return statistics.median(ts)
+
+
+def per_config(fa, flush, peak):
+    """Forward TFLOP/s of the four forward workloads and backward TFLOP/s of
+    the backward workload (kernel-only, inputs resident, L2 flushed)."""
+    import torch
+    out = {}
+    for w in workloads.WORKLOADS:
+        x = workloads.workload_inputs(w, with_dout=True)
+        q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
+        o = torch.empty_like(q)
+        lse = torch.empty((w.B, w.Hq, w.Nq), device="cuda", dtype=torch.float32)
+        fwd = lambda: fa.fa_fwd(q, k, v, o, lse, w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.d, w.scale, int(w.causal))
+        ms = time_one(fwd, flush)
+        ent = {"fwd_ms": ms, "fwd_tflops": w.fwd_flops() / ms / 1e9}
+        ent["fwd_frac_of_peak"] = ent["fwd_tflops"] / peak
+        if w.direction == "bwd" or w is MAIN:
+            dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+            bwd = lambda: fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.d, w.scale,
+                                    int(w.causal))
+            ms = time_one(bwd, flush)
+            ent.update({"bwd_ms": ms, "bwd_tflops": w.bwd_flops() / ms / 1e9})
+            ent["bwd_frac_of_peak"] = ent["bwd_tflops"] / peak
+        out[w.name] = {kk: (round(vv, 4) if isinstance(vv, float) else vv) for kk, vv in ent.items()}
+        del q, k, v, do, o, lse
+        torch.cuda.synchronize()
+    assert fa.fa_get_status() == 0
+    return out
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    import __graft_entry__
+    __graft_entry__.build()
+    import exact_attention_99_gb300 as fa
+    fa.fa_debug_set(0, 0)
+
+    w = MAIN
+    peak, peak_src = load_peaks()
+    x = workloads.workload_inputs(w, with_dout=True)
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
+    o, dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    lse = torch.empty((w.B, w.Hq, w.Nq), device="cuda", dtype=torch.float32)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    args_f = (w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.d, w.scale, int(w.causal))
+    K = args.steps
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    e0, e1 = [ev() for _ in range(K)], [ev() for _ in range(K)]
+    kf0, kf1, kb0, kb1 = ([ev() for _ in range(K)] for _ in range(4))
+
+    def step(i=None):
+        if i is not None:
+            fa.fa_profile_events(kf0[i], kf1[i])
+        st = fa.fa_fwd(q, k, v, o, lse, *args_f)
+        if i is not None:
+            fa.fa_profile_events(kb0[i], kb1[i])
+        st |= fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, *args_f)
+        if i is not None:
+            fa.fa_profile_events(None, None)
+        if st:
+            raise RuntimeError(f"launch failed: {st}")
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    sampler = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else
+                           int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]))
+    sampler.start()
+    time.sleep(0.2)
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush.zero_()
+        e0[i].record()
+        step(i)
+        e1[i].record()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    status = fa.fa_get_status()
+    if status != 0:
+        raise RuntimeError(f"device status {fa.fa_status_string(status)}")
+    step_ms = [a.elapsed_time(b) for a, b in zip(e0, e1)]
+    total_ms = sum(step_ms)
+    fwd_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(kf0, kf1))
+    bwd_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(kb0, kb1))
+    if world > 1:
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    value = world * K * step_flops(w) / (total_ms * 1e-3) / 1e12
+
+    # end to end through the public API: pinned host inputs in, results out
+    host_in = {n: x[n].pin_memory() for n in ("q", "k", "v", "do")}
+    host_out = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in
+                (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+    dev_in = {"q": q, "k": k, "v": v, "do": do}
+    dev_out = {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
+    ke = min(K, 10)
+    ee0, ee1 = [ev() for _ in range(ke)], [ev() for _ in range(ke)]
+    torch.cuda.synchronize()
+    for i in range(ke):
+        flush.zero_()
+        ee0[i].record()
+        for n, t in host_in.items():
+            dev_in[n].copy_(t, non_blocking=True)
+        step()
+        for n, t in dev_out.items():
+            host_out[n].copy_(t, non_blocking=True)
+        ee1[i].record()
+    torch.cuda.synchronize()
+    e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(ee0, ee1))
+    e2e_value = world * step_flops(w) / (e2e_ms * 1e-3) / 1e12
+
+    if rank != 0:
+        if world > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return
+
+    # dominant kernel and its roofline
+    if bwd_ms >= fwd_ms:
+        kname, kflops, kms = "bwd_main_kernel", w.bwd_flops(), bwd_ms
+    else:
+        kname, kflops, kms = "fa_fwd_kernel", w.fwd_flops(), fwd_ms
+    achieved = kflops / (kms * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "kernel": kname, "achieved": round(achieved, 2), "peak": peak,
+                "peak_source": peak_src, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                "traffic": profiled_traffic(kname, w.name), "avg_launch_ms": round(kms, 4),
+                "flops_per_launch": kflops}
+
+    configs = per_config(fa, flush, peak)
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(total_ms / K, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Nq": w.Nq, "Nk": w.Nk, "d": w.d,
+                   "causal": w.causal, "step": "fwd (O, LSE) + bwd (dQ, dK, dV)", "l2": "flushed before every step",
+                   "parallelism": f"replicas x{world}"},
+        "fwd_kernel_ms": round(fwd_ms, 4), "bwd_main_kernel_ms": round(bwd_ms, 4),
+        "fwd_tflops": round(w.fwd_flops() / fwd_ms / 1e9, 2),
+        "bwd_main_tflops": round(w.bwd_flops() / bwd_ms / 1e9, 2),
+        "roofline": roofline,
+        "clocks": clocks,
+        "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": 4 * K,
+        "configs": configs,
+    }
+    if world == 1:
+        flops_done, el, heads = oracle_sample(w, x, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": flops_done / el / 1e12, "unit": "TFLOP/s", "cores": blas_threads(),
+                                "kind": "oracle",
+                                "sample": f"{heads} of {w.B * w.Hq} (batch, head) slices of {w.name}, fp64 "
+                                          f"forward + backward, {el:.1f} s"}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -18,7 +18,7 @@ import math
 import os
 
 __all__ = ["FAError", "lib", "fa_fwd", "fa_bwd", "fa_get_status", "fa_status_string", "fa_debug_set",
-           "fa_debug_exp2", "forward", "backward", "STATUS"]
+           "fa_debug_exp2", "fa_profile_events", "forward", "backward", "STATUS"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libfa.so")
@@ -61,6 +61,8 @@ def lib() -> ctypes.CDLL:
         L.fa_status_string.restype = ctypes.c_char_p
         L.fa_debug_set.argtypes = [ull, i]
         L.fa_debug_set.restype = i
+        L.fa_profile_events.argtypes = [vp, vp]
+        L.fa_profile_events.restype = i
         L.fa_debug_exp2.argtypes = [vp, vp, i, i, vp]
         L.fa_debug_exp2.restype = i
         _lib = L
@@ -104,6 +106,13 @@ def fa_status_string(status: int) -> str:
 
 def fa_debug_set(wait_limit_ns: int = 0, inject: int = 0) -> int:
     return lib().fa_debug_set(int(wait_limit_ns), int(inject))
+
+
+def fa_profile_events(begin=None, end=None) -> int:
+    """begin/end: torch.cuda.Event (created with enable_timing) or None."""
+    b = None if begin is None else begin.cuda_event
+    e = None if end is None else end.cuda_event
+    return lib().fa_profile_events(b, e)
 
 
 def fa_debug_exp2(x, y, n, mode, stream=None) -> int:

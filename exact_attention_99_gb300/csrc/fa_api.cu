@@ -27,7 +27,7 @@ std::mutex g_mu;
 int g_sms[kMaxDevices];
 unsigned* g_status_ptr[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-DebugCfg g_debug = {kDefaultWaitNs, 0};
+DebugCfg g_debug = {kDefaultWaitNs, 0, nullptr, nullptr};
 
 int current_device() {
   int dev = -1;
@@ -203,6 +203,14 @@ extern "C" int fa_debug_set(unsigned long long wait_limit_ns, int inject) {
   std::lock_guard<std::mutex> lk(g_mu);
   g_debug.wait_limit_ns = wait_limit_ns == 0 ? kDefaultWaitNs : wait_limit_ns;
   g_debug.inject = inject;
+  return FA_OK;
+}
+
+extern "C" int fa_profile_events(void* begin, void* end) {
+  if ((begin == nullptr) != (end == nullptr)) return FA_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_debug.ev_begin = static_cast<cudaEvent_t>(begin);
+  g_debug.ev_end = static_cast<cudaEvent_t>(end);
   return FA_OK;
 }
 

@@ -604,7 +604,8 @@ cudaError_t launch_t(const Problem& pb, const void* o, const float* lse, const v
   p.n_qtiles = Nq_pad / 128;
   p.scale = pb.scale;
   p.scale_log2 = pb.scale * 1.4426950408889634f;
-  p.wait_limit_ns = debug_cfg().wait_limit_ns;
+  const DebugCfg dc = debug_cfg();
+  p.wait_limit_ns = dc.wait_limit_ns;
   p.status = status_word();
   if (!p.status) return cudaErrorMemoryAllocation;
   using C = Cfg<D>;
@@ -613,8 +614,10 @@ cudaError_t launch_t(const Problem& pb, const void* o, const float* lse, const v
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const unsigned grid = unsigned(pb.B) * pb.Hkv * p.n_ktiles;
+  if (dc.ev_begin) cudaEventRecord(dc.ev_begin, stream);
   kern<<<grid, kThreads, smem, stream>>>(mq, mk, mv, mdo, p);
   e = cudaGetLastError();
+  if (dc.ev_end) cudaEventRecord(dc.ev_end, stream);
   if (e != cudaSuccess) return e;
   const long long n8 = (long long)acc_elems / 8;
   bwd_post_kernel<<<unsigned((n8 + 255) / 256), 256, 0, stream>>>(dq_acc, static_cast<__nv_bfloat16*>(dq), n8,

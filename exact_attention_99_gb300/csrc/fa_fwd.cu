@@ -551,8 +551,11 @@ cudaError_t launch_t(const Problem& pb, void* o, float* lse, cudaStream_t stream
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmemDyn);
   if (e != cudaSuccess) return e;
   const int grid = p.n_units < num_sms() ? p.n_units : num_sms();
+  if (dc.ev_begin) cudaEventRecord(dc.ev_begin, stream);
   kern<<<grid, kThreads, Cfg<D>::kSmemDyn, stream>>>(mq, mk, mv, p);
-  return cudaGetLastError();
+  e = cudaGetLastError();
+  if (dc.ev_end) cudaEventRecord(dc.ev_end, stream);
+  return e;
 }
 
 }  // namespace fwd

@@ -21,6 +21,8 @@ struct Problem {
 struct DebugCfg {
   unsigned long long wait_limit_ns;
   int inject;
+  cudaEvent_t ev_begin;  // recorded around the main kernel when set
+  cudaEvent_t ev_end;
 };
 DebugCfg debug_cfg();
 

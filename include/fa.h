@@ -102,7 +102,17 @@ const char* fa_status_string(int status);
  *   unit, mode 1 = the fitted polynomial on the FMA pipes.
  */
 int fa_debug_set(unsigned long long wait_limit_ns, int inject);
+
 int fa_debug_exp2(const float* x, float* y, int n, int mode, void* stream);
+
+/*
+ * fa_profile_events — begin/end are cudaEvent_t handles (or NULL to stop).
+ *   While set, fa_fwd records `begin` on its stream right before its kernel
+ *   and `end` right after it; fa_bwd does the same around its main
+ *   (five-GEMM) kernel, leaving out the preprocess and dQ-convert kernels.
+ *   The events are owned by the caller. Process-wide; not thread-safe.
+ */
+int fa_profile_events(void* begin, void* end);
 
 #ifdef __cplusplus
 }
