@@ -266,6 +266,9 @@ def run_ours(args):
     ev = lambda: torch.cuda.Event(enable_timing=True)
     e0, e1 = [ev() for _ in range(K)], [ev() for _ in range(K)]
     kf0, kf1, kb0, kb1 = ([ev() for _ in range(K)] for _ in range(4))
+    for e in kf0 + kf1 + kb0 + kb1:  # torch creates the CUDA event on first record
+        e.record()
+    torch.cuda.synchronize()
 
     def step(i=None):
         if i is not None:
