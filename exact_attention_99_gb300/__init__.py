@@ -17,7 +17,7 @@ import ctypes
 import math
 import os
 
-__all__ = ["FAError", "lib", "fa_fwd", "fa_bwd", "fa_get_status", "fa_status_string", "fa_debug_set",
+__all__ = ["FAError", "lib", "fa_fwd", "fa_bwd", "fa_bwd_noalloc", "fa_get_status", "fa_status_string", "fa_debug_set",
            "fa_debug_exp2", "fa_profile_events", "forward", "backward", "STATUS"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -55,6 +55,8 @@ def lib() -> ctypes.CDLL:
         L.fa_fwd.restype = i
         L.fa_bwd.argtypes = [vp] * 9 + [i, i, i, i, i, i, f, i, vp]
         L.fa_bwd.restype = i
+        L.fa_bwd_noalloc.argtypes = [vp] * 9 + [i, i, i, i, i, i, f, i, vp]
+        L.fa_bwd_noalloc.restype = i
         L.fa_get_status.argtypes = [vp]
         L.fa_get_status.restype = i
         L.fa_status_string.argtypes = [i]
@@ -94,6 +96,13 @@ def fa_fwd(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, stream=None) -
 def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Nq, Nk, d, scale, causal, stream=None) -> int:
     return lib().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
                         B, Hq, Hkv, Nq, Nk, d, float(scale), int(causal), _stream(stream))
+
+
+def fa_bwd_noalloc(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Nq, Nk, d, scale, causal, stream=None) -> int:
+    """fa_bwd with its workspace in the library's fixed device array (no
+    device allocation during the call; see fa.h for the size limit)."""
+    return lib().fa_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
+                                _ptr(dv), B, Hq, Hkv, Nq, Nk, d, float(scale), int(causal), _stream(stream))
 
 
 def fa_get_status(stream=None) -> int:

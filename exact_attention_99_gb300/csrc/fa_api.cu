@@ -132,6 +132,17 @@ bool make_bshd_map(CUtensorMap* m, const void* base, int B, int N, int H, int d,
   return r == CUDA_SUCCESS;
 }
 
+int check_bwd_args(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                   void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Nq, int Nk, int d, float scale,
+                   int causal) {
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(dout) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return FA_ERR_INVALID_ARG;
+  const int st = check_sizes(B, Hq, Hkv, Nq, Nk, d, scale, causal);
+  if (st != FA_OK) return st;
+  return check_device();
+}
+
 cudaError_t launch_debug_exp2(const float* x, float* y, int n, int mode, cudaStream_t stream) {
   debug_exp2_kernel<<<(n + 255) / 256, 256, 0, stream>>>(x, y, n, mode);
   return cudaGetLastError();

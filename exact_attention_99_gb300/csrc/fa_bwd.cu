@@ -31,7 +31,9 @@
 #include <cuda_bf16.h>
 
 #include <cmath>
+#include <mutex>
 
+#include "../../include/fa.h"
 #include "fa_internal.h"
 #include "sm103_math.cuh"
 #include "sm103_ptx.cuh"
@@ -642,3 +644,59 @@ cudaError_t launch_bwd(const Problem& p, const void* o, const float* lse, const 
 }
 
 }  // namespace fa
+
+// ---------------------------------------------------------------------------
+// Allocation-free backward (fa_bwd_noalloc in fa.h).
+//
+// fa_bwd asks the stream-ordered allocator for its fp32 workspace on every
+// call. Some callers must not allocate device memory at that point: serving
+// loops that fix their whole memory plan at start-up and treat any later
+// allocation as a failure, and code that runs where the CUDA allocator may
+// not be entered at all (for instance inside another allocator's hooks).
+// For them the workspace lives in a fixed file-scope device array instead.
+// Its address is a device address only on the device side; host code must
+// look it up per device with cudaGetSymbolAddress, which is done once per
+// device on that device's first call.
+namespace fa {
+namespace {
+
+static __device__ __align__(256) float g_bwd_noalloc_scratch[FA_BWD_NOALLOC_SCRATCH_BYTES / sizeof(float)];
+
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+float* g_noalloc_ptr[kNoAllocMaxDevices];
+
+// Device address of this device's scratch array (nullptr on failure).
+float* noalloc_scratch() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_bwd_noalloc_scratch) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    g_noalloc_ptr[dev] = static_cast<float*>(ptr);
+  }
+  return g_noalloc_ptr[dev];
+}
+
+}  // namespace
+}  // namespace fa
+
+extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                              const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Nq, int Nk,
+                              int d, float scale, int causal, void* stream) {
+  const int st = fa::check_bwd_args(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Nq, Nk, d, scale, causal);
+  if (st != FA_OK) return st;
+  const fa::Problem p{q, k, v, B, Hq, Hkv, Nq, Nk, d, scale, causal};
+  if (fa::bwd_workspace_bytes(p) > FA_BWD_NOALLOC_SCRATCH_BYTES) return FA_ERR_UNSUPPORTED;
+  float* ws = fa::noalloc_scratch();
+  if (ws == nullptr) return FA_ERR_LAUNCH;
+  // The preprocess kernel zeroes the dQ accumulator and rewrites every LSE/D
+  // row it reads, so nothing left in the array by an earlier call is used.
+  return fa::launch_bwd(p, o, lse, dout, dq, dk, dv, ws, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? FA_OK
+             : FA_ERR_LAUNCH;
+}

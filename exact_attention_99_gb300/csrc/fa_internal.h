@@ -38,6 +38,11 @@ bool make_bshd_map(CUtensorMap* m, const void* base, int B, int N, int H, int d,
 
 // Launchers. Return a cudaError_t (cudaSuccess on success).
 cudaError_t launch_fwd(const Problem& p, void* o, float* lse, cudaStream_t stream);
+// The host-side checks fa_bwd performs (pointers, sizes, device), as one call.
+int check_bwd_args(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                   void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Nq, int Nk, int d, float scale,
+                   int causal);
+
 // Backward workspace (fp32 dQ accumulator, padded LSE*log2e and D rows).
 size_t bwd_workspace_bytes(const Problem& p);
 cudaError_t launch_bwd(const Problem& p, const void* o, const float* lse, const void* dout, void* dq, void* dk,

@@ -80,6 +80,33 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
            void* stream);
 
 /*
+ * fa_bwd_noalloc — the same backward pass as fa_bwd, for callers that may
+ * not allocate device memory during the call: serving loops that fix their
+ * memory plan at start-up, and code that runs where the CUDA allocator must
+ * not be entered. The pages have no counterpart of this call; it only
+ * changes where the workspace lives.
+ *   Arguments, layouts, results and argument errors are those of fa_bwd.
+ *   Workspace: a file-scope device array of FA_BWD_NOALLOC_SCRATCH_BYTES
+ *     (64 MiB) inside the library. Every device that loads the library holds
+ *     it until the process exits. The call needs
+ *       4 * (B*Nq*Hq*d + 2*B*Hq*ceil(Nq/128)*128) bytes of it and returns
+ *     FA_ERR_UNSUPPORTED, without enqueuing anything, when that exceeds the
+ *     array.
+ *   No cudaMalloc, cudaFree or other allocating routine is called.
+ *   Set-up: the first call on each device looks up the array's device
+ *     address on that device (cudaGetSymbolAddress); make that first call
+ *     before any stream capture. A failed look-up returns FA_ERR_LAUNCH.
+ *   Sharing: all calls on a device share the one array, and it keeps the
+ *     last call's contents (the call re-initialises what it reads). Calls
+ *     whose work overlaps on the GPU (different streams, no ordering between
+ *     them) race on the array and give wrong results; order them.
+ */
+#define FA_BWD_NOALLOC_SCRATCH_BYTES (64ull << 20)
+int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                   void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Nq, int Nk, int d, float scale,
+                   int causal, void* stream);
+
+/*
  * fa_get_status — synchronises `stream`, then returns and clears the
  * current device's status word: FA_OK, or FA_ERR_TIMEOUT if any kernel of
  * this library gave up on a bounded wait since the last call. A CUDA error
