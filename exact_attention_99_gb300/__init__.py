@@ -18,7 +18,7 @@ import math
 import os
 
 __all__ = ["FAError", "lib", "fa_fwd", "fa_bwd", "fa_bwd_noalloc", "fa_get_status", "fa_status_string", "fa_debug_set",
-           "fa_debug_exp2", "fa_profile_events", "forward", "backward", "STATUS"]
+           "fa_debug_exp2", "fa_profile_events", "fa_trace", "forward", "backward", "STATUS"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libfa.so")
@@ -65,6 +65,8 @@ def lib() -> ctypes.CDLL:
         L.fa_debug_set.restype = i
         L.fa_profile_events.argtypes = [vp, vp]
         L.fa_profile_events.restype = i
+        L.fa_trace.argtypes = [vp]
+        L.fa_trace.restype = i
         L.fa_debug_exp2.argtypes = [vp, vp, i, i, vp]
         L.fa_debug_exp2.restype = i
         _lib = L
@@ -122,6 +124,14 @@ def fa_profile_events(begin=None, end=None) -> int:
     b = None if begin is None else begin.cuda_event
     e = None if end is None else end.cuda_event
     return lib().fa_profile_events(b, e)
+
+
+TRACE_CTAS, TRACE_STEPS, TRACE_POINTS = 4, 64, 16
+
+
+def fa_trace(buf=None) -> int:
+    """buf: CUDA int64 tensor of TRACE_CTAS*TRACE_STEPS*TRACE_POINTS words, or None."""
+    return lib().fa_trace(_ptr(buf))
 
 
 def fa_debug_exp2(x, y, n, mode, stream=None) -> int:

@@ -27,7 +27,7 @@ std::mutex g_mu;
 int g_sms[kMaxDevices];
 unsigned* g_status_ptr[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-DebugCfg g_debug = {kDefaultWaitNs, 0, nullptr, nullptr};
+DebugCfg g_debug = {kDefaultWaitNs, 0, nullptr, nullptr, nullptr};
 
 int current_device() {
   int dev = -1;
@@ -222,6 +222,13 @@ extern "C" int fa_profile_events(void* begin, void* end) {
   std::lock_guard<std::mutex> lk(g_mu);
   g_debug.ev_begin = static_cast<cudaEvent_t>(begin);
   g_debug.ev_end = static_cast<cudaEvent_t>(end);
+  return FA_OK;
+}
+
+extern "C" int fa_trace(void* buf) {
+  if (buf != nullptr && (reinterpret_cast<uintptr_t>(buf) & 7u) != 0) return FA_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_debug.trace = static_cast<unsigned long long*>(buf);
   return FA_OK;
 }
 

@@ -78,7 +78,14 @@ struct Params {
   float scale, scale_log2;
   unsigned long long wait_limit_ns;
   unsigned* status;
+  unsigned long long* trace;  // optional pipeline trace
 };
+
+// Trace points (fa_trace), per query-tile step:
+//   MMA      0 dP issued, 1 P ready (dV next), 2 next Q ready (S next), 3 dS ready (dK next), 4 dQ^T issued
+//   compute  5 LSE/D ready, 6 S^T ready, 7 P^T stored, 8 dP^T ready, 9 dS^T stored
+//   drain    10 dQ^T ready, 11 dQ^T columns released, 12 reductions issued
+//   producer 13 Q slot free, 14 dO slot free
 
 struct Work {
   int b, kvh, j;
@@ -198,8 +205,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float* lse2 = sVec + vs * 256;
       const float* dlt = lse2 + 128;
       if (!mbar_wait_bounded(&ctl.vec_full[vs], (st >> 1) & 1, abort_flag, LIM)) { ok = false; break; }
+      if (threadIdx.x == 0) trace_stamp(p.trace, st, 5);
       if (!mbar_wait_bounded(&ctl.s_full, ph_s, abort_flag, LIM)) { ok = false; break; }
       ph_s ^= 1;
+      if (threadIdx.x == 0) trace_stamp(p.trace, st, 6);
       tc_fence_after();
       uint32_t x[128];
 #pragma unroll
@@ -241,11 +250,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
+      if (threadIdx.x == 0) trace_stamp(p.trace, st, 7);
       if (lane == 0) mbar_arrive(&ctl.p_full);
 
       // dS^T = P^T o (dP^T - D)
       if (!mbar_wait_bounded(&ctl.dp_full, ph_dp, abort_flag, LIM)) { ok = false; break; }
       ph_dp ^= 1;
+      if (threadIdx.x == 0) trace_stamp(p.trace, st, 8);
       tc_fence_after();
 #pragma unroll
       for (int c0 = 0; c0 < 128; c0 += 32) {
@@ -271,6 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
+      if (threadIdx.x == 0) trace_stamp(p.trace, st, 9);
       if (lane == 0) {
         mbar_arrive(&ctl.ds_full);
         mbar_arrive(&ctl.vec_empty[vs]);
@@ -288,6 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int h = w.kvh * p.group + st / w.nq;
       if (!mbar_wait_bounded(&ctl.dq_full, ph_dq, abort_flag, LIM)) { ok = false; break; }
       ph_dq ^= 1;
+      if (threadIdx.x == 128) trace_stamp(p.trace, st, 10);
       tc_fence_after();
       if (D == 128) {
         uint32_t v[128];
@@ -298,6 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&ctl.dq_empty);
+        if (threadIdx.x == 128) trace_stamp(p.trace, st, 11);
         // dQ^T: lane = d index, column = query row of the tile
         float* base = p.dq_acc + ((size_t(w.b) * p.Nq + it * 128) * p.Hq + h) * D + lr;
         const size_t rstride = size_t(p.Hq) * D;
@@ -305,6 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 128; ++c)
           if (c < nrows) red_add_f32(base + c * rstride, u2f(v[c]));
+        if (threadIdx.x == 128) trace_stamp(p.trace, st, 12);
       } else {
         uint32_t v[64];
 #pragma unroll
@@ -384,6 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
+          trace_stamp(p.trace, st, 13 + t);
           ++slot_it;
           mbar_arrive_expect_tx(&ctl.slot_full[slot], C::kTile);
           const CUtensorMap* map = t == 0 ? &tmQ : &tmDO;
@@ -441,10 +457,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           ph_dqe ^= 1;
         }
         tc_fence_after();
+        trace_stamp(p.trace, st, 0);
         issue_kmajor(C::kColDP, aV, aSl + sdo * C::kTile);  // dP^T = V dO^T
         mma_commit(&ctl.dp_full);
         if (!mbar_wait_bounded(&ctl.p_full, ph_p, abort_flag, LIM)) { ok = false; break; }
         ph_p ^= 1;
+        trace_stamp(p.trace, st, 1);
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)  // dV += P^T dO   (P^T in TMEM, dO MN-major)
@@ -454,12 +472,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t sq_next = 0;
         if (st + 1 < w.steps) {
           if (!wait_slot(sq_next)) { ok = false; break; }
+          trace_stamp(p.trace, st, 2);
           tc_fence_after();
           issue_kmajor(C::kColS, aK, aSl + sq_next * C::kTile);  // S^T(i+1)
           mma_commit(&ctl.s_full);
         }
         if (!mbar_wait_bounded(&ctl.ds_full, ph_ds, abort_flag, LIM)) { ok = false; break; }
         ph_ds ^= 1;
+        trace_stamp(p.trace, st, 3);
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {  // dK += dS^T Q   (dS^T K-major, Q MN-major)
@@ -478,6 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    idDQ, kk > 0);
         }
         mma_commit(&ctl.dq_full);
+        trace_stamp(p.trace, st, 4);
         sq = sq_next;
       }
       if (ok) mma_commit(&ctl.acc_full);
@@ -608,6 +629,7 @@ cudaError_t launch_t(const Problem& pb, const void* o, const float* lse, const v
   p.scale_log2 = pb.scale * 1.4426950408889634f;
   const DebugCfg dc = debug_cfg();
   p.wait_limit_ns = dc.wait_limit_ns;
+  p.trace = dc.trace;
   p.status = status_word();
   if (!p.status) return cudaErrorMemoryAllocation;
   using C = Cfg<D>;

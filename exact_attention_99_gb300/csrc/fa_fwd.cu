@@ -74,7 +74,15 @@ struct Params {
   unsigned long long wait_limit_ns;
   int inject;
   unsigned* status;
+  unsigned long long* trace;  // optional pipeline trace
 };
+
+// Trace points (fa_trace); a step is the CTA's running key-tile counter
+// across its units:
+//   MMA         0 PV0 issued, 1 PV1 issued, 2 S0(next) issued, 3 S1(next) issued
+//   softmax s   4+3s S ready, 5+3s alpha published, 6+3s P stored
+//   correction  10+2s alpha seen, 11+2s O released for PV
+//   producer    14 K slot free, 15 V slot free
 
 struct __align__(8) Ctl {
   uint64_t q_full[2];
@@ -200,6 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = ((warp & 3) << 5) + lane;
     const uint32_t t_s = tmem + (uint32_t(warp & 3) << 21) + uint32_t(s * 128);  // lane quarter + S columns
     uint32_t ph_s = 0, ph_se = 0;
+    int blk = 0;  // running key-tile counter (trace only)
     const float sl = p.scale_log2;
     bool ok = true;
     for (int rnd = 0; ok; ++rnd) {
@@ -207,6 +216,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (u >= p.n_units) break;
       const Unit un = decode_unit<CAUSAL>(p, u);
       const int n = un.n[s];
+      const int blk0 = blk;
+      blk += un.nb;
       if (n == 0) continue;
       const int rg = un.row0 + s * 128 + row;  // global query row
       const int off = p.Nk - p.Nq;
@@ -214,6 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < n; ++j) {
         if (!mbar_wait_bounded(&ctl.s_full[s], ph_s, abort_flag, LIM)) { ok = false; break; }
         ph_s ^= 1;
+        if (row == 0) trace_stamp(p.trace, blk0 + j, 4 + 3 * s);
         tc_fence_after();
         uint32_t x[128];
 #pragma unroll
@@ -242,6 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float alpha = ex2_mufu(m_run - m_use);
         ctl.alpha[s][row] = alpha;
         __syncwarp();
+        if (row == 0) trace_stamp(p.trace, blk0 + j, 5 + 3 * s);
         if (lane == 0) mbar_arrive(&ctl.alpha_full[s]);
 
         const uint64_t sl2 = pack2(sl, sl);
@@ -276,6 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
+        if (row == 0) trace_stamp(p.trace, blk0 + j, 6 + 3 * s);
         if (lane == 0) mbar_arrive(&ctl.p_full[s]);
       }
       if (!ok) break;
@@ -294,17 +308,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = (wq << 5) + lane;
     const uint32_t t_lane = tmem + (uint32_t(wq) << 21);
     uint32_t ph_a[2] = {0, 0}, ph_st[2] = {0, 0}, ph_of[2] = {0, 0};
+    int blk = 0;
     bool ok = true;
     for (int rnd = 0; ok; ++rnd) {
       const int u = unit_at(rnd, blockIdx.x);
       if (u >= p.n_units) break;
       const Unit un = decode_unit<CAUSAL>(p, u);
+      const int blk0 = blk;
+      blk += un.nb;
       for (int j = 0; j < un.nb && ok; ++j) {
 #pragma unroll
         for (int s = 0; s < 2; ++s) {
           if (j >= un.n[s]) continue;
           if (!mbar_wait_bounded(&ctl.alpha_full[s], ph_a[s], abort_flag, LIM)) { ok = false; break; }
           ph_a[s] ^= 1;
+          if (row == 0) trace_stamp(p.trace, blk0 + j, 10 + 2 * s);
           const float a = ctl.alpha[s][row];
           if (j > 0 && __any_sync(0xffffffffu, a < 1.0f)) {
             tc_fence_after();
@@ -328,6 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_before();
           __syncwarp();
+          if (row == 0) trace_stamp(p.trace, blk0 + j, 11 + 2 * s);
           if (lane == 0) mbar_arrive(&ctl.o_ready[s]);
         }
       }
@@ -384,6 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------- TMA producer
     if (lane == 0) {
       uint32_t kv_it = 0, ph_qe = 0;
+      int blk = 0;
       bool first = true, ok = true;
       bool injected = false;
       for (int rnd = 0; ok; ++rnd) {
@@ -410,6 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t slot = kv_it % C::kSlots;
             const uint32_t ph = ((kv_it / C::kSlots) & 1) ^ 1;
             if (!mbar_wait_bounded(&ctl.kv_empty[slot], ph, abort_flag, LIM)) { ok = false; break; }
+            trace_stamp(p.trace, blk + j, 14 + t);
             ++kv_it;
             if (p.inject == 1 && !injected) {  // test hook: never deliver this tile
               injected = true;
@@ -423,6 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                           un.b);
           }
         }
+        blk += un.nb;
       }
       if (*abort_flag) {
         // let copies already in flight land before shared memory is released
@@ -437,6 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idPV = idesc_bf16_f32(128, D, 0, 1);
       const uint32_t sQa = smem_u32(sQ), sKVa = smem_u32(sKV);
       uint32_t kv_it = 0, ph_q[2] = {0, 0}, ph_p[2] = {0, 0}, ph_o[2] = {0, 0};
+      int blk = 0;
       bool ok = true;
       auto issue_S = [&](int s, uint32_t kslot) {
 #pragma unroll
@@ -492,9 +515,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait_bounded(&ctl.o_ready[s], ph_o[s], abort_flag, LIM)) { ok = false; break; }
             ph_o[s] ^= 1;
             tc_fence_after();
+            trace_stamp(p.trace, blk + j, s);
             issue_PV(s, vslot, j > 0);
             if (j == un.n[s] - 1) mma_commit(&ctl.o_full[s]);
             if (j + 1 < un.n[s]) {
+              trace_stamp(p.trace, blk + j, 2 + s);
               issue_S(s, kslot);
               mma_commit(&ctl.s_full[s]);
             }
@@ -504,6 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (nxt) mma_commit(&ctl.kv_empty[kslot]);
           if (j + 2 == un.nb) mma_commit(&ctl.q_empty);
         }
+        blk += un.nb;
       }
       if (*abort_flag) {
         // drain the tensor pipe before TMEM is released
@@ -545,6 +571,7 @@ cudaError_t launch_t(const Problem& pb, void* o, float* lse, cudaStream_t stream
   const DebugCfg dc = debug_cfg();
   p.wait_limit_ns = dc.wait_limit_ns;
   p.inject = dc.inject;
+  p.trace = dc.trace;
   p.status = status_word();
   if (!p.status) return cudaErrorMemoryAllocation;
   auto kern = fa_fwd_kernel<D, CAUSAL>;

@@ -23,6 +23,7 @@ struct DebugCfg {
   int inject;
   cudaEvent_t ev_begin;  // recorded around the main kernel when set
   cudaEvent_t ev_end;
+  unsigned long long* trace;  // optional device trace buffer
 };
 DebugCfg debug_cfg();
 

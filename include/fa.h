@@ -141,6 +141,22 @@ int fa_debug_exp2(const float* x, float* y, int n, int mode, void* stream);
  */
 int fa_profile_events(void* begin, void* end);
 
+/*
+ * fa_trace — buf: device buffer of FA_TRACE_WORDS uint64 words (or NULL to
+ *   stop). While set, the first FA_TRACE_CTAS CTAs of each main kernel write
+ *   %globaltimer stamps (ns) at their pipeline hand-off points into
+ *   buf[(cta * FA_TRACE_STEPS + step) * FA_TRACE_POINTS + point], for the
+ *   first FA_TRACE_STEPS steps of that CTA; a step is one key tile of one
+ *   unit (forward) or one query tile (backward). The points are listed in the
+ *   kernels' sources. The buffer is owned by the caller; the library only
+ *   writes it. Process-wide; not thread-safe.
+ */
+#define FA_TRACE_CTAS 4
+#define FA_TRACE_STEPS 64
+#define FA_TRACE_POINTS 16
+#define FA_TRACE_WORDS (FA_TRACE_CTAS * FA_TRACE_STEPS * FA_TRACE_POINTS)
+int fa_trace(void* buf);
+
 #ifdef __cplusplus
 }
 #endif
