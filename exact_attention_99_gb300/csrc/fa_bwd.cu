@@ -19,15 +19,21 @@
 //              query heads of the GQA group x 128-row query tiles.
 //     warps 0-3  compute: one thread per key row; P^T = 2^(S^T*scale*log2e -
 //                LSE*log2e), dS^T = P^T o (dP^T - D)
-//     warps 4-7  dQ drain (TMEM -> fp32 reductions into the accumulator) and
-//                the dK/dV epilogue
+//     warps 4-7  dQ drain and the dK/dV epilogue. d = 128: dQ^T leaves TMEM
+//                into a shared-memory staging buffer and is added to the fp32
+//                accumulator by TMA bulk reductions; d = 64: coalesced fp32
+//                reductions.
+//     Shared memory: K and V tiles (resident), a 2-slot Q ring, a 1-slot dO
+//     ring (its last reader, dV, runs early in each step), the dS^T tile,
+//     the dQ staging buffer, LSE/D vectors.
 //     warp 8     TMA producer, warp 9 MMA issuer, warps 10-11 idle
 //     TMEM: S^T [0,128) with P^T (bf16) over its first 64 columns;
 //           dP^T [128,256), reused for dQ^T once read; dV [256,256+d);
 //           dK [256+d, 256+2d).
 //     MMA order per query tile i:
 //       dP(i), dV(i) += P^T dO, S(i+1), dK(i) += dS^T Q, dQ^T(i) = K^T dS^T
-//   bwd_post : dQ = bf16(scale * accumulator).
+//   bwd_post : dQ = bf16(scale * accumulator), transposed back to BSHD.
+//   The accumulator is [B*Hq, d, Nq_pad] fp32 (query index innermost).
 #include <cuda_bf16.h>
 
 #include <cmath>
@@ -42,25 +48,26 @@ namespace fa {
 namespace bwd {
 
 constexpr int kThreads = 384;
-constexpr int kSlots = 4;
 
 template <int D>
 struct Cfg {
   static constexpr int kTile = 128 * D * 2;  // K, V, Q or dO tile of 128 rows
   static constexpr int kDsBytes = 128 * 128 * 2;
+  static constexpr int kStgBytes = D == 128 ? 32768 : 0;  // dQ^T staging: 4 warps x 2 boxes of [32 d][32 q] fp32
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kTile;
-  static constexpr int kOffSlots = 2 * kTile;
-  static constexpr int kOffDs = kOffSlots + kSlots * kTile;
-  static constexpr int kOffVec = kOffDs + kDsBytes;  // [2 stages][lse2 128 | delta 128] fp32
+  static constexpr int kOffQ = 2 * kTile;   // 2 slots
+  static constexpr int kOffDO = 4 * kTile;  // 1 slot
+  static constexpr int kOffDs = 5 * kTile;
+  static constexpr int kOffStg = kOffDs + kDsBytes;
+  static constexpr int kOffVec = kOffStg + kStgBytes;  // [2 stages][lse2 128 | delta 128] fp32
   static constexpr int kOffCtl = kOffVec + 2 * 2 * 128 * 4;
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
 };
 
 struct __align__(8) Ctl {
   uint64_t kv_full;
-  uint64_t slot_full[kSlots];
-  uint64_t slot_empty[kSlots];
+  uint64_t q_full[2], q_empty[2], do_full, do_empty;
   uint64_t vec_full[2];
   uint64_t vec_empty[2];
   uint64_t s_full, p_full, dp_full, ds_full, dq_full, dq_empty, acc_full, drain;
@@ -71,7 +78,7 @@ struct __align__(8) Ctl {
 struct Params {
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
-  float* dq_acc;        // [B, Nq, Hq, D] fp32
+  float* dq_acc;        // [B*Hq, D, Nq_pad] fp32
   const float* lse2;    // [B*Hq, Nq_pad]: LSE*log2(e), +inf for padded / empty rows
   const float* delta;   // [B*Hq, Nq_pad]
   int B, Hq, Hkv, Nq, Nk, Nq_pad, group, n_ktiles, n_qtiles;
@@ -138,7 +145,7 @@ template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-                    const Params p) {
+                    const __grid_constant__ CUtensorMap tmAcc, const Params p) {
   using C = Cfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   Ctl& ctl = *reinterpret_cast<Ctl*>(smem + C::kOffCtl);
@@ -156,10 +163,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     ctl.abort = 0;
     mbar_init(&ctl.kv_full, 1);
-    for (int i = 0; i < kSlots; ++i) {
-      mbar_init(&ctl.slot_full[i], 1);
-      mbar_init(&ctl.slot_empty[i], 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&ctl.q_full[i], 1);
+      mbar_init(&ctl.q_empty[i], 1);
     }
+    mbar_init(&ctl.do_full, 1);
+    mbar_init(&ctl.do_empty, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ctl.vec_full[i], 1);
       mbar_init(&ctl.vec_empty[i], 4);
@@ -184,7 +193,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = ctl.tmem_base;
   uint8_t* sK = smem + C::kOffK;
   uint8_t* sV = smem + C::kOffV;
-  uint8_t* sSlots = smem + C::kOffSlots;
+  uint8_t* sQ = smem + C::kOffQ;
+  uint8_t* sDO = smem + C::kOffDO;
   uint8_t* sDs = smem + C::kOffDs;
   float* sVec = reinterpret_cast<float*>(smem + C::kOffVec);
 
@@ -312,13 +322,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&ctl.dq_empty);
         if (threadIdx.x == 128) trace_stamp(p.trace, st, 11);
-        // dQ^T: lane = d index, column = query row of the tile
-        float* base = p.dq_acc + ((size_t(w.b) * p.Nq + it * 128) * p.Hq + h) * D + lr;
-        const size_t rstride = size_t(p.Hq) * D;
-        const int nrows = min(128, p.Nq - it * 128);
+        // dQ^T: lane = d index, column = query row of the tile. Stage it as
+        // 128-byte-swizzled boxes of [32 d rows][32 q] fp32, two boxes per
+        // warp and half-tile, and add each box into the accumulator with a
+        // TMA reduction; the buffer is rewritten once the previous
+        // reductions have read it.
+        uint8_t* stg = smem + C::kOffStg + wq * 8192;
 #pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (c < nrows) red_add_f32(base + c * rstride, u2f(v[c]));
+        for (int half = 0; half < 2; ++half) {
+          if (lane == 0) bulk_wait_read_all();
+          __syncwarp();
+#pragma unroll
+          for (int b2 = 0; b2 < 2; ++b2) {
+            const int qb = half * 2 + b2;
+            uint8_t* box = stg + b2 * 4096 + lane * 128;
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              *reinterpret_cast<uint4*>(box + ((u ^ (lane & 7)) << 4)) =
+                  make_uint4(v[qb * 32 + 4 * u], v[qb * 32 + 4 * u + 1], v[qb * 32 + 4 * u + 2], v[qb * 32 + 4 * u + 3]);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+#pragma unroll
+            for (int b2 = 0; b2 < 2; ++b2)
+              tma_reduce_add_4d(&tmAcc, stg + b2 * 4096, it * 128 + (half * 2 + b2) * 32, wq * 32, h, w.b);
+            bulk_commit();
+          }
+        }
         if (threadIdx.x == 128) trace_stamp(p.trace, st, 12);
       } else {
         uint32_t v[64];
@@ -329,15 +360,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&ctl.dq_empty);
-        // dQ: lane = query row, 64 columns = d
+        // dQ: lane = query row, 64 columns = d; for a fixed d the warp's
+        // lanes hit consecutive query rows of the accumulator
         const int q = it * 128 + lr;
-        if (q < p.Nq) {
-          float* dst = p.dq_acc + ((size_t(w.b) * p.Nq + q) * p.Hq + h) * D;
+        float* dst = p.dq_acc + (size_t(w.b) * p.Hq + h) * D * size_t(p.Nq_pad) + q;
 #pragma unroll
-          for (int c = 0; c < 64; c += 4) red_add_v4(dst + c, u2f(v[c]), u2f(v[c + 1]), u2f(v[c + 2]), u2f(v[c + 3]));
-        }
+        for (int c = 0; c < 64; ++c) red_add_f32(dst + size_t(c) * p.Nq_pad, u2f(v[c]));
       }
     }
+    if (D == 128 && lane == 0) bulk_wait_all();  // the accumulator is complete when the kernel ends
     // epilogue: dV, dK rows of this key tile (lane = key row)
     if (ok) {
       const int key = w.j * 128 + lr;
@@ -388,26 +419,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_4d(sK + c * 16384, &tmK, &ctl.kv_full, c * 64, w.kvh, w.j * 128, w.b);
         tma_load_4d(sV + c * 16384, &tmV, &ctl.kv_full, c * 64, w.kvh, w.j * 128, w.b);
       }
-      uint32_t slot_it = 0;
       for (int st = 0; st < w.steps && ok; ++st) {
         const int it = w.i0 + st % w.nq;
         const int h = w.kvh * p.group + st / w.nq;
-#pragma unroll 1
-        for (int t = 0; t < 2; ++t) {  // Q then dO
-          const uint32_t slot = slot_it % kSlots;
-          if (!mbar_wait_bounded(&ctl.slot_empty[slot], ((slot_it / kSlots) & 1) ^ 1, abort_flag, LIM)) {
-            ok = false;
-            break;
-          }
-          trace_stamp(p.trace, st, 13 + t);
-          ++slot_it;
-          mbar_arrive_expect_tx(&ctl.slot_full[slot], C::kTile);
-          const CUtensorMap* map = t == 0 ? &tmQ : &tmDO;
+        const int qs = st & 1;
+        if (!mbar_wait_bounded(&ctl.q_empty[qs], ((st >> 1) & 1) ^ 1, abort_flag, LIM)) { ok = false; break; }
+        trace_stamp(p.trace, st, 13);
+        mbar_arrive_expect_tx(&ctl.q_full[qs], C::kTile);
 #pragma unroll
-          for (int c = 0; c < D / 64; ++c)
-            tma_load_4d(sSlots + slot * C::kTile + c * 16384, map, &ctl.slot_full[slot], c * 64, h, it * 128, w.b);
-        }
-        if (!ok) break;
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_4d(sQ + qs * C::kTile + c * 16384, &tmQ, &ctl.q_full[qs], c * 64, h, it * 128, w.b);
+        if (!mbar_wait_bounded(&ctl.do_empty, (st & 1) ^ 1, abort_flag, LIM)) { ok = false; break; }
+        trace_stamp(p.trace, st, 14);
+        mbar_arrive_expect_tx(&ctl.do_full, C::kTile);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_4d(sDO + c * 16384, &tmDO, &ctl.do_full, c * 64, h, it * 128, w.b);
         const int vs = st & 1;
         if (!mbar_wait_bounded(&ctl.vec_empty[vs], ((st >> 1) & 1) ^ 1, abort_flag, LIM)) { ok = false; break; }
         mbar_arrive_expect_tx(&ctl.vec_full[vs], 1024);
@@ -426,16 +453,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idSS = idesc_bf16_f32(128, 128, 0, 0);     // S^T, dP^T
       constexpr uint32_t idAcc = idesc_bf16_f32(128, D, 0, 1);      // dV, dK
       constexpr uint32_t idDQ = D == 128 ? idesc_bf16_f32(128, 128, 1, 1) : idesc_bf16_f32(128, 64, 1, 1);
-      const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aSl = smem_u32(sSlots), aDs = smem_u32(sDs);
+      const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aQ = smem_u32(sQ), aDO = smem_u32(sDO),
+                     aDs = smem_u32(sDs);
       bool ok = mbar_wait_bounded(&ctl.kv_full, 0, abort_flag, LIM);
       uint32_t ph_p = 0, ph_ds = 0, ph_dqe = 0;
-      uint32_t slot_it = 0;
-      auto wait_slot = [&](uint32_t& slot) -> bool {
-        slot = slot_it % kSlots;
-        const bool r = mbar_wait_bounded(&ctl.slot_full[slot], (slot_it / kSlots) & 1, abort_flag, LIM);
-        ++slot_it;
-        return r;
-      };
       auto issue_kmajor = [&](uint32_t d_col, uint32_t a_base, uint32_t b_base) {  // [128 x 128] += A B^T, K = D
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -443,22 +464,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ss(tmem + d_col, sdesc_sw128(a_base + ko, 16, 1024), sdesc_sw128(b_base + ko, 16, 1024), idSS, kk > 0);
         }
       };
-      uint32_t sq = 0, sdo = 0;
-      if (ok) ok = wait_slot(sq);
+      if (ok) ok = mbar_wait_bounded(&ctl.q_full[0], 0, abort_flag, LIM);
       if (ok) {
         tc_fence_after();
-        issue_kmajor(C::kColS, aK, aSl + sq * C::kTile);  // S^T(0) = K Q_0^T
+        issue_kmajor(C::kColS, aK, aQ);  // S^T(0) = K Q_0^T
         mma_commit(&ctl.s_full);
       }
       for (int st = 0; st < w.steps && ok; ++st) {
-        if (!wait_slot(sdo)) { ok = false; break; }
+        const uint32_t aQcur = aQ + (st & 1) * C::kTile;
+        if (!mbar_wait_bounded(&ctl.do_full, st & 1, abort_flag, LIM)) { ok = false; break; }
         if (st > 0) {
           if (!mbar_wait_bounded(&ctl.dq_empty, ph_dqe, abort_flag, LIM)) { ok = false; break; }
           ph_dqe ^= 1;
         }
         tc_fence_after();
         trace_stamp(p.trace, st, 0);
-        issue_kmajor(C::kColDP, aV, aSl + sdo * C::kTile);  // dP^T = V dO^T
+        issue_kmajor(C::kColDP, aV, aDO);  // dP^T = V dO^T
         mma_commit(&ctl.dp_full);
         if (!mbar_wait_bounded(&ctl.p_full, ph_p, abort_flag, LIM)) { ok = false; break; }
         ph_p ^= 1;
@@ -466,15 +487,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)  // dV += P^T dO   (P^T in TMEM, dO MN-major)
-          mma_ts(tmem + C::kColDV, tmem + C::kColS + kk * 8, sdesc_sw128(aSl + sdo * C::kTile + kk * 2048, 16384, 1024),
-                 idAcc, (st > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&ctl.slot_empty[sdo]);
-        uint32_t sq_next = 0;
+          mma_ts(tmem + C::kColDV, tmem + C::kColS + kk * 8, sdesc_sw128(aDO + kk * 2048, 16384, 1024), idAcc,
+                 (st > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&ctl.do_empty);
         if (st + 1 < w.steps) {
-          if (!wait_slot(sq_next)) { ok = false; break; }
+          const int nx = (st + 1) & 1;
+          if (!mbar_wait_bounded(&ctl.q_full[nx], ((st + 1) >> 1) & 1, abort_flag, LIM)) { ok = false; break; }
           trace_stamp(p.trace, st, 2);
           tc_fence_after();
-          issue_kmajor(C::kColS, aK, aSl + sq_next * C::kTile);  // S^T(i+1)
+          issue_kmajor(C::kColS, aK, aQ + nx * C::kTile);  // S^T(i+1)
           mma_commit(&ctl.s_full);
         }
         if (!mbar_wait_bounded(&ctl.ds_full, ph_ds, abort_flag, LIM)) { ok = false; break; }
@@ -485,9 +506,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < 8; ++kk) {  // dK += dS^T Q   (dS^T K-major, Q MN-major)
           const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
           mma_ss(tmem + C::kColDK, sdesc_sw128(aDs + ko, 16, 1024),
-                 sdesc_sw128(aSl + sq * C::kTile + kk * 2048, 16384, 1024), idAcc, (st > 0 || kk > 0) ? 1u : 0u);
+                 sdesc_sw128(aQcur + kk * 2048, 16384, 1024), idAcc, (st > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(&ctl.slot_empty[sq]);
+        mma_commit(&ctl.q_empty[st & 1]);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           if (D == 128)  // dQ^T = K^T dS^T  (both MN-major)
@@ -499,7 +520,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(&ctl.dq_full);
         trace_stamp(p.trace, st, 4);
-        sq = sq_next;
       }
       if (ok) mma_commit(&ctl.acc_full);
       if (*abort_flag) {
@@ -568,29 +588,36 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* o, co
     delta[bh * Nq_pad + q] = 0.0f;
   }
   // zero the dQ accumulator
-  const long long n4 = 1LL * B * Nq * Hq * D / 4;
+  const long long n4 = 1LL * B * Hq * D * Nq_pad / 4;
   for (long long i = tid; i < n4; i += nthreads) reinterpret_cast<float4*>(dq_acc)[i] = make_float4(0, 0, 0, 0);
 }
 
-__global__ void __launch_bounds__(256) bwd_post_kernel(const float* dq_acc, __nv_bfloat16* dq, long long n8,
-                                                       float scale) {
-  const long long i = 1LL * blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= n8) return;
-  const float4 a = reinterpret_cast<const float4*>(dq_acc)[2 * i];
-  const float4 b = reinterpret_cast<const float4*>(dq_acc)[2 * i + 1];
-  uint4 r;
-  r.x = pack_bf16x2(a.x * scale, a.y * scale);
-  r.y = pack_bf16x2(a.z * scale, a.w * scale);
-  r.z = pack_bf16x2(b.x * scale, b.y * scale);
-  r.w = pack_bf16x2(b.z * scale, b.w * scale);
-  reinterpret_cast<uint4*>(dq)[i] = r;
+// dq[b, q, h, :] = bf16(scale * acc[b*Hq + h, :, q]); one block per (32
+// query rows, b*Hq + h), transposed through shared memory.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_post_kernel(const float* dq_acc, __nv_bfloat16* dq, int Hq, int Nq,
+                                                       int Nq_pad, float scale) {
+  __shared__ float tile[D][33];
+  const int bh = blockIdx.y;
+  const int q0 = blockIdx.x * 32;
+  const float* src = dq_acc + size_t(bh) * D * Nq_pad + q0;
+  for (int i = threadIdx.x; i < D * 32; i += 256) tile[i >> 5][i & 31] = src[size_t(i >> 5) * Nq_pad + (i & 31)];
+  __syncthreads();
+  const int b = bh / Hq, h = bh - b * Hq;
+  for (int i = threadIdx.x; i < D * 16; i += 256) {
+    const int q = i / (D / 2), d2 = (i - q * (D / 2)) * 2;
+    const int qg = q0 + q;
+    if (qg < Nq)
+      *reinterpret_cast<uint32_t*>(dq + ((size_t(b) * Nq + qg) * Hq + h) * D + d2) =
+          pack_bf16x2(tile[d2][q] * scale, tile[d2 + 1][q] * scale);
+  }
 }
 
 template <int D, bool CAUSAL>
 cudaError_t launch_t(const Problem& pb, const void* o, const float* lse, const void* dout, void* dq, void* dk, void* dv,
                      float* ws, cudaStream_t stream) {
   const int Nq_pad = (pb.Nq + 127) / 128 * 128;
-  const size_t acc_elems = size_t(pb.B) * pb.Nq * pb.Hq * D;
+  const size_t acc_elems = size_t(pb.B) * pb.Hq * D * Nq_pad;
   float* dq_acc = ws;
   float* lse2 = ws + acc_elems;
   float* delta = lse2 + size_t(pb.B) * pb.Hq * Nq_pad;
@@ -610,6 +637,15 @@ cudaError_t launch_t(const Problem& pb, const void* o, const float* lse, const v
       !make_bshd_map(&mv, pb.v, pb.B, pb.Nk, pb.Hkv, D, 128) ||
       !make_bshd_map(&mdo, dout, pb.B, pb.Nq, pb.Hq, D, 128))
     return cudaErrorInvalidValue;
+  CUtensorMap macc;  // fp32 accumulator [B, Hq, D, Nq_pad], boxes of 32 q x 32 d
+  {
+    const uint64_t dims[4] = {uint64_t(Nq_pad), uint64_t(D), uint64_t(pb.Hq), uint64_t(pb.B)};
+    const uint64_t strides[3] = {uint64_t(Nq_pad) * 4, uint64_t(D) * Nq_pad * 4, uint64_t(pb.Hq) * D * Nq_pad * 4};
+    const uint32_t box[4] = {32, 32, 1, 1};
+    if (!encode_tiled(&macc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dq_acc, dims, strides, box,
+                      CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
   Params p;
   p.dk = static_cast<__nv_bfloat16*>(dk);
   p.dv = static_cast<__nv_bfloat16*>(dv);
@@ -639,13 +675,12 @@ cudaError_t launch_t(const Problem& pb, const void* o, const float* lse, const v
   if (e != cudaSuccess) return e;
   const unsigned grid = unsigned(pb.B) * pb.Hkv * p.n_ktiles;
   if (dc.ev_begin) cudaEventRecord(dc.ev_begin, stream);
-  kern<<<grid, kThreads, smem, stream>>>(mq, mk, mv, mdo, p);
+  kern<<<grid, kThreads, smem, stream>>>(mq, mk, mv, mdo, macc, p);
   e = cudaGetLastError();
   if (dc.ev_end) cudaEventRecord(dc.ev_end, stream);
   if (e != cudaSuccess) return e;
-  const long long n8 = (long long)acc_elems / 8;
-  bwd_post_kernel<<<unsigned((n8 + 255) / 256), 256, 0, stream>>>(dq_acc, static_cast<__nv_bfloat16*>(dq), n8,
-                                                                  pb.scale);
+  bwd_post_kernel<D><<<dim3(unsigned(Nq_pad / 32), unsigned(pb.B * pb.Hq)), 256, 0, stream>>>(
+      dq_acc, static_cast<__nv_bfloat16*>(dq), pb.Hq, pb.Nq, Nq_pad, pb.scale);
   return cudaGetLastError();
 }
 
@@ -653,7 +688,7 @@ cudaError_t launch_t(const Problem& pb, const void* o, const float* lse, const v
 
 size_t bwd_workspace_bytes(const Problem& p) {
   const size_t Nq_pad = size_t(p.Nq + 127) / 128 * 128;
-  return sizeof(float) * (size_t(p.B) * p.Nq * p.Hq * p.d + 2 * size_t(p.B) * p.Hq * Nq_pad);
+  return sizeof(float) * size_t(p.B) * p.Hq * Nq_pad * size_t(p.d + 2);
 }
 
 cudaError_t launch_bwd(const Problem& p, const void* o, const float* lse, const void* dout, void* dq, void* dk,

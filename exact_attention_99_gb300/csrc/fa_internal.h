@@ -37,6 +37,11 @@ unsigned* status_word();
 // box {64, 1, box_rows, 1}, 128-byte swizzle, zero fill out of range.
 bool make_bshd_map(CUtensorMap* m, const void* base, int B, int N, int H, int d, int box_rows);
 
+// Any tiled tensor map: rank <= 5, dims innermost first, strides (bytes) of
+// dims 1..rank-1, zero fill out of range.
+bool encode_tiled(CUtensorMap* m, CUtensorMapDataType dtype, int rank, const void* base, const uint64_t* dims,
+                  const uint64_t* strides, const uint32_t* box, CUtensorMapSwizzle swizzle);
+
 // Launchers. Return a cudaError_t (cudaSuccess on success).
 cudaError_t launch_fwd(const Problem& p, void* o, float* lse, cudaStream_t stream);
 // The host-side checks fa_bwd performs (pointers, sizes, device), as one call.

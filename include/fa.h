@@ -89,7 +89,7 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
  *   Workspace: a file-scope device array of FA_BWD_NOALLOC_SCRATCH_BYTES
  *     (64 MiB) inside the library. Every device that loads the library holds
  *     it until the process exits. The call needs
- *       4 * (B*Nq*Hq*d + 2*B*Hq*ceil(Nq/128)*128) bytes of it and returns
+ *       4 * B*Hq*ceil(Nq/128)*128 * (d + 2) bytes of it and returns
  *     FA_ERR_UNSUPPORTED, without enqueuing anything, when that exceeds the
  *     array.
  *   No cudaMalloc, cudaFree or other allocating routine is called.

@@ -57,7 +57,7 @@ def test_noalloc_matches_fa_bwd_twice(fa):
 
 
 def test_noalloc_rejects_workspace_beyond_the_array(fa):
-    # 4*(B*Nq*Hq*d + 2*B*Hq*Nq) bytes = 4*(33554432 + 524288) > 64 MiB
+    # 4 * B*Hq*Nq*(d + 2) bytes = 4 * 16*16384*130 > 64 MiB
     B, Hq, Hkv, N, d = 1, 16, 16, 16384, 128
     p = 1 << 20  # aligned, non-null: the size check fails before anything is launched
     assert fa.fa_bwd_noalloc(*([p] * 9), B, Hq, Hkv, N, N, d, d ** -0.5, 1) == FA_ERR_UNSUPPORTED
