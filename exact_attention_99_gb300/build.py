@@ -48,6 +48,8 @@ def build(force: bool = False, extra_flags: list[str] | None = None, verbose: bo
     os.makedirs(BUILD_DIR, exist_ok=True)
     cc = nvcc()
     flags = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-I", os.path.join(ROOT, "include")] + ARCH
+    if os.environ.get("FA_BUILD_TRACE") == "1":  # compile in the pipeline trace (fa_trace)
+        flags += ["-DFA_ENABLE_TRACE"]
     flags += list(extra_flags or [])
     if verbose:
         flags += ["-Xptxas", "-v"]

@@ -25,6 +25,7 @@ constexpr unsigned long long kDefaultWaitNs = 2000000000ull;
 
 std::mutex g_mu;
 int g_sms[kMaxDevices];
+cudaMemPool_t g_pool[kMaxDevices];
 unsigned* g_status_ptr[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 DebugCfg g_debug = {kDefaultWaitNs, 0, nullptr, nullptr, nullptr};
@@ -79,6 +80,30 @@ __global__ void debug_exp2_kernel(const float* x, float* y, int n, int mode) {
 }
 
 }  // namespace
+
+// Stream-ordered pool for the backward workspace, one per device, that
+// keeps freed memory for the next call (release threshold = max) instead of
+// returning it to the driver at every synchronisation.
+cudaMemPool_t workspace_pool() {
+  const int dev = current_device();
+  if (dev < 0) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_pool[dev] == nullptr) {
+    cudaMemPoolProps props = {};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    cudaMemPool_t pool = nullptr;
+    if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    uint64_t keep = ~0ull;
+    cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+    g_pool[dev] = pool;
+  }
+  return g_pool[dev];
+}
 
 DebugCfg debug_cfg() {
   std::lock_guard<std::mutex> lk(g_mu);
@@ -201,8 +226,9 @@ extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o
   if (st != FA_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   Problem p{q, k, v, B, Hq, Hkv, Nq, Nk, d, scale, causal};
+  cudaMemPool_t pool = workspace_pool();
   void* ws = nullptr;
-  if (cudaMallocAsync(&ws, bwd_workspace_bytes(p), s) != cudaSuccess) {
+  if (pool == nullptr || cudaMallocFromPoolAsync(&ws, bwd_workspace_bytes(p), pool, s) != cudaSuccess) {
     cudaGetLastError();
     return FA_ERR_ALLOC;
   }
@@ -252,6 +278,9 @@ extern "C" int fa_profile_events(void* begin, void* end) {
 }
 
 extern "C" int fa_trace(void* buf) {
+#ifndef FA_ENABLE_TRACE
+  if (buf != nullptr) return FA_ERR_UNSUPPORTED;
+#endif
   if (buf != nullptr && (reinterpret_cast<uintptr_t>(buf) & 7u) != 0) return FA_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lk(g_mu);
   g_debug.trace = static_cast<unsigned long long*>(buf);

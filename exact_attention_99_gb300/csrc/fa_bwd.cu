@@ -103,9 +103,18 @@ struct Work {
 template <bool CAUSAL>
 __device__ __forceinline__ Work decode(const Params& p) {
   Work w;
-  const int bk = p.B * p.Hkv;
-  w.j = blockIdx.x / bk;  // ascending key tile = descending work when causal
-  const int r = blockIdx.x - w.j * bk;
+  // causal: key tile major (ascending key tile = descending work, so the
+  // longest CTAs start first); non-causal: all key tiles of one head in a
+  // row, so concurrent CTAs share Q, dO and the dQ accumulator in L2
+  int r;
+  if (CAUSAL) {
+    const int bk = p.B * p.Hkv;
+    w.j = blockIdx.x / bk;
+    r = blockIdx.x - w.j * bk;
+  } else {
+    r = blockIdx.x / p.n_ktiles;
+    w.j = blockIdx.x - r * p.n_ktiles;
+  }
   w.b = r / p.Hkv;
   w.kvh = r - w.b * p.Hkv;
   w.i0 = 0;
@@ -592,24 +601,35 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* o, co
   for (long long i = tid; i < n4; i += nthreads) reinterpret_cast<float4*>(dq_acc)[i] = make_float4(0, 0, 0, 0);
 }
 
-// dq[b, q, h, :] = bf16(scale * acc[b*Hq + h, :, q]); one block per (32
-// query rows, b*Hq + h), transposed through shared memory.
+// dq[b, q, h, :] = bf16(scale * acc[b*Hq + h, :, q]). One thread per 8 d x
+// 4 q block: eight float4 loads (the two half-warps read the two halves of
+// each 32-byte sector), four 16-byte bf16 stores (16 consecutive threads
+// write one 256-byte row of dq).
 template <int D>
-__global__ void __launch_bounds__(256) bwd_post_kernel(const float* dq_acc, __nv_bfloat16* dq, int Hq, int Nq,
+__global__ void __launch_bounds__(256) bwd_post_kernel(const float* dq_acc, __nv_bfloat16* dq, int BH, int Hq, int Nq,
                                                        int Nq_pad, float scale) {
-  __shared__ float tile[D][33];
-  const int bh = blockIdx.y;
-  const int q0 = blockIdx.x * 32;
-  const float* src = dq_acc + size_t(bh) * D * Nq_pad + q0;
-  for (int i = threadIdx.x; i < D * 32; i += 256) tile[i >> 5][i & 31] = src[size_t(i >> 5) * Nq_pad + (i & 31)];
-  __syncthreads();
+  constexpr int kD8 = D / 8;
+  const long long t = 1LL * blockIdx.x * blockDim.x + threadIdx.x;
+  const long long per_bh = 1LL * kD8 * (Nq_pad / 4);
+  if (t >= per_bh * BH) return;
+  const int bh = int(t / per_bh);
+  const int r = int(t - bh * per_bh);
+  const int q4 = (r / kD8) * 4;
+  const int d8 = (r % kD8) * 8;
+  const float* src = dq_acc + (size_t(bh) * D + d8) * Nq_pad + q4;
+  float4 v[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) v[k] = *reinterpret_cast<const float4*>(src + size_t(k) * Nq_pad);
   const int b = bh / Hq, h = bh - b * Hq;
-  for (int i = threadIdx.x; i < D * 16; i += 256) {
-    const int q = i / (D / 2), d2 = (i - q * (D / 2)) * 2;
-    const int qg = q0 + q;
-    if (qg < Nq)
-      *reinterpret_cast<uint32_t*>(dq + ((size_t(b) * Nq + qg) * Hq + h) * D + d2) =
-          pack_bf16x2(tile[d2][q] * scale, tile[d2 + 1][q] * scale);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int q = q4 + j;
+    if (q >= Nq) break;
+    float f[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) f[k] = (j == 0 ? v[k].x : j == 1 ? v[k].y : j == 2 ? v[k].z : v[k].w) * scale;
+    *reinterpret_cast<uint4*>(dq + ((size_t(b) * Nq + q) * Hq + h) * D + d8) =
+        make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
   }
 }
 
@@ -679,8 +699,11 @@ cudaError_t launch_t(const Problem& pb, const void* o, const float* lse, const v
   e = cudaGetLastError();
   if (dc.ev_end) cudaEventRecord(dc.ev_end, stream);
   if (e != cudaSuccess) return e;
-  bwd_post_kernel<D><<<dim3(unsigned(Nq_pad / 32), unsigned(pb.B * pb.Hq)), 256, 0, stream>>>(
-      dq_acc, static_cast<__nv_bfloat16*>(dq), pb.Hq, pb.Nq, Nq_pad, pb.scale);
+  {
+    const long long threads = 1LL * pb.B * pb.Hq * (D / 8) * (Nq_pad / 4);
+    bwd_post_kernel<D><<<unsigned((threads + 255) / 256), 256, 0, stream>>>(
+        dq_acc, static_cast<__nv_bfloat16*>(dq), pb.B * pb.Hq, pb.Hq, pb.Nq, Nq_pad, pb.scale);
+  }
   return cudaGetLastError();
 }
 

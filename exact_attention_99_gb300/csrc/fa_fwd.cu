@@ -115,9 +115,17 @@ template <bool CAUSAL>
 __device__ __forceinline__ Unit decode_unit(const Params& p, int u) {
   Unit x;
   const int bh_count = p.B * p.Hq;
-  const int r = u / bh_count;
-  const int bh = u - r * bh_count;
-  // causal: longest units (last query blocks) first
+  // causal: rounds over all heads, longest units (last query blocks) first;
+  // non-causal: all query blocks of one head in a row, so the CTAs that run
+  // together share K and V through L2
+  int r, bh;
+  if (CAUSAL) {
+    r = u / bh_count;
+    bh = u - r * bh_count;
+  } else {
+    bh = u / p.n_mblocks;
+    r = u - bh * p.n_mblocks;
+  }
   const int mb = CAUSAL ? (p.n_mblocks - 1 - r) : r;
   x.b = bh / p.Hq;
   x.h = bh - x.b * p.Hq;

@@ -27,6 +27,10 @@ struct DebugCfg {
 };
 DebugCfg debug_cfg();
 
+// Per-device stream-ordered pool for the backward workspace (nullptr if it
+// could not be created).
+cudaMemPool_t workspace_pool();
+
 // Device properties cached per device.
 int num_sms();
 

@@ -27,11 +27,18 @@ __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
 
 // Optional pipeline trace (fa_trace in fa.h): stamp %globaltimer for (step,
 // point) of this CTA when a trace buffer is set and the CTA and step fall in
-// the traced window.
+// the traced window. Compiled in only with -DFA_ENABLE_TRACE: even unused,
+// the checks cost a few percent of kernel time.
 constexpr int kTraceCtas = 4, kTraceSteps = 64, kTracePoints = 16;
 __device__ __forceinline__ void trace_stamp(unsigned long long* buf, int step, int point) {
+#ifdef FA_ENABLE_TRACE
   if (buf != nullptr && blockIdx.x < kTraceCtas && step < kTraceSteps)
     buf[(blockIdx.x * kTraceSteps + step) * kTracePoints + point] = globaltimer_ns();
+#else
+  (void)buf;
+  (void)step;
+  (void)point;
+#endif
 }
 
 // --------------------------------------------------------------------------

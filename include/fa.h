@@ -71,8 +71,10 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
  *        inputs), dout [B,Nq,Hq,d] (bf16)
  *   out: dq [B,Nq,Hq,d], dk [B,Nk,Hkv,d], dv [B,Nk,Hkv,d] (bf16), fully written.
  * Allocates its fp32 workspace (dq accumulator, row terms D_i) with the
- * stream-ordered allocator on `stream` and frees it on the same stream;
- * returns FA_ERR_ALLOC if that fails. GQA gradients of dk/dv are summed over
+ * stream-ordered allocator on `stream`, from a memory pool the library keeps
+ * per device, and frees it on the same stream; the pool keeps freed memory
+ * (up to the largest workspace used so far) for later calls until the
+ * process exits. Returns FA_ERR_ALLOC if the allocation fails. GQA gradients of dk/dv are summed over
  * the query heads of each group inside the kernel.
  */
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout, void* dq,
@@ -149,7 +151,9 @@ int fa_profile_events(void* begin, void* end);
  *   first FA_TRACE_STEPS steps of that CTA; a step is one key tile of one
  *   unit (forward) or one query tile (backward). The points are listed in the
  *   kernels' sources. The buffer is owned by the caller; the library only
- *   writes it. Process-wide; not thread-safe.
+ *   writes it. Process-wide; not thread-safe. Available only in a library
+ *   built with -DFA_ENABLE_TRACE (the build's FA_BUILD_TRACE=1); otherwise a
+ *   non-NULL buffer returns FA_ERR_UNSUPPORTED.
  */
 #define FA_TRACE_CTAS 4
 #define FA_TRACE_STEPS 64
