@@ -19,7 +19,8 @@
 //     warps 0-3   softmax, stage 0      (one thread per query row)
 //     warps 4-7   softmax, stage 1
 //     warps 8-11  correction + epilogue (rescale O when a row max grows;
-//                                        O / l -> bf16, LSE)
+//                                        O / l -> bf16 staged in shared
+//                                        memory and written by TMA, LSE)
 //     warp 12     TMA producer          (Q per unit, K/V ring)
 //     warp 13     MMA issuer            (tcgen05.mma, one thread)
 //     warps 14-15 idle
@@ -54,12 +55,24 @@ constexpr int kMaxSlots = 8;
 #endif
 constexpr int kPolyEvery = FA_POLY_EVERY;
 
+// Rescale threshold (log2 units). A row's reference max m, to which O and l
+// are scaled, moves to the new row max only when that max exceeds m by more
+// than kTau; otherwise the block is exponentiated against the stale m, so
+// every unnormalised probability stays below 2^kTau. The result is the same
+// for any kTau (O, l and LSE all use the same m); kTau = 0 moves m on every
+// growth.
+#ifndef FA_RESCALE_TAU
+#define FA_RESCALE_TAU 8.0f
+#endif
+constexpr float kTau = FA_RESCALE_TAU;
+
 template <int D>
 struct Cfg {
   static constexpr int kChunks = D / 64;          // 64-wide swizzle atoms along d
   static constexpr int kTileBytes = 128 * D * 2;  // one 128-row tile of Q, K or V
   static constexpr int kSlots = D == 128 ? 4 : 8;
-  static constexpr int kSmemDyn = (2 + kSlots) * kTileBytes + 1024;
+  static constexpr int kStgBytes = 16384;  // O staging: 4 warps x [32 rows x 64 cols] bf16
+  static constexpr int kSmemDyn = (2 + kSlots) * kTileBytes + kStgBytes + 1024;
   static constexpr uint32_t kOCol0 = 256;
 };
 
@@ -161,13 +174,15 @@ __device__ __forceinline__ int unit_at(int round, int c) {
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV, const Params p) {
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                  const Params p) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ Ctl ctl;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;                          // 2 tiles
   uint8_t* sKV = smem + 2 * C::kTileBytes;     // kSlots tiles
+  uint8_t* sStg = sKV + C::kSlots * C::kTileBytes;  // O staging
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -257,7 +272,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           mD = fmax3(mD, u2f(x[c + 6]), u2f(x[c + 7]));
         }
         const float mx = fmaxf(fmaxf(mA, mB), fmaxf(mC, mD));
-        const float m_new = fmaxf(m_run, mx * sl);
+        const float m_cand = fmaxf(m_run, mx * sl);
+        const float m_new = (m_cand > m_run + kTau) ? m_cand : m_run;
         const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
         const float alpha = ex2_mufu(m_run - m_use);
         ctl.alpha[s][row] = alpha;
@@ -386,24 +402,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const float inv = l > 0.0f ? 1.0f / l : 0.0f;
         const uint32_t t_o = t_lane + C::kOCol0 + uint32_t(s * D);
+        // each warp stages its 32 rows x 64 columns (bf16, 128-byte swizzle)
+        // and writes them with one TMA store; rows past Nq are clipped
+        uint8_t* stg = sStg + wq * 4096;
+        const int wrow0 = un.row0 + s * 128 + wq * 32;
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld32(t_o + c * 32, v);
-          tmem_wait_ld();
-          uint32_t pk[16];
+        for (int hf = 0; hf < D / 64; ++hf) {
+          if (lane == 0) bulk_wait_read_all();  // the previous store has read the buffer
+          __syncwarp();
+#pragma unroll 1
+          for (int c2 = 0; c2 < 2; ++c2) {
+            uint32_t v[32];
+            tmem_ld32(t_o + hf * 64 + c2 * 32, v);
+            tmem_wait_ld();
+            uint32_t pk[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(u2f(v[2 * i]) * inv, u2f(v[2 * i + 1]) * inv);
-          if (valid) {
-            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+            for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(u2f(v[2 * i]) * inv, u2f(v[2 * i + 1]) * inv);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+            for (int i = 0; i < 4; ++i)
+              *reinterpret_cast<uint4*>(stg + lane * 128 + (((c2 * 4 + i) ^ (lane & 7)) << 4)) =
+                  make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && wrow0 < p.Nq) {
+            tma_store_4d(&tmO, stg, hf * 64, un.h, wrow0, un.b);
+            bulk_commit();
           }
         }
         if (valid) *lse_dst = l > 0.0f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
         tc_fence_before();
       }
     }
+    if (lane == 0) bulk_wait_all();  // stores complete (and staging reads done) before the CTA exits
   } else {
     setmaxnreg_dec<80>();
   }
@@ -526,6 +557,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             trace_stamp(p.trace, blk + j, s);
             issue_PV(s, vslot, j > 0);
             if (j == un.n[s] - 1) mma_commit(&ctl.o_full[s]);
+            // V_j is free once the last PV reading it completes: release it
+            // before the next S is issued so the refill starts earlier
+            if (s == 1 || j >= un.n[1]) mma_commit(&ctl.kv_empty[vslot]);
             if (j + 1 < un.n[s]) {
               trace_stamp(p.trace, blk + j, 2 + s);
               issue_S(s, kslot);
@@ -533,7 +567,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           if (!ok) break;
-          mma_commit(&ctl.kv_empty[vslot]);
           if (nxt) mma_commit(&ctl.kv_empty[kslot]);
           if (j + 2 == un.nb) mma_commit(&ctl.q_empty);
         }
@@ -560,9 +593,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D, bool CAUSAL>
 cudaError_t launch_t(const Problem& pb, void* o, float* lse, cudaStream_t stream) {
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   if (!make_bshd_map(&mq, pb.q, pb.B, pb.Nq, pb.Hq, D, 128) || !make_bshd_map(&mk, pb.k, pb.B, pb.Nk, pb.Hkv, D, 128) ||
-      !make_bshd_map(&mv, pb.v, pb.B, pb.Nk, pb.Hkv, D, 128))
+      !make_bshd_map(&mv, pb.v, pb.B, pb.Nk, pb.Hkv, D, 128) || !make_bshd_map(&mo, o, pb.B, pb.Nq, pb.Hq, D, 32))
     return cudaErrorInvalidValue;
   Params p;
   p.o = static_cast<__nv_bfloat16*>(o);
@@ -587,7 +620,7 @@ cudaError_t launch_t(const Problem& pb, void* o, float* lse, cudaStream_t stream
   if (e != cudaSuccess) return e;
   const int grid = p.n_units < num_sms() ? p.n_units : num_sms();
   if (dc.ev_begin) cudaEventRecord(dc.ev_begin, stream);
-  kern<<<grid, kThreads, Cfg<D>::kSmemDyn, stream>>>(mq, mk, mv, p);
+  kern<<<grid, kThreads, Cfg<D>::kSmemDyn, stream>>>(mq, mk, mv, mo, p);
   e = cudaGetLastError();
   if (dc.ev_end) cudaEventRecord(dc.ev_end, stream);
   return e;
