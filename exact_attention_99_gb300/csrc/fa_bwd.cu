@@ -15,8 +15,10 @@
 // Kernels:
 //   bwd_pre  : D_i and LSE * log2(e) per query row (padded to whole tiles),
 //              zero the fp32 dQ accumulator.
-//   bwd_main : one CTA per (batch, kv head, 128-key tile); loops over the
-//              query heads of the GQA group x 128-row query tiles.
+//   bwd_main : one CTA per (batch, kv head, 128-key tile) -- per pair of key
+//              tiles (j, n-1-j) when causal, so every CTA has the same work --
+//              looping over the query heads of the GQA group x 128-row query
+//              tiles that see the tile.
 //     warps 0-3  compute: one thread per key row; P^T = 2^(S^T*scale*log2e -
 //                LSE*log2e), dS^T = P^T o (dP^T - D)
 //     warps 4-7  dQ drain and the dK/dV epilogue. d = 128: dQ^T leaves TMEM
@@ -65,14 +67,30 @@ struct Cfg {
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
 };
 
+// A CTA's work: one or two key tiles ("items") of one (batch, kv head),
+// each visited against every query tile that sees it, for every query head
+// of the group.
+struct Item {
+  int j;      // key tile
+  int i0;     // first query tile that sees it
+  int nq;     // query tiles per head
+  int steps;  // group * nq
+};
+struct Work {
+  int b, kvh, n_items;
+  Item it[2];
+};
+
 struct __align__(8) Ctl {
   uint64_t kv_full;
   uint64_t q_full[2], q_empty[2], do_full, do_empty;
   uint64_t vec_full[2];
   uint64_t vec_empty[2];
+  uint64_t kv_empty, acc_empty;
   uint64_t s_full, p_full, dp_full, ds_full, dq_full, dq_empty, acc_full, drain;
   uint32_t tmem_base;
   uint32_t abort;
+  Work work;  // this CTA's items, decoded once
 };
 
 struct Params {
@@ -94,39 +112,47 @@ struct Params {
 //   drain    10 dQ^T ready, 11 dQ^T columns released, 12 reductions issued
 //   producer 13 Q slot free, 14 dO slot free
 
-struct Work {
-  int b, kvh, j;
-  int i0, nq;   // first query tile, query tiles per head
-  int steps;    // group * nq
-};
-
 template <bool CAUSAL>
 __device__ __forceinline__ Work decode(const Params& p) {
   Work w;
-  // causal: key tile major (ascending key tile = descending work, so the
-  // longest CTAs start first); non-causal: all key tiles of one head in a
-  // row, so concurrent CTAs share Q, dO and the dQ accumulator in L2
   int r;
   if (CAUSAL) {
-    const int bk = p.B * p.Hkv;
-    w.j = blockIdx.x / bk;
-    r = blockIdx.x - w.j * bk;
+    // key tiles j and n-1-j share a CTA: the pair always has n+1 query-tile
+    // steps (for Nq = Nk), so all CTAs carry the same work; heads in a row
+    const int n_pairs = (p.n_ktiles + 1) / 2;
+    r = blockIdx.x / n_pairs;
+    const int pr = blockIdx.x - r * n_pairs;
+    const int j2 = p.n_ktiles - 1 - pr;
+    w.it[0].j = pr;
+    w.it[1].j = j2;
+    w.n_items = j2 > pr ? 2 : 1;
   } else {
+    // all key tiles of one head in a row, so concurrent CTAs share Q, dO and
+    // the dQ accumulator in L2
     r = blockIdx.x / p.n_ktiles;
-    w.j = blockIdx.x - r * p.n_ktiles;
+    w.it[0].j = blockIdx.x - r * p.n_ktiles;
+    w.it[1].j = 0;
+    w.n_items = 1;
   }
   w.b = r / p.Hkv;
   w.kvh = r - w.b * p.Hkv;
-  w.i0 = 0;
-  if (CAUSAL) {
-    const int first_row = w.j * 128 - (p.Nk - p.Nq);  // first query row that sees key j*128
-    w.i0 = first_row <= 0 ? 0 : first_row / 128;
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    int i0 = 0;
+    if (CAUSAL) {
+      const int first_row = w.it[k].j * 128 - (p.Nk - p.Nq);  // first query row that sees the tile's first key
+      i0 = first_row <= 0 ? 0 : first_row / 128;
+    }
+    int nq = p.n_qtiles - i0;
+    if (nq < 0 || k >= w.n_items) nq = 0;
+    w.it[k].i0 = i0;
+    w.it[k].nq = nq;
+    w.it[k].steps = nq * p.group;
   }
-  w.nq = p.n_qtiles - w.i0;
-  if (w.nq < 0) w.nq = 0;
-  w.steps = w.nq * p.group;
   return w;
 }
+
+__device__ __forceinline__ Item pick(const Work& w, int k) { return w.it[k]; }
 
 // swizzled (128-byte) byte offset of element (row, col) in a [128 rows x 128
 // cols] bf16 tile stored as two 64-column atoms
@@ -161,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int wg = warp >> 2;
-  const Work w = decode<CAUSAL>(p);
+  const Work& w = ctl.work;  // read from shared memory to keep it out of every role's registers
   const uint64_t LIM = p.wait_limit_ns;
   volatile uint32_t* abort_flag = &ctl.abort;
 
@@ -171,6 +197,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (threadIdx.x == 0) {
     ctl.abort = 0;
+    ctl.work = decode<CAUSAL>(p);
     mbar_init(&ctl.kv_full, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ctl.q_full[i], 1);
@@ -189,6 +216,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&ctl.dq_full, 1);
     mbar_init(&ctl.dq_empty, 4);
     mbar_init(&ctl.acc_full, 1);
+    mbar_init(&ctl.kv_empty, 1);
+    mbar_init(&ctl.acc_empty, 4);
     mbar_init(&ctl.drain, 1);
     fence_mbar_init();
   }
@@ -212,99 +241,104 @@ __global__ void __launch_bounds__(kThreads, 1)
     setmaxnreg_inc<232>();
     const int row = ((warp & 3) << 5) + lane;  // key row within the tile
     const uint32_t t_lane = tmem + (uint32_t(warp & 3) << 21);
-    const int key = w.j * 128 + row;
-    const bool kvalid = key < p.Nk;  // keys past Nk are zero-filled: give them P = 0
     const int off = p.Nk - p.Nq;
     const float sl = p.scale_log2;
     uint32_t ph_s = 0, ph_dp = 0;
     bool ok = true;
-    for (int st = 0; st < w.steps && ok; ++st) {
-      const int it = w.i0 + st % w.nq;  // query tile
-      const int vs = st & 1;
-      const float* lse2 = sVec + vs * 256;
-      const float* dlt = lse2 + 128;
-      if (!mbar_wait_bounded(&ctl.vec_full[vs], (st >> 1) & 1, abort_flag, LIM)) { ok = false; break; }
-      if (threadIdx.x == 0) trace_stamp(p.trace, st, 5);
-      if (!mbar_wait_bounded(&ctl.s_full, ph_s, abort_flag, LIM)) { ok = false; break; }
-      ph_s ^= 1;
-      if (threadIdx.x == 0) trace_stamp(p.trace, st, 6);
-      tc_fence_after();
-      uint32_t x[128];
+    int g = 0;  // step counter across items
+    for (int ii = 0; ii < w.n_items && ok; ++ii) {
+      const Item I = pick(w, ii);
+      const int key = I.j * 128 + row;
+      const bool kvalid = key < p.Nk;  // keys past Nk are zero-filled: give them P = 0
+      for (int st = 0; st < I.steps && ok; ++st, ++g) {
+        const int it = I.i0 + st % I.nq;  // query tile
+        const int vs = g & 1;
+        const float* lse2 = sVec + vs * 256;
+        const float* dlt = lse2 + 128;
+        if (!mbar_wait_bounded(&ctl.vec_full[vs], (g >> 1) & 1, abort_flag, LIM)) { ok = false; break; }
+        if (threadIdx.x == 0) trace_stamp(p.trace, g, 5);
+        if (!mbar_wait_bounded(&ctl.s_full, ph_s, abort_flag, LIM)) { ok = false; break; }
+        ph_s ^= 1;
+        if (threadIdx.x == 0) trace_stamp(p.trace, g, 6);
+        tc_fence_after();
+        uint32_t x[128];
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
-        tmem_ld32(t_lane + C::kColS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&x[c * 32]));
-      tmem_wait_ld();
-      // causal: query row q sees this key iff q >= key - off
-      const bool need_mask = CAUSAL && (it * 128 < w.j * 128 + 127 - off);
-      const int qlim = key - off - it * 128;  // columns c < qlim are hidden
-      float pv[128];
-#pragma unroll
-      for (int c = 0; c < 128; c += 4) {
-        const float4 l4 = *reinterpret_cast<const float4*>(lse2 + c);
-        const uint64_t y0 = ffma2(pack2(u2f(x[c]), u2f(x[c + 1])), pack2(sl, sl), pack2(-l4.x, -l4.y));
-        const uint64_t y1 = ffma2(pack2(u2f(x[c + 2]), u2f(x[c + 3])), pack2(sl, sl), pack2(-l4.z, -l4.w));
-        float a0, a1, a2, a3;
-        unpack2(y0, a0, a1);
-        unpack2(y1, a2, a3);
-        pv[c] = ex2_mufu(a0);
-        pv[c + 1] = ex2_mufu(a1);
-        pv[c + 2] = ex2_mufu(a2);
-        pv[c + 3] = ex2_mufu(a3);
-        if (!kvalid) {
-          pv[c] = pv[c + 1] = pv[c + 2] = pv[c + 3] = 0.0f;
-        } else if (need_mask) {
-          if (c < qlim) pv[c] = 0.0f;
-          if (c + 1 < qlim) pv[c + 1] = 0.0f;
-          if (c + 2 < qlim) pv[c + 2] = 0.0f;
-          if (c + 3 < qlim) pv[c + 3] = 0.0f;
-        }
-      }
-      {
-        uint32_t pk[64];
-#pragma unroll
-        for (int c = 0; c < 64; ++c) pk[c] = pack_bf16x2(pv[2 * c], pv[2 * c + 1]);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_st16(t_lane + C::kColS + c * 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[c * 16]));
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (threadIdx.x == 0) trace_stamp(p.trace, st, 7);
-      if (lane == 0) mbar_arrive(&ctl.p_full);
-
-      // dS^T = P^T o (dP^T - D)
-      if (!mbar_wait_bounded(&ctl.dp_full, ph_dp, abort_flag, LIM)) { ok = false; break; }
-      ph_dp ^= 1;
-      if (threadIdx.x == 0) trace_stamp(p.trace, st, 8);
-      tc_fence_after();
-#pragma unroll
-      for (int c0 = 0; c0 < 128; c0 += 32) {
-        uint32_t g[32];
-        tmem_ld32(t_lane + C::kColDP + c0, g);
+        for (int c = 0; c < 4; ++c)
+          tmem_ld32(t_lane + C::kColS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&x[c * 32]));
         tmem_wait_ld();
+        // causal: query row q sees this key iff q >= key - off
+        const bool need_mask = CAUSAL && (it * 128 < I.j * 128 + 127 - off);
+        const int qlim = key - off - it * 128;  // columns c < qlim are hidden
+        float pv[128];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {  // 8 columns = one 16-byte unit
-          const int c = c0 + u * 8;
-          const float4 d0 = *reinterpret_cast<const float4*>(dlt + c);
-          const float4 d1 = *reinterpret_cast<const float4*>(dlt + c + 4);
-          const float dd[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
-          uint32_t pk[4];
-#pragma unroll
-          for (int e = 0; e < 8; e += 2) {
-            const float s0 = pv[c + e] * (u2f(g[u * 8 + e]) - dd[e]);
-            const float s1 = pv[c + e + 1] * (u2f(g[u * 8 + e + 1]) - dd[e + 1]);
-            pk[e >> 1] = pack_bf16x2(s0, s1);
-          }
-          *reinterpret_cast<uint4*>(sDs + sw128_off(row, c)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        for (int c = 0; c < 128; c += 4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(lse2 + c);
+          const uint64_t y0 = ffma2(pack2(u2f(x[c]), u2f(x[c + 1])), pack2(sl, sl), pack2(-l4.x, -l4.y));
+          const uint64_t y1 = ffma2(pack2(u2f(x[c + 2]), u2f(x[c + 3])), pack2(sl, sl), pack2(-l4.z, -l4.w));
+          float a0, a1, a2, a3;
+          unpack2(y0, a0, a1);
+          unpack2(y1, a2, a3);
+          pv[c] = ex2_mufu(a0);
+          pv[c + 1] = ex2_mufu(a1);
+          pv[c + 2] = ex2_mufu(a2);
+          pv[c + 3] = ex2_mufu(a3);
         }
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncwarp();
-      if (threadIdx.x == 0) trace_stamp(p.trace, st, 9);
-      if (lane == 0) {
-        mbar_arrive(&ctl.ds_full);
-        mbar_arrive(&ctl.vec_empty[vs]);
+        // masking only on diagonal tiles and past-the-end keys, in its own
+        // pass so the common case carries no per-element selects
+        if (need_mask || !kvalid) {
+          const int lim = kvalid ? qlim : 128;
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (c < lim) pv[c] = 0.0f;
+        }
+        {
+          uint32_t pk[64];
+#pragma unroll
+          for (int c = 0; c < 64; ++c) pk[c] = pack_bf16x2(pv[2 * c], pv[2 * c + 1]);
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            tmem_st16(t_lane + C::kColS + c * 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[c * 16]));
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (threadIdx.x == 0) trace_stamp(p.trace, g, 7);
+        if (lane == 0) mbar_arrive(&ctl.p_full);
+
+        // dS^T = P^T o (dP^T - D)
+        if (!mbar_wait_bounded(&ctl.dp_full, ph_dp, abort_flag, LIM)) { ok = false; break; }
+        ph_dp ^= 1;
+        if (threadIdx.x == 0) trace_stamp(p.trace, g, 8);
+        tc_fence_after();
+#pragma unroll
+        for (int c0 = 0; c0 < 128; c0 += 32) {
+          uint32_t gg[32];
+          tmem_ld32(t_lane + C::kColDP + c0, gg);
+          tmem_wait_ld();
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {  // 8 columns = one 16-byte unit
+            const int c = c0 + u * 8;
+            const float4 d0 = *reinterpret_cast<const float4*>(dlt + c);
+            const float4 d1 = *reinterpret_cast<const float4*>(dlt + c + 4);
+            const float dd[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+            uint32_t pk[4];
+#pragma unroll
+            for (int e = 0; e < 8; e += 2) {
+              const float s0 = pv[c + e] * (u2f(gg[u * 8 + e]) - dd[e]);
+              const float s1 = pv[c + e + 1] * (u2f(gg[u * 8 + e + 1]) - dd[e + 1]);
+              pk[e >> 1] = pack_bf16x2(s0, s1);
+            }
+            *reinterpret_cast<uint4*>(sDs + sw128_off(row, c)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (threadIdx.x == 0) trace_stamp(p.trace, g, 9);
+        if (lane == 0) {
+          mbar_arrive(&ctl.ds_full);
+          mbar_arrive(&ctl.vec_empty[vs]);
+        }
       }
     }
   } else if (wg == 1) {
@@ -312,144 +346,164 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int wq = warp & 3;
     const uint32_t t_lane = tmem + (uint32_t(wq) << 21);
     const int lr = (wq << 5) + lane;  // TMEM lane: d index (D=128) or query row (D=64)
-    uint32_t ph_dq = 0;
+    uint32_t ph_dq = 0, nacc = 0;
     bool ok = true;
-    for (int st = 0; st < w.steps && ok; ++st) {
-      const int it = w.i0 + st % w.nq;
-      const int h = w.kvh * p.group + st / w.nq;
-      if (!mbar_wait_bounded(&ctl.dq_full, ph_dq, abort_flag, LIM)) { ok = false; break; }
-      ph_dq ^= 1;
-      if (threadIdx.x == 128) trace_stamp(p.trace, st, 10);
-      tc_fence_after();
-      if (D == 128) {
-        uint32_t v[128];
+    int g = 0;
+    for (int ii = 0; ii < w.n_items && ok; ++ii) {
+      const Item I = pick(w, ii);
+      for (int st = 0; st < I.steps && ok; ++st, ++g) {
+        const int it = I.i0 + st % I.nq;
+        const int h = w.kvh * p.group + st / I.nq;
+        if (!mbar_wait_bounded(&ctl.dq_full, ph_dq, abort_flag, LIM)) { ok = false; break; }
+        ph_dq ^= 1;
+        if (threadIdx.x == 128) trace_stamp(p.trace, g, 10);
+        tc_fence_after();
+        if (D == 128) {
+          uint32_t v[128];
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-          tmem_ld32(t_lane + C::kColDP + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&v[c * 32]));
-        tmem_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl.dq_empty);
-        if (threadIdx.x == 128) trace_stamp(p.trace, st, 11);
-        // dQ^T: lane = d index, column = query row of the tile. Stage it as
-        // 128-byte-swizzled boxes of [32 d rows][32 q] fp32, two boxes per
-        // warp and half-tile, and add each box into the accumulator with a
-        // TMA reduction; the buffer is rewritten once the previous
-        // reductions have read it.
-        uint8_t* stg = smem + C::kOffStg + wq * 8192;
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          if (lane == 0) bulk_wait_read_all();
+          for (int c = 0; c < 4; ++c)
+            tmem_ld32(t_lane + C::kColDP + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&v[c * 32]));
+          tmem_wait_ld();
+          tc_fence_before();
           __syncwarp();
+          if (lane == 0) mbar_arrive(&ctl.dq_empty);
+          if (threadIdx.x == 128) trace_stamp(p.trace, g, 11);
+          // dQ^T: lane = d index, column = query row of the tile. Stage it as
+          // 128-byte-swizzled boxes of [32 d rows][32 q] fp32, two boxes per
+          // warp and half-tile, and add each box into the accumulator with a
+          // TMA reduction; the buffer is rewritten once the previous
+          // reductions have read it.
+          uint8_t* stg = smem + C::kOffStg + wq * 8192;
 #pragma unroll
-          for (int b2 = 0; b2 < 2; ++b2) {
-            const int qb = half * 2 + b2;
-            uint8_t* box = stg + b2 * 4096 + lane * 128;
+          for (int half = 0; half < 2; ++half) {
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
-              *reinterpret_cast<uint4*>(box + ((u ^ (lane & 7)) << 4)) =
-                  make_uint4(v[qb * 32 + 4 * u], v[qb * 32 + 4 * u + 1], v[qb * 32 + 4 * u + 2], v[qb * 32 + 4 * u + 3]);
+            for (int b2 = 0; b2 < 2; ++b2) {
+              const int qb = half * 2 + b2;
+              uint8_t* box = stg + b2 * 4096 + lane * 128;
+#pragma unroll
+              for (int u = 0; u < 8; ++u)
+                *reinterpret_cast<uint4*>(box + ((u ^ (lane & 7)) << 4)) =
+                    make_uint4(v[qb * 32 + 4 * u], v[qb * 32 + 4 * u + 1], v[qb * 32 + 4 * u + 2],
+                               v[qb * 32 + 4 * u + 3]);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+#pragma unroll
+              for (int b2 = 0; b2 < 2; ++b2)
+                tma_reduce_add_4d(&tmAcc, stg + b2 * 4096, it * 128 + (half * 2 + b2) * 32, wq * 32, h, w.b);
+              bulk_commit();
+            }
           }
-          fence_proxy_async_smem();
+          if (threadIdx.x == 128) trace_stamp(p.trace, g, 12);
+        } else {
+          uint32_t v[64];
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+            tmem_ld32(t_lane + C::kColDP + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&v[c * 32]));
+          tmem_wait_ld();
+          tc_fence_before();
           __syncwarp();
-          if (lane == 0) {
+          if (lane == 0) mbar_arrive(&ctl.dq_empty);
+          // dQ: lane = query row, 64 columns = d; for a fixed d the warp's
+          // lanes hit consecutive query rows of the accumulator
+          const int q = it * 128 + lr;
+          float* dst = p.dq_acc + (size_t(w.b) * p.Hq + h) * D * size_t(p.Nq_pad) + q;
 #pragma unroll
-            for (int b2 = 0; b2 < 2; ++b2)
-              tma_reduce_add_4d(&tmAcc, stg + b2 * 4096, it * 128 + (half * 2 + b2) * 32, wq * 32, h, w.b);
-            bulk_commit();
-          }
+          for (int c = 0; c < 64; ++c) red_add_f32(dst + size_t(c) * p.Nq_pad, u2f(v[c]));
         }
-        if (threadIdx.x == 128) trace_stamp(p.trace, st, 12);
-      } else {
-        uint32_t v[64];
-#pragma unroll
-        for (int c = 0; c < 2; ++c)
-          tmem_ld32(t_lane + C::kColDP + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&v[c * 32]));
-        tmem_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl.dq_empty);
-        // dQ: lane = query row, 64 columns = d; for a fixed d the warp's
-        // lanes hit consecutive query rows of the accumulator
-        const int q = it * 128 + lr;
-        float* dst = p.dq_acc + (size_t(w.b) * p.Hq + h) * D * size_t(p.Nq_pad) + q;
-#pragma unroll
-        for (int c = 0; c < 64; ++c) red_add_f32(dst + size_t(c) * p.Nq_pad, u2f(v[c]));
       }
-    }
-    if (D == 128 && lane == 0) bulk_wait_all();  // the accumulator is complete when the kernel ends
-    // epilogue: dV, dK rows of this key tile (lane = key row)
-    if (ok) {
-      const int key = w.j * 128 + lr;
+      if (!ok) break;
+      // epilogue of this item: dV, dK rows of its key tile (lane = key row)
+      const int key = I.j * 128 + lr;
       const bool valid = key < p.Nk;
       __nv_bfloat16* dv = p.dv + ((size_t(w.b) * p.Nk + key) * p.Hkv + w.kvh) * D;
       __nv_bfloat16* dk = p.dk + ((size_t(w.b) * p.Nk + key) * p.Hkv + w.kvh) * D;
-      if (w.steps == 0) {
+      if (I.steps == 0) {
         if (valid) {
           for (int c = 0; c < D / 8; ++c) {
             reinterpret_cast<uint4*>(dv)[c] = make_uint4(0, 0, 0, 0);
             reinterpret_cast<uint4*>(dk)[c] = make_uint4(0, 0, 0, 0);
           }
         }
-      } else if (mbar_wait_bounded(&ctl.acc_full, 0, abort_flag, LIM)) {
-        tc_fence_after();
+        continue;
+      }
+      if (!mbar_wait_bounded(&ctl.acc_full, nacc & 1, abort_flag, LIM)) { ok = false; break; }
+      ++nacc;
+      tc_fence_after();
 #pragma unroll 1
-        for (int t = 0; t < 2; ++t) {
-          const uint32_t col = t == 0 ? C::kColDV : C::kColDK;
-          const float mul = t == 0 ? 1.0f : p.scale;
-          __nv_bfloat16* dst = t == 0 ? dv : dk;
+      for (int t = 0; t < 2; ++t) {
+        const uint32_t col = t == 0 ? C::kColDV : C::kColDK;
+        const float mul = t == 0 ? 1.0f : p.scale;
+        __nv_bfloat16* dst = t == 0 ? dv : dk;
 #pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t v[32];
-            tmem_ld32(t_lane + col + c * 32, v);
-            tmem_wait_ld();
-            uint32_t pk[16];
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(t_lane + col + c * 32, v);
+          tmem_wait_ld();
+          uint32_t pk[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(u2f(v[2 * i]) * mul, u2f(v[2 * i + 1]) * mul);
-            if (valid) {
-              uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+          for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(u2f(v[2 * i]) * mul, u2f(v[2 * i + 1]) * mul);
+          if (valid) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
-              for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-            }
+            for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
           }
         }
       }
+      // the accumulators may now be overwritten by the next item
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl.acc_empty);
     }
+    if (D == 128 && lane == 0) bulk_wait_all();  // the accumulator is complete when the kernel ends
   } else {
     setmaxnreg_dec<104>();
   }
+  int total_steps = 0;
+#pragma unroll
+  for (int k = 0; k < 2; ++k) total_steps += w.it[k].steps;
   if (warp == 8) {
     // ------------------------------------------------------- TMA producer
-    if (lane == 0 && w.steps > 0) {
+    if (lane == 0 && total_steps > 0) {
       bool ok = true;
-      mbar_arrive_expect_tx(&ctl.kv_full, 2 * C::kTile);
+      int g = 0, nkv = 0;
+      for (int ii = 0; ii < w.n_items && ok; ++ii) {
+        const Item I = pick(w, ii);
+        if (I.steps == 0) continue;
+        if (nkv > 0 && !mbar_wait_bounded(&ctl.kv_empty, (nkv - 1) & 1, abort_flag, LIM)) { ok = false; break; }
+        ++nkv;
+        mbar_arrive_expect_tx(&ctl.kv_full, 2 * C::kTile);
 #pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
-        tma_load_4d(sK + c * 16384, &tmK, &ctl.kv_full, c * 64, w.kvh, w.j * 128, w.b);
-        tma_load_4d(sV + c * 16384, &tmV, &ctl.kv_full, c * 64, w.kvh, w.j * 128, w.b);
-      }
-      for (int st = 0; st < w.steps && ok; ++st) {
-        const int it = w.i0 + st % w.nq;
-        const int h = w.kvh * p.group + st / w.nq;
-        const int qs = st & 1;
-        if (!mbar_wait_bounded(&ctl.q_empty[qs], ((st >> 1) & 1) ^ 1, abort_flag, LIM)) { ok = false; break; }
-        trace_stamp(p.trace, st, 13);
-        mbar_arrive_expect_tx(&ctl.q_full[qs], C::kTile);
+        for (int c = 0; c < D / 64; ++c) {
+          tma_load_4d(sK + c * 16384, &tmK, &ctl.kv_full, c * 64, w.kvh, I.j * 128, w.b);
+          tma_load_4d(sV + c * 16384, &tmV, &ctl.kv_full, c * 64, w.kvh, I.j * 128, w.b);
+        }
+        for (int st = 0; st < I.steps && ok; ++st, ++g) {
+          const int it = I.i0 + st % I.nq;
+          const int h = w.kvh * p.group + st / I.nq;
+          const int qs = g & 1;
+          if (!mbar_wait_bounded(&ctl.q_empty[qs], ((g >> 1) & 1) ^ 1, abort_flag, LIM)) { ok = false; break; }
+          trace_stamp(p.trace, g, 13);
+          mbar_arrive_expect_tx(&ctl.q_full[qs], C::kTile);
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_4d(sQ + qs * C::kTile + c * 16384, &tmQ, &ctl.q_full[qs], c * 64, h, it * 128, w.b);
-        if (!mbar_wait_bounded(&ctl.do_empty, (st & 1) ^ 1, abort_flag, LIM)) { ok = false; break; }
-        trace_stamp(p.trace, st, 14);
-        mbar_arrive_expect_tx(&ctl.do_full, C::kTile);
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_4d(sQ + qs * C::kTile + c * 16384, &tmQ, &ctl.q_full[qs], c * 64, h, it * 128, w.b);
+          if (!mbar_wait_bounded(&ctl.do_empty, (g & 1) ^ 1, abort_flag, LIM)) { ok = false; break; }
+          trace_stamp(p.trace, g, 14);
+          mbar_arrive_expect_tx(&ctl.do_full, C::kTile);
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_4d(sDO + c * 16384, &tmDO, &ctl.do_full, c * 64, h, it * 128, w.b);
-        const int vs = st & 1;
-        if (!mbar_wait_bounded(&ctl.vec_empty[vs], ((st >> 1) & 1) ^ 1, abort_flag, LIM)) { ok = false; break; }
-        mbar_arrive_expect_tx(&ctl.vec_full[vs], 1024);
-        const size_t roff = (size_t(w.b) * p.Hq + h) * p.Nq_pad + size_t(it) * 128;
-        bulk_load(sVec + vs * 256, p.lse2 + roff, 512, &ctl.vec_full[vs]);
-        bulk_load(sVec + vs * 256 + 128, p.delta + roff, 512, &ctl.vec_full[vs]);
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_4d(sDO + c * 16384, &tmDO, &ctl.do_full, c * 64, h, it * 128, w.b);
+          const int vs = g & 1;
+          if (!mbar_wait_bounded(&ctl.vec_empty[vs], ((g >> 1) & 1) ^ 1, abort_flag, LIM)) { ok = false; break; }
+          mbar_arrive_expect_tx(&ctl.vec_full[vs], 1024);
+          const size_t roff = (size_t(w.b) * p.Hq + h) * p.Nq_pad + size_t(it) * 128;
+          bulk_load(sVec + vs * 256, p.lse2 + roff, 512, &ctl.vec_full[vs]);
+          bulk_load(sVec + vs * 256 + 128, p.delta + roff, 512, &ctl.vec_full[vs]);
+        }
       }
       if (*abort_flag) {
         const uint64_t t0 = globaltimer_ns();
@@ -458,14 +512,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 9) {
     // ---------------------------------------------------------- MMA issuer
-    if (lane == 0 && w.steps > 0) {
+    if (lane == 0 && total_steps > 0) {
       constexpr uint32_t idSS = idesc_bf16_f32(128, 128, 0, 0);     // S^T, dP^T
       constexpr uint32_t idAcc = idesc_bf16_f32(128, D, 0, 1);      // dV, dK
       constexpr uint32_t idDQ = D == 128 ? idesc_bf16_f32(128, 128, 1, 1) : idesc_bf16_f32(128, 64, 1, 1);
       const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aQ = smem_u32(sQ), aDO = smem_u32(sDO),
                      aDs = smem_u32(sDs);
-      bool ok = mbar_wait_bounded(&ctl.kv_full, 0, abort_flag, LIM);
+      bool ok = true;
       uint32_t ph_p = 0, ph_ds = 0, ph_dqe = 0;
+      int g = 0, nkv = 0;
       auto issue_kmajor = [&](uint32_t d_col, uint32_t a_base, uint32_t b_base) {  // [128 x 128] += A B^T, K = D
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -473,64 +528,77 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ss(tmem + d_col, sdesc_sw128(a_base + ko, 16, 1024), sdesc_sw128(b_base + ko, 16, 1024), idSS, kk > 0);
         }
       };
-      if (ok) ok = mbar_wait_bounded(&ctl.q_full[0], 0, abort_flag, LIM);
-      if (ok) {
+      for (int ii = 0; ii < w.n_items && ok; ++ii) {
+        const Item I = pick(w, ii);
+        if (I.steps == 0) continue;
+        ok = mbar_wait_bounded(&ctl.kv_full, nkv & 1, abort_flag, LIM);
+        if (ok) ok = mbar_wait_bounded(&ctl.q_full[g & 1], (g >> 1) & 1, abort_flag, LIM);
+        if (!ok) break;
+        ++nkv;
         tc_fence_after();
-        issue_kmajor(C::kColS, aK, aQ);  // S^T(0) = K Q_0^T
+        issue_kmajor(C::kColS, aK, aQ + (g & 1) * C::kTile);  // S^T = K Q^T for the item's first step
         mma_commit(&ctl.s_full);
-      }
-      for (int st = 0; st < w.steps && ok; ++st) {
-        const uint32_t aQcur = aQ + (st & 1) * C::kTile;
-        if (!mbar_wait_bounded(&ctl.do_full, st & 1, abort_flag, LIM)) { ok = false; break; }
-        if (st > 0) {
-          if (!mbar_wait_bounded(&ctl.dq_empty, ph_dqe, abort_flag, LIM)) { ok = false; break; }
-          ph_dqe ^= 1;
-        }
-        tc_fence_after();
-        trace_stamp(p.trace, st, 0);
-        issue_kmajor(C::kColDP, aV, aDO);  // dP^T = V dO^T
-        mma_commit(&ctl.dp_full);
-        if (!mbar_wait_bounded(&ctl.p_full, ph_p, abort_flag, LIM)) { ok = false; break; }
-        ph_p ^= 1;
-        trace_stamp(p.trace, st, 1);
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)  // dV += P^T dO   (P^T in TMEM, dO MN-major)
-          mma_ts(tmem + C::kColDV, tmem + C::kColS + kk * 8, sdesc_sw128(aDO + kk * 2048, 16384, 1024), idAcc,
-                 (st > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&ctl.do_empty);
-        if (st + 1 < w.steps) {
-          const int nx = (st + 1) & 1;
-          if (!mbar_wait_bounded(&ctl.q_full[nx], ((st + 1) >> 1) & 1, abort_flag, LIM)) { ok = false; break; }
-          trace_stamp(p.trace, st, 2);
+        for (int st = 0; st < I.steps && ok; ++st, ++g) {
+          const uint32_t aQcur = aQ + (g & 1) * C::kTile;
+          if (!mbar_wait_bounded(&ctl.do_full, g & 1, abort_flag, LIM)) { ok = false; break; }
+          if (g > 0) {
+            if (!mbar_wait_bounded(&ctl.dq_empty, ph_dqe, abort_flag, LIM)) { ok = false; break; }
+            ph_dqe ^= 1;
+          }
           tc_fence_after();
-          issue_kmajor(C::kColS, aK, aQ + nx * C::kTile);  // S^T(i+1)
-          mma_commit(&ctl.s_full);
-        }
-        if (!mbar_wait_bounded(&ctl.ds_full, ph_ds, abort_flag, LIM)) { ok = false; break; }
-        ph_ds ^= 1;
-        trace_stamp(p.trace, st, 3);
-        tc_fence_after();
+          trace_stamp(p.trace, g, 0);
+          issue_kmajor(C::kColDP, aV, aDO);  // dP^T = V dO^T
+          mma_commit(&ctl.dp_full);
+          if (!mbar_wait_bounded(&ctl.p_full, ph_p, abort_flag, LIM)) { ok = false; break; }
+          ph_p ^= 1;
+          // before the first dV of a later item overwrites the accumulators,
+          // the previous item's dK/dV must have been read out of TMEM
+          if (st == 0 && nkv > 1 && !mbar_wait_bounded(&ctl.acc_empty, (nkv - 2) & 1, abort_flag, LIM)) {
+            ok = false;
+            break;
+          }
+          trace_stamp(p.trace, g, 1);
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {  // dK += dS^T Q   (dS^T K-major, Q MN-major)
-          const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(tmem + C::kColDK, sdesc_sw128(aDs + ko, 16, 1024),
-                 sdesc_sw128(aQcur + kk * 2048, 16384, 1024), idAcc, (st > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(&ctl.q_empty[st & 1]);
+          for (int kk = 0; kk < 8; ++kk)  // dV += P^T dO   (P^T in TMEM, dO MN-major)
+            mma_ts(tmem + C::kColDV, tmem + C::kColS + kk * 8, sdesc_sw128(aDO + kk * 2048, 16384, 1024), idAcc,
+                   (st > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&ctl.do_empty);
+          if (st + 1 < I.steps) {
+            const int nx = (g + 1) & 1;
+            if (!mbar_wait_bounded(&ctl.q_full[nx], ((g + 1) >> 1) & 1, abort_flag, LIM)) { ok = false; break; }
+            trace_stamp(p.trace, g, 2);
+            tc_fence_after();
+            issue_kmajor(C::kColS, aK, aQ + nx * C::kTile);  // S^T for the next step
+            mma_commit(&ctl.s_full);
+          }
+          if (!mbar_wait_bounded(&ctl.ds_full, ph_ds, abort_flag, LIM)) { ok = false; break; }
+          ph_ds ^= 1;
+          trace_stamp(p.trace, g, 3);
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          if (D == 128)  // dQ^T = K^T dS^T  (both MN-major)
-            mma_ss(tmem + C::kColDP, sdesc_sw128(aK + kk * 2048, 16384, 1024), sdesc_sw128(aDs + kk * 2048, 16384, 1024),
-                   idDQ, kk > 0);
-          else  // dQ = dS K  (both MN-major)
-            mma_ss(tmem + C::kColDP, sdesc_sw128(aDs + kk * 2048, 16384, 1024), sdesc_sw128(aK + kk * 2048, 16384, 1024),
-                   idDQ, kk > 0);
+          for (int kk = 0; kk < 8; ++kk) {  // dK += dS^T Q   (dS^T K-major, Q MN-major)
+            const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
+            mma_ss(tmem + C::kColDK, sdesc_sw128(aDs + ko, 16, 1024), sdesc_sw128(aQcur + kk * 2048, 16384, 1024),
+                   idAcc, (st > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(&ctl.q_empty[g & 1]);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            if (D == 128)  // dQ^T = K^T dS^T  (both MN-major)
+              mma_ss(tmem + C::kColDP, sdesc_sw128(aK + kk * 2048, 16384, 1024),
+                     sdesc_sw128(aDs + kk * 2048, 16384, 1024), idDQ, kk > 0);
+            else  // dQ = dS K  (both MN-major)
+              mma_ss(tmem + C::kColDP, sdesc_sw128(aDs + kk * 2048, 16384, 1024),
+                     sdesc_sw128(aK + kk * 2048, 16384, 1024), idDQ, kk > 0);
+          }
+          mma_commit(&ctl.dq_full);
+          trace_stamp(p.trace, g, 4);
         }
-        mma_commit(&ctl.dq_full);
-        trace_stamp(p.trace, st, 4);
+        if (!ok) break;
+        mma_commit(&ctl.acc_full);  // dK, dV of this item are complete
+        mma_commit(&ctl.kv_empty);  // K, V of this item no longer read
       }
-      if (ok) mma_commit(&ctl.acc_full);
       if (*abort_flag) {
         mma_commit(&ctl.drain);
         const uint64_t t0 = globaltimer_ns();
@@ -693,7 +761,7 @@ cudaError_t launch_t(const Problem& pb, const void* o, const float* lse, const v
   auto kern = bwd_main_kernel<D, CAUSAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const unsigned grid = unsigned(pb.B) * pb.Hkv * p.n_ktiles;
+  const unsigned grid = unsigned(pb.B) * pb.Hkv * (CAUSAL ? (p.n_ktiles + 1) / 2 : p.n_ktiles);
   if (dc.ev_begin) cudaEventRecord(dc.ev_begin, stream);
   kern<<<grid, kThreads, smem, stream>>>(mq, mk, mv, mdo, macc, p);
   e = cudaGetLastError();
