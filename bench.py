@@ -47,6 +47,25 @@ def step_flops(w) -> float:
     return w.fwd_flops() + w.bwd_flops()
 
 
+def max_over_ranks(value: float) -> float:
+    """Largest `value` over all ranks (the job is as slow as its slowest rank).
+    Uses the process group's own device: CUDA for nccl, CPU for gloo."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(value)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(world: int, steps: int, flops_per_step: float, total_ms: float) -> float:
+    """Whole-job throughput: every rank runs `steps` steps of the same per-GPU
+    workload (weak scaling), and the job takes `total_ms` (max over ranks)."""
+    return world * steps * flops_per_step / (total_ms * 1e-3) / 1e12
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -309,11 +328,8 @@ def run_ours(args):
     total_ms = sum(step_ms)
     fwd_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(kf0, kf1))
     bwd_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(kb0, kb1))
-    if world > 1:
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    value = world * K * step_flops(w) / (total_ms * 1e-3) / 1e12
+    total_ms = max_over_ranks(total_ms)
+    value = job_tflops(world, K, step_flops(w), total_ms)
 
     # end to end through the public API: pinned host inputs in, results out
     host_in = {n: x[n].pin_memory() for n in ("q", "k", "v", "do")}
