@@ -521,11 +521,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       uint32_t ph_p = 0, ph_ds = 0, ph_dqe = 0;
       int g = 0, nkv = 0;
-      auto issue_kmajor = [&](uint32_t d_col, uint32_t a_base, uint32_t b_base) {  // [128 x 128] += A B^T, K = D
+      // Tile descriptors are built once; a K step is one add of a constant,
+      // so MMAs issue back to back (the tensor core idles otherwise).
+      const uint32_t kK = sdesc_lo(aK, 16), kV = sdesc_lo(aV, 16), kQ = sdesc_lo(aQ, 16);  // K-major
+      const uint32_t kDO = sdesc_lo(aDO, 16), kDs = sdesc_lo(aDs, 16);
+      const uint32_t mQ = sdesc_lo(aQ, 16384), mDO = sdesc_lo(aDO, 16384);  // MN-major
+      const uint32_t mK = sdesc_lo(aK, 16384), mDs = sdesc_lo(aDs, 16384);
+      auto issue_kmajor = [&](uint32_t d_col, uint32_t a0, uint32_t b0) {  // [128 x 128] += A B^T, K = D
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(tmem + d_col, sdesc_sw128(a_base + ko, 16, 1024), sdesc_sw128(b_base + ko, 16, 1024), idSS, kk > 0);
+          mma_ss_lo(tmem + d_col, sdesc_step(a0, ko), sdesc_step(b0, ko), idSS, kk > 0);
         }
       };
       for (int ii = 0; ii < w.n_items && ok; ++ii) {
@@ -536,10 +542,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         ++nkv;
         tc_fence_after();
-        issue_kmajor(C::kColS, aK, aQ + (g & 1) * C::kTile);  // S^T = K Q^T for the item's first step
+        issue_kmajor(C::kColS, kK, sdesc_step(kQ, (g & 1) * C::kTile));  // S^T = K Q^T for the item's first step
         mma_commit(&ctl.s_full);
         for (int st = 0; st < I.steps && ok; ++st, ++g) {
-          const uint32_t aQcur = aQ + (g & 1) * C::kTile;
+          const uint32_t mQcur = sdesc_step(mQ, (g & 1) * C::kTile);
           if (!mbar_wait_bounded(&ctl.do_full, g & 1, abort_flag, LIM)) { ok = false; break; }
           if (g > 0) {
             if (!mbar_wait_bounded(&ctl.dq_empty, ph_dqe, abort_flag, LIM)) { ok = false; break; }
@@ -547,7 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           trace_stamp(p.trace, g, 0);
-          issue_kmajor(C::kColDP, aV, aDO);  // dP^T = V dO^T
+          issue_kmajor(C::kColDP, kV, kDO);  // dP^T = V dO^T
           mma_commit(&ctl.dp_full);
           if (!mbar_wait_bounded(&ctl.p_full, ph_p, abort_flag, LIM)) { ok = false; break; }
           ph_p ^= 1;
@@ -561,7 +567,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)  // dV += P^T dO   (P^T in TMEM, dO MN-major)
-            mma_ts(tmem + C::kColDV, tmem + C::kColS + kk * 8, sdesc_sw128(aDO + kk * 2048, 16384, 1024), idAcc,
+            mma_ts_lo(tmem + C::kColDV, tmem + C::kColS + kk * 8, sdesc_step(mDO, kk * 2048), idAcc,
                    (st > 0 || kk > 0) ? 1u : 0u);
           mma_commit(&ctl.do_empty);
           if (st + 1 < I.steps) {
@@ -569,7 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait_bounded(&ctl.q_full[nx], ((g + 1) >> 1) & 1, abort_flag, LIM)) { ok = false; break; }
             trace_stamp(p.trace, g, 2);
             tc_fence_after();
-            issue_kmajor(C::kColS, aK, aQ + nx * C::kTile);  // S^T for the next step
+            issue_kmajor(C::kColS, kK, sdesc_step(kQ, nx * C::kTile));  // S^T for the next step
             mma_commit(&ctl.s_full);
           }
           if (!mbar_wait_bounded(&ctl.ds_full, ph_ds, abort_flag, LIM)) { ok = false; break; }
@@ -579,18 +585,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {  // dK += dS^T Q   (dS^T K-major, Q MN-major)
             const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
-            mma_ss(tmem + C::kColDK, sdesc_sw128(aDs + ko, 16, 1024), sdesc_sw128(aQcur + kk * 2048, 16384, 1024),
-                   idAcc, (st > 0 || kk > 0) ? 1u : 0u);
+            mma_ss_lo(tmem + C::kColDK, sdesc_step(kDs, ko), sdesc_step(mQcur, kk * 2048), idAcc,
+                   (st > 0 || kk > 0) ? 1u : 0u);
           }
           mma_commit(&ctl.q_empty[g & 1]);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             if (D == 128)  // dQ^T = K^T dS^T  (both MN-major)
-              mma_ss(tmem + C::kColDP, sdesc_sw128(aK + kk * 2048, 16384, 1024),
-                     sdesc_sw128(aDs + kk * 2048, 16384, 1024), idDQ, kk > 0);
+              mma_ss_lo(tmem + C::kColDP, sdesc_step(mK, kk * 2048), sdesc_step(mDs, kk * 2048), idDQ, kk > 0);
             else  // dQ = dS K  (both MN-major)
-              mma_ss(tmem + C::kColDP, sdesc_sw128(aDs + kk * 2048, 16384, 1024),
-                     sdesc_sw128(aK + kk * 2048, 16384, 1024), idDQ, kk > 0);
+              mma_ss_lo(tmem + C::kColDP, sdesc_step(mDs, kk * 2048), sdesc_step(mK, kk * 2048), idDQ, kk > 0);
           }
           mma_commit(&ctl.dq_full);
           trace_stamp(p.trace, g, 4);

@@ -500,22 +500,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t kv_it = 0, ph_q[2] = {0, 0}, ph_p[2] = {0, 0}, ph_o[2] = {0, 0};
       int blk = 0;
       bool ok = true;
+      // Tile descriptors are built once; a K step is one add of a constant,
+      // so MMAs issue back to back (the tensor core idles otherwise).
+      const uint32_t dQ = sdesc_lo(sQa, 16);      // Q tiles, K-major
+      const uint32_t dK = sdesc_lo(sKVa, 16);     // K tiles, K-major
+      const uint32_t dV = sdesc_lo(sKVa, 16384);  // V tiles, MN-major
       auto issue_S = [&](int s, uint32_t kslot) {
+        const uint32_t a0 = sdesc_step(dQ, s * C::kTileBytes);
+        const uint32_t b0 = sdesc_step(dK, kslot * C::kTileBytes);
+        const uint32_t d = tmem + uint32_t(s * 128);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
-          const uint64_t ad = sdesc_sw128(sQa + s * C::kTileBytes + koff, 16, 1024);
-          const uint64_t bd = sdesc_sw128(sKVa + kslot * C::kTileBytes + koff, 16, 1024);
-          mma_ss(tmem + uint32_t(s * 128), ad, bd, idS, kk > 0);
+          mma_ss_lo(d, sdesc_step(a0, koff), sdesc_step(b0, koff), idS, kk > 0);
         }
       };
       auto issue_PV = [&](int s, uint32_t vslot, bool acc) {
+        const uint32_t b0 = sdesc_step(dV, vslot * C::kTileBytes);
+        const uint32_t d = tmem + C::kOCol0 + uint32_t(s * D), a = tmem + uint32_t(s * 128);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t bd = sdesc_sw128(sKVa + vslot * C::kTileBytes + kk * 2048, 16384, 1024);
-          mma_ts(tmem + C::kOCol0 + uint32_t(s * D), tmem + uint32_t(s * 128 + kk * 8), bd, idPV,
-                 (acc || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts_lo(d, a + kk * 8, sdesc_step(b0, kk * 2048), idPV, (acc || kk > 0) ? 1u : 0u);
       };
       auto wait_kv = [&](uint32_t& slot) -> bool {
         slot = kv_it % C::kSlots;
