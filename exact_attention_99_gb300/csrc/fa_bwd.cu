@@ -311,12 +311,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (threadIdx.x == 0) trace_stamp(p.trace, g, 8);
         tc_fence_after();
 #pragma unroll
-        for (int c0 = 0; c0 < 128; c0 += 32) {
-          uint32_t gg[32];
-          tmem_ld32(t_lane + C::kColDP + c0, gg);
+        for (int c0 = 0; c0 < 128; c0 += 64) {
+          uint32_t gg[64];  // two loads in flight per wait
+          tmem_ld32(t_lane + C::kColDP + c0, *reinterpret_cast<uint32_t(*)[32]>(&gg[0]));
+          tmem_ld32(t_lane + C::kColDP + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(&gg[32]));
           tmem_wait_ld();
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {  // 8 columns = one 16-byte unit
+          for (int u = 0; u < 8; ++u) {  // 8 columns = one 16-byte unit
             const int c = c0 + u * 8;
             const float4 d0 = *reinterpret_cast<const float4*>(dlt + c);
             const float4 d1 = *reinterpret_cast<const float4*>(dlt + c + 4);
