@@ -84,6 +84,11 @@ struct Params {
   float scale_log2;
   int n_mblocks;
   int n_units;
+  // Row-split tail (non-causal): the units [n_full, n_units) of the last,
+  // partly filled round run as two work items each, one per 128-row stage,
+  // on twice as many CTAs; the work items are the n_full whole units
+  // followed by those halves, n_items in all.
+  int n_items, n_full;
   unsigned long long wait_limit_ns;
   int inject;
   unsigned* status;
@@ -96,6 +101,9 @@ struct Params {
 //   softmax s   4+3s S ready, 5+3s alpha published, 6+3s P stored
 //   correction  10+2s alpha seen, 11+2s O released for PV
 //   producer    14 K slot free, 15 V slot free
+// and, in the last step slot (kernel events): 0 entry, 1 set-up done,
+// 2 epilogue start (last unit), 6 teardown start, 7 exit.
+constexpr int kEv = kTraceSteps - 1;
 
 struct __align__(8) Ctl {
   uint64_t q_full[2];
@@ -125,8 +133,14 @@ struct Unit {
 };
 
 template <bool CAUSAL>
-__device__ __forceinline__ Unit decode_unit(const Params& p, int u) {
+__device__ __forceinline__ Unit decode_unit(const Params& p, int item) {
   Unit x;
+  int u = item, half = -1;
+  if (!CAUSAL && item >= p.n_full) {
+    const int k = item - p.n_full;
+    u = p.n_full + (k >> 1);
+    half = k & 1;
+  }
   const int bh_count = p.B * p.Hq;
   // causal: rounds over all heads, longest units (last query blocks) first;
   // non-causal: all query blocks of one head in a row, so the CTAs that run
@@ -160,6 +174,10 @@ __device__ __forceinline__ Unit decode_unit(const Params& p, int u) {
       x.n[s] = kmax < 0 ? 0 : (kmax >> 7) + 1;
     }
   }
+  if (half >= 0) {  // one stage of a row-split unit; the other item has the other rows
+    x.n[half ^ 1] = 0;
+    x.rows[half ^ 1] = false;
+  }
   x.nb = max(x.n[0], x.n[1]);
   return x;
 }
@@ -189,6 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int wg = warp >> 2;
   volatile uint32_t* abort_flag = &ctl.abort;
   const uint64_t LIM = p.wait_limit_ns;
+  if (threadIdx.x == 0) trace_stamp(p.trace, kEv, 0);
 
   if (threadIdx.x == 0) {
     ctl.abort = 0;
@@ -223,6 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl.tmem_base;
+  if (threadIdx.x == 0) trace_stamp(p.trace, kEv, 1);
 
   if (wg <= 1) {
     // ------------------------------------------------------------ softmax
@@ -236,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int rnd = 0; ok; ++rnd) {
       const int u = unit_at(rnd, blockIdx.x);
-      if (u >= p.n_units) break;
+      if (u >= p.n_items) break;
       const Unit un = decode_unit<CAUSAL>(p, u);
       const int n = un.n[s];
       const int blk0 = blk;
@@ -336,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int rnd = 0; ok; ++rnd) {
       const int u = unit_at(rnd, blockIdx.x);
-      if (u >= p.n_units) break;
+      if (u >= p.n_items) break;
       const Unit un = decode_unit<CAUSAL>(p, u);
       const int blk0 = blk;
       blk += un.nb;
@@ -376,6 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       // epilogue: O / l -> bf16, LSE
+      if (row == 0) trace_stamp(p.trace, kEv, 2);
 #pragma unroll 1
       for (int s = 0; s < 2; ++s) {
         if (!un.rows[s]) continue;
@@ -447,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool injected = false;
       for (int rnd = 0; ok; ++rnd) {
         const int u = unit_at(rnd, blockIdx.x);
-        if (u >= p.n_units) break;
+        if (u >= p.n_items) break;
         const Unit un = decode_unit<CAUSAL>(p, u);
         if (un.nb == 0) continue;
         if (!first) {
@@ -530,7 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       for (int rnd = 0; ok; ++rnd) {
         const int u = unit_at(rnd, blockIdx.x);
-        if (u >= p.n_units) break;
+        if (u >= p.n_items) break;
         const Unit un = decode_unit<CAUSAL>(p, u);
         if (un.nb == 0) continue;
         for (int s = 0; s < 2 && ok; ++s) {
@@ -588,12 +609,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // ------------------------------------------------------------- teardown
+  if (warp == 8 && lane == 0) trace_stamp(p.trace, kEv, 6);
   __syncwarp();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   if (warp == 13) tmem_dealloc(tmem, 512);
   if (threadIdx.x == 0 && ctl.abort) atomicOr(p.status, kDevTimeout);
+  if (threadIdx.x == 0) trace_stamp(p.trace, kEv, 7);
 }
 
 template <int D, bool CAUSAL>
@@ -614,6 +637,17 @@ cudaError_t launch_t(const Problem& pb, void* o, float* lse, cudaStream_t stream
   p.scale_log2 = pb.scale * 1.4426950408889634f;
   p.n_mblocks = (pb.Nq + 255) / 256;
   p.n_units = p.n_mblocks * pb.B * pb.Hq;
+  // Row-split tail: when the T = n_units mod G units of the last round fit
+  // on G CTAs twice over, each runs as two single-stage items (its two
+  // 128-row halves). A single-stage item has no second stage to overlap its
+  // softmax with, but takes well under a whole unit's time, so the last
+  // round ends sooner. Causal units stay whole: their longest-first order
+  // already fills the last round with short units.
+  const int G = num_sms();
+  const int T = p.n_units % G;
+  const int n_split = (!CAUSAL && T > 0 && 2 * T <= G && pb.Nq > 128) ? T : 0;
+  p.n_full = p.n_units - n_split;
+  p.n_items = p.n_full + 2 * n_split;
   const DebugCfg dc = debug_cfg();
   p.wait_limit_ns = dc.wait_limit_ns;
   p.inject = dc.inject;
@@ -623,7 +657,7 @@ cudaError_t launch_t(const Problem& pb, void* o, float* lse, cudaStream_t stream
   auto kern = fa_fwd_kernel<D, CAUSAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmemDyn);
   if (e != cudaSuccess) return e;
-  const int grid = p.n_units < num_sms() ? p.n_units : num_sms();
+  const int grid = p.n_items < G ? p.n_items : G;
   if (dc.ev_begin) cudaEventRecord(dc.ev_begin, stream);
   kern<<<grid, kThreads, Cfg<D>::kSmemDyn, stream>>>(mq, mk, mv, mo, p);
   e = cudaGetLastError();

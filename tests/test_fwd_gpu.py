@@ -63,6 +63,36 @@ def test_small_shapes(fa, shape, causal):
     run_case(fa, B, Hq, Hkv, Nq, Nk, d, causal, seed=hash((shape, causal)) % 10000)
 
 
+def split_plan(n_sms, B, Hq, Nq, causal):
+    """Which units the forward runs as two single-stage (128-row) items: the
+    T = units mod SMs units of the last, partly filled round, when 2T <= SMs
+    (non-causal, Nq > 128 only). Returns T, or 0 for no split."""
+    units = B * Hq * ((Nq + 255) // 256)
+    t = units % n_sms
+    return t if (t and 2 * t <= n_sms and not causal and Nq > 128) else 0
+
+
+SPLIT = [
+    # B, Hq, Hkv, Nq, Nk, d, units split on a 152-SM GB300
+    (1, 2, 2, 300, 700, 128, 4),    # ragged Nq (the last unit holds 44 rows, all in its first half) and Nk
+    (1, 40, 40, 256, 1000, 64, 40),
+    (1, 54, 6, 768, 640, 128, 10),  # 162 units: a full round, then 10 split units (GQA)
+    (2, 36, 4, 512, 384, 128, 0),   # 144 units: more than half the SMs, no split
+    (1, 2, 2, 128, 384, 64, 0),     # one 128-row block: nothing to split
+]
+
+
+@pytest.mark.parametrize("shape", SPLIT, ids=lambda s: "x".join(map(str, s)))
+def test_row_split_tail(fa, shape):
+    """Non-causal units of the last round run as one item per 128-row stage;
+    parity against the oracle with and without that split."""
+    B, Hq, Hkv, Nq, Nk, d, t152 = shape
+    n_sms = torch.cuda.get_device_properties(0).multi_processor_count
+    if n_sms == 152:
+        assert split_plan(n_sms, B, Hq, Nq, False) == t152
+    run_case(fa, B, Hq, Hkv, Nq, Nk, d, False, seed=sum(shape))
+
+
 def test_workload_small_full(fa):
     w = workloads.WORKLOADS[0]
     run_case(fa, w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.d, w.causal, w.seed, w.sigma_qk)
@@ -119,12 +149,13 @@ def test_zero_q_mean(fa):
     assert (lse.double().cpu() - want[None, None]).abs().max().item() <= 1e-3
 
 
-def test_deterministic_and_offset_invariant(fa):
+@pytest.mark.parametrize("causal", [True, False])  # non-causal: 16 units, each run as two 128-row items
+def test_deterministic_and_offset_invariant(fa, causal):
     B, Hq, Hkv, N, d = 2, 4, 2, 384, 128
     x = workloads.make_inputs(B, Hq, Hkv, N, N, d, seed=9)
     q, k, v = (x[n].cuda() for n in ("q", "k", "v"))
-    o1, l1 = fa.forward(q, k, v, causal=True)
-    o2, l2 = fa.forward(q, k, v, causal=True)
+    o1, l1 = fa.forward(q, k, v, causal=causal)
+    o2, l2 = fa.forward(q, k, v, causal=causal)
     # same tensors placed at a 16-byte-aligned offset inside larger buffers
     pad = 8
     bufs = []
@@ -132,7 +163,7 @@ def test_deterministic_and_offset_invariant(fa):
         big = torch.empty(t.numel() + pad, dtype=t.dtype, device=t.device)
         big[pad:].copy_(t.reshape(-1))
         bufs.append(big[pad:].view(t.shape))
-    o3, l3 = fa.forward(*bufs, causal=True)
+    o3, l3 = fa.forward(*bufs, causal=causal)
     torch.cuda.synchronize()
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
     assert torch.equal(o1, o3) and torch.equal(l1, l3)
