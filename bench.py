@@ -105,8 +105,10 @@ def profiled_traffic(kernel: str, workload: str):
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons while running."""
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples of SM clock and throttle reasons, every 50 ms; only
+    the samples whose timestamps fall inside the timed window (mark_begin /
+    mark_end) are summarised."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -114,11 +116,18 @@ class ClockSampler:
         self.dev = device_index
         self.lines = []
         self.proc = None
+        self.t_begin = self.t_end = None
+
+    def mark_begin(self):
+        self.t_begin = time.time()
+
+    def mark_end(self):
+        self.t_end = time.time()
 
     def start(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                                          "-lms", "200", "-i", str(self.dev)], stdout=subprocess.PIPE,
+                                          "-lms", "50", "-i", str(self.dev)], stdout=subprocess.PIPE,
                                          stderr=subprocess.DEVNULL, text=True)
             threading.Thread(target=self._read, daemon=True).start()
         except (OSError, FileNotFoundError):
@@ -137,11 +146,18 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
+        import datetime
         sm, mx, reasons, power = [], [], set(), []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in self.lines:
             parts = [x.strip() for x in line.split(",")]
             if len(parts) < 9:
+                continue
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                continue
+            if self.t_begin is not None and not (self.t_begin <= ts <= self.t_end):
                 continue
             try:
                 sm.append(float(parts[1]))
@@ -153,9 +169,10 @@ class ClockSampler:
                 if flag.lower().startswith("active"):
                     reasons.add(n)
         if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples in the timed window"], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "power_w_max": max(power), "samples": len(sm)}
+                "power_w_median": statistics.median(power), "power_w_max": max(power), "samples": len(sm),
+                "window_s": round(self.t_end - self.t_begin, 3)}
 
 
 def oracle_sample(w, x, seconds: float, max_heads: int | None = None, first: int = 0):
@@ -312,12 +329,14 @@ def run_ours(args):
     sampler.start()
     time.sleep(0.2)
     torch.cuda.synchronize()
+    sampler.mark_begin()
     for i in range(K):
         flush.zero_()
         e0[i].record()
         step(i)
         e1[i].record()
     torch.cuda.synchronize()
+    sampler.mark_end()
     if world > 1:
         dist.barrier()
     clocks = sampler.stop()
@@ -402,16 +421,48 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_profile_target(args):
+    """Profiling target: runs only the forward or only the backward of one
+    named workload, --warmup + --steps times, and prints nothing else. Used
+    to capture one kernel of one workload under ncu; prints no bench line."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import exact_attention_99_gb300 as fa
+    fa.fa_debug_set(0, 0)
+    byname = {w.name: w for w in workloads.WORKLOADS}
+    w = byname[args.profile_workload]
+    x = workloads.workload_inputs(w, with_dout=True)
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
+    o, dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    lse = torch.empty((w.B, w.Hq, w.Nq), device="cuda", dtype=torch.float32)
+    a = (w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.d, w.scale, int(w.causal))
+    if fa.fa_fwd(q, k, v, o, lse, *a):
+        raise RuntimeError("fa_fwd failed")
+    for _ in range(args.warmup + args.steps):
+        st = fa.fa_fwd(q, k, v, o, lse, *a) if args.profile_pass == "fwd" else \
+            fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, *a)
+        if st:
+            raise RuntimeError(f"launch failed: {st}")
+    torch.cuda.synchronize()
+    if fa.fa_get_status() != 0:
+        raise RuntimeError("device status not OK")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=400)  # about 0.4 s timed: long enough to sample clocks
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--profile-workload", default=None, help="profiling target: run one workload's pass only")
+    ap.add_argument("--profile-pass", choices=["fwd", "bwd"], default="fwd")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
-    if args.impl == "reference":
+    if args.profile_workload:
+        run_profile_target(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
