@@ -250,8 +250,10 @@ def time_one(fn, flush, reps=5, warm=2):
 
 
 def per_config(fa, flush, peak):
-    """Forward TFLOP/s of the four forward workloads and backward TFLOP/s of
-    the backward workload (kernel-only, inputs resident, L2 flushed)."""
+    """Forward TFLOP/s of every workload; backward TFLOP/s (preprocess, main
+    kernel and dQ convert) of the backward workload, the headline workload
+    and, at scale for grouped-query heads, the causal GQA workload
+    (kernel-only, inputs resident, L2 flushed)."""
     import torch
     out = {}
     for w in workloads.WORKLOADS:
@@ -263,7 +265,7 @@ def per_config(fa, flush, peak):
         ms = time_one(fwd, flush)
         ent = {"fwd_ms": ms, "fwd_tflops": w.fwd_flops() / ms / 1e9}
         ent["fwd_frac_of_peak"] = ent["fwd_tflops"] / peak
-        if w.direction == "bwd" or w is MAIN:
+        if w.direction == "bwd" or w is MAIN or w.Hkv < w.Hq:
             dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
             bwd = lambda: fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.d, w.scale,
                                     int(w.causal))

@@ -9,7 +9,7 @@ import torch
 
 import workloads
 from oracle import attn_ref
-from tests.gpu_util import assert_close, to64
+from tests.gpu_util import assert_close, assert_close_scaled, to64
 
 pytestmark = pytest.mark.gpu
 
@@ -105,3 +105,49 @@ def test_gradient_identities_on_gpu(fa):
     want = x["do"].double().sum(dim=1)
     assert (dv.double().cpu().sum(dim=1) - want).abs().max().item() <= 0.5
     assert dk.double().cpu().sum(dim=1).abs().max().item() <= 0.5
+
+
+def test_gqa_causal_full_size_one_group(fa):
+    """GQA backward at scale: the causal GQA workload's shape (B=1, Hq=32,
+    Hkv=8, N=16384) with the backward workload's input distribution (all
+    N(0,1)), run whole on the GPU; the oracle recomputes every gradient of
+    one kv group (kv head 5 and its query heads 20-23), dK and dV summed over
+    the group. dV and dK of the first keys sum over all 4 x 16384 queries of
+    the group and reach |x| of 4-8, where one bf16 ulp is 0.03 and output
+    rounding alone costs up to 1.6e-2, so the elementwise bound grows with
+    the value (assert_close_scaled); mean-abs stays at 2e-3."""
+    w = workloads.WORKLOADS[3]
+    x = workloads.make_inputs(w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.d, w.seed, with_dout=True)
+    dq, dk, dv = gpu_grads(fa, x, w.causal, w.scale)
+    g = w.Hq // w.Hkv
+    kvh = 5
+    hs = slice(kvh * g, (kvh + 1) * g)
+    qs, dos = (x[n][:, :, hs].double().numpy() for n in ("q", "do"))
+    ks, vs = (x[n][:, :, kvh:kvh + 1].double().numpy() for n in ("k", "v"))
+    rdq, rdk, rdv = attn_ref.backward(qs, ks, vs, dos, w.scale, w.causal)
+    assert_close_scaled("dq[group 5]", to64(dq[:, :, hs]), rdq)
+    assert_close_scaled("dk[kv 5]", to64(dk[:, :, kvh:kvh + 1]), rdk)
+    assert_close_scaled("dv[kv 5]", to64(dv[:, :, kvh:kvh + 1]), rdv)
+    for t in (dq, dk, dv):
+        assert torch.isfinite(t).all()
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_ragged_lengths_at_scale(fa, causal):
+    """Nq != Nk, neither a multiple of 128, GQA, both passes, every element
+    against the oracle (bottom-right causal alignment: the first
+    Nk - Nq keys are visible to every row)."""
+    B, Hq, Hkv, Nq, Nk, d = 1, 8, 2, 3000, 5000, 128
+    x = workloads.make_inputs(B, Hq, Hkv, Nq, Nk, d, seed=24 + int(causal), with_dout=True)
+    scale = d ** -0.5
+    q, k, v = (x[n].cuda() for n in ("q", "k", "v"))
+    o, lse = fa.forward(q, k, v, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    ro, rlse = attn_ref.forward(*(x[n].double().numpy() for n in ("q", "k", "v")), scale, causal)
+    assert_close("o", to64(o), ro)
+    assert_close("lse", to64(lse), rlse, max_tol=1e-3, mean_tol=1e-3)
+    dq, dk, dv = gpu_grads(fa, x, causal, scale)
+    rdq, rdk, rdv = attn_ref.backward(*(x[n].double().numpy() for n in ("q", "k", "v", "do")), scale, causal)
+    assert_close("dq", to64(dq), rdq)
+    assert_close("dk", to64(dk), rdk)
+    assert_close("dv", to64(dv), rdv)
