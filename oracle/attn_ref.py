@@ -37,6 +37,12 @@ What it computes (the plain definition, written out):
 Readings where the pages are silent:
   * causal alignment is bottom-right: key j is visible to query i iff
     j <= i + (Nk - Nq); with Nq == Nk this is j <= i;
+  * sliding windows (local attention; the FlashAttention-4 article and the
+    FA-2 notes name variable and sliding-window masks without defining
+    them): with the same bottom-right offset, key j is visible to query i
+    iff i + off - window_left <= j <= i + off + window_right, off = Nk - Nq,
+    a negative bound meaning no limit on that side; causal is
+    window_right = 0 with no left limit;
   * grouped-query attention maps query head h to kv head h // (Hq // Hkv);
   * a row with no visible key has O = 0 and LSE = -inf and contributes no
     gradient.
@@ -59,19 +65,35 @@ def _group(hq: int, hkv: int) -> int:
     return hq // hkv
 
 
-def visible_mask(rows: np.ndarray, nq: int, nk: int, causal: bool) -> np.ndarray:
-    """Boolean [len(rows), nk]: True where key j is visible to query row i."""
-    rows = np.asarray(rows, dtype=np.int64)
-    if not causal:
-        return np.ones((rows.shape[0], nk), dtype=bool)
-    j = np.arange(nk, dtype=np.int64)[None, :]
-    return j <= rows[:, None] + (nk - nq)
-
-
-def _scores(Q: np.ndarray, K: np.ndarray, scale: float, rows: np.ndarray, nq: int, causal: bool) -> np.ndarray:
-    S = scale * (Q @ K.T)
+def _window(causal: bool, window):
+    """(left, right) bounds, negative = unbounded; causal forces right = 0."""
+    wl, wr = (-1, -1) if window is None else (int(window[0]), int(window[1]))
     if causal:
-        S = np.where(visible_mask(rows, nq, K.shape[0], causal), S, -np.inf)
+        wr = 0 if wr < 0 else min(wr, 0)
+    return wl, wr
+
+
+def visible_mask(rows: np.ndarray, nq: int, nk: int, causal: bool, window=None) -> np.ndarray:
+    """Boolean [len(rows), nk]: True where key j is visible to query row i.
+    ``window`` = (left, right) as in the module notes (None: no window)."""
+    rows = np.asarray(rows, dtype=np.int64)
+    wl, wr = _window(causal, window)
+    j = np.arange(nk, dtype=np.int64)[None, :]
+    diag = rows[:, None] + (nk - nq)
+    vis = np.ones((rows.shape[0], nk), dtype=bool)
+    if wr >= 0:
+        vis &= j <= diag + wr
+    if wl >= 0:
+        vis &= j >= diag - wl
+    return vis
+
+
+def _scores(Q: np.ndarray, K: np.ndarray, scale: float, rows: np.ndarray, nq: int, causal: bool,
+            window=None) -> np.ndarray:
+    S = scale * (Q @ K.T)
+    wl, wr = _window(causal, window)
+    if wl >= 0 or wr >= 0:
+        S = np.where(visible_mask(rows, nq, K.shape[0], causal, window), S, -np.inf)
     return S
 
 
@@ -93,19 +115,20 @@ def _softmax_grad(P: np.ndarray, dP: np.ndarray, D: np.ndarray) -> np.ndarray:
     return P * (dP - D[:, None])
 
 
-def probabilities(Q: np.ndarray, K: np.ndarray, scale: float, causal: bool) -> np.ndarray:
+def probabilities(Q: np.ndarray, K: np.ndarray, scale: float, causal: bool, window=None) -> np.ndarray:
     """P for one head: Q [Nq, d], K [Nk, d] -> [Nq, Nk] (fp64)."""
     Q = np.asarray(Q, dtype=np.float64)
     K = np.asarray(K, dtype=np.float64)
     nq = Q.shape[0]
-    S = _scores(Q, K, scale, np.arange(nq), nq, causal)
+    S = _scores(Q, K, scale, np.arange(nq), nq, causal, window)
     P, _ = _softmax_stats(S)
     return P
 
 
-def forward(q, k, v, scale: float, causal: bool, rows=None):
+def forward(q, k, v, scale: float, causal: bool, rows=None, window=None):
     """O and LSE. ``rows`` optionally restricts the query rows computed
-    (indices into Nq); the outputs then have len(rows) in place of Nq."""
+    (indices into Nq); the outputs then have len(rows) in place of Nq.
+    ``window`` = (left, right) sliding-window bounds (module notes)."""
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
     v = np.asarray(v, dtype=np.float64)
@@ -124,14 +147,14 @@ def forward(q, k, v, scale: float, causal: bool, rows=None):
             V = v[b, :, kv, :]
             for r0 in range(0, R, PANEL_ROWS):
                 rr = rows[r0:r0 + PANEL_ROWS]
-                S = _scores(q[b, rr, h, :], K, scale, rr, Nq, causal)
+                S = _scores(q[b, rr, h, :], K, scale, rr, Nq, causal, window)
                 P, l = _softmax_stats(S)
                 o[b, r0:r0 + len(rr), h, :] = P @ V
                 lse[b, h, r0:r0 + len(rr)] = l
     return o, lse
 
 
-def backward(q, k, v, do, scale: float, causal: bool):
+def backward(q, k, v, do, scale: float, causal: bool, window=None):
     """Analytic dQ, dK, dV of L = sum(dO * O) (fp64, oracle's own O)."""
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
@@ -153,7 +176,7 @@ def backward(q, k, v, do, scale: float, causal: bool):
                 rr = rows_all[r0:r0 + PANEL_ROWS]
                 Q = q[b, rr, h, :]
                 dO = do[b, rr, h, :]
-                S = _scores(Q, K, scale, rr, Nq, causal)
+                S = _scores(Q, K, scale, rr, Nq, causal, window)
                 P, _ = _softmax_stats(S)
                 O = P @ V
                 D = np.sum(dO * O, axis=1)

@@ -94,8 +94,9 @@ def check_causal_row0(fwd):
     np.testing.assert_allclose(lse[0, 0, 0], 0.6 * q[0, 0, 0] @ k[0, 0, 0], rtol=0, atol=1e-12)
 
 
-def brute_force(q, k, v, scale, causal):
-    """Scalar loops with math.exp and math.fsum (tiny inputs only)."""
+def brute_force(q, k, v, scale, causal, window=None):
+    """Scalar loops with math.exp and math.fsum (tiny inputs only). A row
+    with no visible key gets O = 0 and LSE = -inf."""
     B, Nq, Hq, d = q.shape
     _, Nk, Hkv, _ = k.shape
     g = Hq // Hkv
@@ -104,7 +105,10 @@ def brute_force(q, k, v, scale, causal):
     for b in range(B):
         for h in range(Hq):
             for i in range(Nq):
-                keys = [j for j in range(Nk) if (not causal) or j <= i + Nk - Nq]
+                keys = [j for j in range(Nk) if seen(i, j, Nq, Nk, causal, window)]
+                if not keys:
+                    lse[b, h, i] = -math.inf
+                    continue
                 logits = [scale * math.fsum(q[b, i, h, c] * k[b, j, h // g, c] for c in range(d)) for j in keys]
                 top = max(logits)
                 w = [math.exp(s - top) for s in logits]
@@ -113,6 +117,22 @@ def brute_force(q, k, v, scale, causal):
                 for c in range(d):
                     o[b, i, h, c] = math.fsum(w[t] * v[b, j, h // g, c] for t, j in enumerate(keys)) / tot
     return o, lse
+
+
+def seen(i, j, nq, nk, causal, window):
+    """Whether query i sees key j: causal keeps j <= i + nk - nq; a window
+    (left, right) keeps i + nk - nq - left <= j <= i + nk - nq + right,
+    a negative bound meaning no limit on that side."""
+    diag = i + nk - nq
+    if causal and j > diag:
+        return False
+    if window is not None:
+        left, right = window
+        if left >= 0 and j < diag - left:
+            return False
+        if right >= 0 and j > diag + right:
+            return False
+    return True
 
 
 def check_brute_force(fwd):
@@ -182,9 +202,45 @@ def check_blockwise_invariance(fwd):
             np.testing.assert_allclose(lse, lseb, rtol=0, atol=1e-12)
 
 
+def check_window_special_cases(fwd):
+    """Sliding windows reduce to known results: (no left limit, right 0) is
+    causal; no limits is the plain softmax; (0, 0) leaves each row the one
+    key on its diagonal, so O_i = V[i + Nk - Nq] and LSE_i is that key's
+    logit (rows whose diagonal key does not exist see nothing)."""
+    for nq, nk in [(9, 9), (6, 11), (11, 6)]:
+        q, k, v = tiny_problem(B=1, Hq=2, Hkv=1, Nq=nq, Nk=nk, d=4, s=1.5)
+        oc, lc = fwd(q, k, v, 0.7, True)
+        ow, lw = fwd(q, k, v, 0.7, False, window=(-1, 0))
+        np.testing.assert_allclose(ow, oc, rtol=0, atol=1e-13)
+        np.testing.assert_allclose(lw, lc, rtol=0, atol=1e-13)
+        of, lf = fwd(q, k, v, 0.7, False)
+        ow, lw = fwd(q, k, v, 0.7, False, window=(-1, -1))
+        np.testing.assert_array_equal(ow, of)
+        np.testing.assert_array_equal(lw, lf)
+        o0, l0 = fwd(q, k, v, 0.7, False, window=(0, 0))
+        for i in range(nq):
+            j = i + nk - nq
+            for h in range(2):
+                if 0 <= j < nk:
+                    np.testing.assert_allclose(o0[0, i, h], v[0, j, 0], rtol=0, atol=1e-13)
+                    np.testing.assert_allclose(l0[0, h, i], 0.7 * q[0, i, h] @ k[0, j, 0], rtol=0, atol=1e-13)
+                else:
+                    assert np.all(o0[0, i, h] == 0) and l0[0, h, i] == -np.inf
+
+
+def check_window_brute_force(fwd):
+    for window, causal, (nq, nk) in [((1, 0), False, (8, 8)), ((2, 3), False, (7, 12)), ((0, 2), False, (12, 7)),
+                                     ((3, -1), False, (10, 10)), ((2, 5), True, (9, 9))]:
+        q, k, v = tiny_problem(B=1, Hq=2, Hkv=2, Nq=nq, Nk=nk, d=3, s=1.5)
+        o, lse = fwd(q, k, v, 0.8, causal, window=window)
+        o_bf, lse_bf = brute_force(q, k, v, 0.8, causal, window)
+        np.testing.assert_allclose(o, o_bf, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lse, lse_bf, rtol=0, atol=1e-12)
+
+
 FORWARD_PINS = [check_worked_examples, check_constant_v, check_zero_q, check_one_hot, check_causal_row0,
                 check_brute_force, check_torch_sdpa, check_gqa_replication, check_key_shift_invariance,
-                check_blockwise_invariance]
+                check_blockwise_invariance, check_window_special_cases, check_window_brute_force]
 
 
 @pytest.mark.parametrize("pin", FORWARD_PINS + [check_rows_sum_to_one], ids=lambda f: f.__name__)
@@ -194,25 +250,26 @@ def test_forward_pin(pin):
 
 # --------------------------------------------------------------- backward --
 
-def loss(q, k, v, do, scale, causal):
-    o, _ = attn_ref.forward(q, k, v, scale, causal)
+def loss(q, k, v, do, scale, causal, window=None):
+    o, _ = attn_ref.forward(q, k, v, scale, causal, window=window)
     return float(np.sum(o * do))
 
 
 def check_finite_differences(bwd):
-    for causal, (nq, nk) in [(False, (5, 5)), (True, (6, 6)), (True, (4, 7))]:
+    for causal, (nq, nk), window in [(False, (5, 5), None), (True, (6, 6), None), (True, (4, 7), None),
+                                     (False, (6, 6), (1, 2)), (True, (7, 5), (2, 0))]:
         q, k, v = tiny_problem(B=1, Hq=2, Hkv=1, Nq=nq, Nk=nk, d=3, s=1.2)
         do = rand(*q.shape)
-        dq, dk, dv = bwd(q, k, v, do, 0.6, causal)
+        dq, dk, dv = bwd(q, k, v, do, 0.6, causal, window=window)
         eps = 1e-6
         for x, g in ((q, dq), (k, dk), (v, dv)):
             num = np.zeros_like(x)
             for idx in np.ndindex(x.shape):
                 old = x[idx]
                 x[idx] = old + eps
-                lp = loss(q, k, v, do, 0.6, causal)
+                lp = loss(q, k, v, do, 0.6, causal, window)
                 x[idx] = old - eps
-                lm = loss(q, k, v, do, 0.6, causal)
+                lm = loss(q, k, v, do, 0.6, causal, window)
                 x[idx] = old
                 num[idx] = (lp - lm) / (2 * eps)
             np.testing.assert_allclose(g, num, rtol=1e-6, atol=1e-8)
@@ -315,11 +372,18 @@ def _fails_some(pins, fn):
 
 
 MUTANTS = {
-    "scale_dropped": ("_scores", lambda orig: (lambda Q, K, scale, rows, nq, causal: orig(Q, K, 1.0, rows, nq, causal))),
+    "scale_dropped": ("_scores", lambda orig: (
+        lambda Q, K, scale, rows, nq, causal, window=None: orig(Q, K, 1.0, rows, nq, causal, window))),
     "top_left_causal": ("visible_mask", lambda orig: (
-        lambda rows, nq, nk, causal: orig(rows, nk, nk, causal))),
+        lambda rows, nq, nk, causal, window=None: orig(rows, nk, nk, causal, window))),
     "mask_off_by_one": ("visible_mask", lambda orig: (
-        lambda rows, nq, nk, causal: orig(np.asarray(rows) - 1, nq, nk, causal))),
+        lambda rows, nq, nk, causal, window=None: orig(np.asarray(rows) - 1, nq, nk, causal, window))),
+    "window_left_off_by_one": ("visible_mask", lambda orig: (
+        lambda rows, nq, nk, causal, window=None: orig(
+            rows, nq, nk, causal, None if window is None else (window[0] + 1 if window[0] >= 0 else -1, window[1])))),
+    "window_right_ignored": ("visible_mask", lambda orig: (
+        lambda rows, nq, nk, causal, window=None: orig(
+            rows, nq, nk, causal, None if window is None else (window[0], -1)))),
     "lse_log2": ("_softmax_stats", lambda orig: (
         lambda S: (lambda P, l: (P, l / math.log(2)))(*orig(S)))),
     "softmax_not_normalised": ("_softmax_stats", lambda orig: (
