@@ -53,6 +53,8 @@ def lib() -> ctypes.CDLL:
         vp, i, f, ull = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_ulonglong
         L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp]
         L.fa_fwd.restype = i
+        L.fa_fwd_window.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, vp]
+        L.fa_fwd_window.restype = i
         L.fa_bwd.argtypes = [vp] * 9 + [i, i, i, i, i, i, f, i, vp]
         L.fa_bwd.restype = i
         L.fa_bwd_noalloc.argtypes = [vp] * 9 + [i, i, i, i, i, i, f, i, vp]
@@ -93,6 +95,19 @@ def _stream(s):
 def fa_fwd(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, stream=None) -> int:
     return lib().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Nq, Nk, d, float(scale),
                         int(causal), _stream(stream))
+
+
+def fa_fwd_window(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, window_left, window_right, stream=None) -> int:
+    return lib().fa_fwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Nq, Nk, d, float(scale),
+                               int(window_left), int(window_right), _stream(stream))
+
+
+def _window_args(causal, window):
+    """(left, right) bounds for the *_window calls; causal caps right at 0."""
+    wl, wr = (-1, -1) if window is None else (int(window[0]), int(window[1]))
+    if causal:
+        wr = 0 if wr < 0 else min(wr, 0)
+    return wl, wr
 
 
 def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Nq, Nk, d, scale, causal, stream=None) -> int:
@@ -144,8 +159,9 @@ def _check_bshd(name, t, B, N, H, d):
         raise ValueError(f"{name} must be a contiguous CUDA bf16 tensor of shape {(B, N, H, d)}")
 
 
-def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None, stream=None):
-    """O, LSE for q [B,Nq,Hq,d], k/v [B,Nk,Hkv,d] (bf16, CUDA, contiguous)."""
+def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None, stream=None, window=None):
+    """O, LSE for q [B,Nq,Hq,d], k/v [B,Nk,Hkv,d] (bf16, CUDA, contiguous).
+    window: optional (left, right) sliding-window bounds (see fa.h)."""
     import torch
     B, Nq, Hq, d = q.shape
     _, Nk, Hkv, _ = k.shape
@@ -158,7 +174,10 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None,
         lse = torch.empty((B, Hq, Nq), device=q.device, dtype=torch.float32)
     else:
         o, lse = out
-    st = fa_fwd(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, stream)
+    if window is None:
+        st = fa_fwd(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, stream)
+    else:
+        st = fa_fwd_window(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, *_window_args(causal, window), stream)
     if st != 0:
         raise FAError(st, "fa_fwd")
     return o, lse

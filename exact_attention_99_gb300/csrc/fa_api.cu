@@ -81,6 +81,13 @@ __global__ void debug_exp2_kernel(const float* x, float* y, int n, int mode) {
 
 }  // namespace
 
+int normalize_window(int w, int Nq, int Nk) {
+  if (w < 0) return -1;
+  if (1LL * w >= 1LL * Nq + Nk) return -1;
+  return w;
+}
+
+
 // Stream-ordered pool for the backward workspace, one per device, that
 // keeps freed memory for the next call (release threshold = max) instead of
 // returning it to the driver at every synchronisation.
@@ -211,6 +218,19 @@ extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, floa
   st = check_device();
   if (st != FA_OK) return st;
   Problem p{q, k, v, B, Hq, Hkv, Nq, Nk, d, scale, causal};
+  return launch_fwd(p, o, lse, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+extern "C" int fa_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                             int Nq, int Nk, int d, float scale, int window_left, int window_right, void* stream) {
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return FA_ERR_INVALID_ARG;
+  int st = check_sizes(B, Hq, Hkv, Nq, Nk, d, scale, 0);
+  if (st != FA_OK) return st;
+  st = check_device();
+  if (st != FA_OK) return st;
+  Problem p{q, k, v, B, Hq, Hkv, Nq, Nk, d, scale, 0};
+  p.window_left = normalize_window(window_left, Nq, Nk);
+  p.window_right = normalize_window(window_right, Nq, Nk);
   return launch_fwd(p, o, lse, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 

@@ -89,6 +89,10 @@ struct Params {
   // on twice as many CTAs; the work items are the n_full whole units
   // followed by those halves, n_items in all.
   int n_items, n_full;
+  // Visible keys of query row i (masked kernels): i + off - wl <= j <=
+  // i + off + wr with off = Nk - Nq; a negative bound is no limit. Causal
+  // is wl = -1, wr = 0.
+  int wl, wr;
   unsigned long long wait_limit_ns;
   int inject;
   unsigned* status;
@@ -127,9 +131,12 @@ struct __align__(8) Ctl {
 
 struct Unit {
   int b, h, kvh, row0;
-  int n[2];   // key tiles each stage visits
-  int nb;     // max(n[0], n[1])
+  int kb0;    // first key tile of the unit
+  int a[2];   // stage s visits key tiles kb0 + a[s] .. kb0 + a[s] + n[s] - 1
+  int n[2];
+  int nb;     // key tiles the unit loads: max over stages of a[s] + n[s]
   bool rows[2];
+  __device__ __forceinline__ bool active(int s, int j) const { return j >= a[s] && j < a[s] + n[s]; }
 };
 
 template <bool CAUSAL>
@@ -160,25 +167,39 @@ __device__ __forceinline__ Unit decode_unit(const Params& p, int item) {
   x.row0 = mb * 256;
   const int off = p.Nk - p.Nq;
   const int nkb = (p.Nk + 127) >> 7;
+  int t0[2];
 #pragma unroll
   for (int s = 0; s < 2; ++s) {
     const int r0 = x.row0 + s * 128;
     x.rows[s] = r0 < p.Nq;
+    t0[s] = 0;
     if (!x.rows[s]) {
       x.n[s] = 0;
     } else if (!CAUSAL) {
       x.n[s] = nkb;
     } else {
+      // keys seen by any row of the stage: [lo, hi]
       const int rl = min(r0 + 127, p.Nq - 1);
-      const int kmax = min(rl + off, p.Nk - 1);
-      x.n[s] = kmax < 0 ? 0 : (kmax >> 7) + 1;
+      const int lo = p.wl >= 0 ? max(0, r0 + off - p.wl) : 0;
+      const int hi = p.wr >= 0 ? min(p.Nk - 1, rl + off + p.wr) : p.Nk - 1;
+      if (hi < lo) {
+        x.n[s] = 0;
+      } else {
+        t0[s] = lo >> 7;
+        x.n[s] = (hi >> 7) - t0[s] + 1;
+      }
     }
   }
   if (half >= 0) {  // one stage of a row-split unit; the other item has the other rows
     x.n[half ^ 1] = 0;
     x.rows[half ^ 1] = false;
   }
-  x.nb = max(x.n[0], x.n[1]);
+  // stage 1's rows follow stage 0's, so its key range starts and ends no
+  // earlier, and (both bounds being >= 0 or absent) leaves no gap after it
+  x.kb0 = x.n[0] > 0 ? t0[0] : t0[1];
+#pragma unroll
+  for (int s = 0; s < 2; ++s) x.a[s] = x.n[s] > 0 ? t0[s] - x.kb0 : 0;
+  x.nb = max(x.a[0] + x.n[0], x.a[1] + x.n[1]);
   return x;
 }
 
@@ -264,6 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (n == 0) continue;
       const int rg = un.row0 + s * 128 + row;  // global query row
       const int off = p.Nk - p.Nq;
+      const int r0 = un.row0 + s * 128, rl = min(r0 + 127, p.Nq - 1);  // the stage's rows
       float m_run = -INFINITY, l_run = 0.0f;
       for (int j = 0; j < n; ++j) {
         if (!mbar_wait_bounded(&ctl.s_full[s], ph_s, abort_flag, LIM)) { ok = false; break; }
@@ -274,14 +296,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 4; ++c) tmem_ld32(t_s + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&x[c * 32]));
         tmem_wait_ld();
-        const int kb = j * 128;
-        const bool need_mask = (kb + 127 >= p.Nk) || (CAUSAL && kb + 127 > un.row0 + s * 128 + off);
+        const int kb = (un.kb0 + un.a[s] + j) * 128;
+        // a tile needs masking when it reaches past the keys or crosses a
+        // window edge of some row of the stage
+        const bool need_mask = (kb + 127 >= p.Nk) ||
+                               (CAUSAL && ((p.wr >= 0 && kb + 127 > r0 + off + p.wr) || (p.wl >= 0 && kb < rl + off - p.wl)));
         if (need_mask) {
-          int lim = p.Nk - kb;
-          if (CAUSAL) lim = min(lim, rg + off + 1 - kb);
+          int lim = p.Nk - kb;  // columns [lo_c, lim) of this row are visible
+          int lo_c = 0;
+          if (CAUSAL && p.wr >= 0) lim = min(lim, rg + off + p.wr + 1 - kb);
+          if (CAUSAL && p.wl >= 0) lo_c = rg + off - p.wl - kb;
 #pragma unroll
           for (int c = 0; c < 128; ++c)
-            if (c >= lim) x[c] = f2u(-INFINITY);
+            if (c >= lim || c < lo_c) x[c] = f2u(-INFINITY);
         }
         float mA = -INFINITY, mB = -INFINITY, mC = -INFINITY, mD = -INFINITY;
 #pragma unroll
@@ -363,12 +390,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < un.nb && ok; ++j) {
 #pragma unroll
         for (int s = 0; s < 2; ++s) {
-          if (j >= un.n[s]) continue;
+          if (!un.active(s, j)) continue;
           if (!mbar_wait_bounded(&ctl.alpha_full[s], ph_a[s], abort_flag, LIM)) { ok = false; break; }
           ph_a[s] ^= 1;
           if (row == 0) trace_stamp(p.trace, blk0 + j, 10 + 2 * s);
           const float a = ctl.alpha[s][row];
-          if (j > 0 && __any_sync(0xffffffffu, a < 1.0f)) {
+          if (j > un.a[s] && __any_sync(0xffffffffu, a < 1.0f)) {
             tc_fence_after();
             const uint32_t t_o = t_lane + C::kOCol0 + uint32_t(s * D);
             const uint64_t a2 = pack2(a, a);
@@ -500,8 +527,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const CUtensorMap* map = t == 0 ? &tmK : &tmV;
 #pragma unroll
             for (int c = 0; c < C::kChunks; ++c)
-              tma_load_4d(sKV + slot * C::kTileBytes + c * 16384, map, &ctl.kv_full[slot], c * 64, un.kvh, j * 128,
-                          un.b);
+              tma_load_4d(sKV + slot * C::kTileBytes + c * 16384, map, &ctl.kv_full[slot], c * 64, un.kvh,
+                          (un.kb0 + j) * 128, un.b);
           }
         }
         blk += un.nb;
@@ -563,7 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok || !wait_kv(kslot)) { ok = false; break; }
         tc_fence_after();
         for (int s = 0; s < 2; ++s) {
-          if (un.n[s] == 0) continue;
+          if (!un.active(s, 0)) continue;
           issue_S(s, kslot);
           mma_commit(&ctl.s_full[s]);
         }
@@ -573,20 +600,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!wait_kv(vslot)) { ok = false; break; }
           const bool nxt = j + 1 < un.nb;
           if (nxt && !wait_kv(kslot)) { ok = false; break; }
+          const int last_v = un.active(1, j) ? 1 : 0;  // the last stage that reads V_j
           for (int s = 0; s < 2; ++s) {
-            if (j >= un.n[s]) continue;
-            if (!mbar_wait_bounded(&ctl.p_full[s], ph_p[s], abort_flag, LIM)) { ok = false; break; }
-            ph_p[s] ^= 1;
-            if (!mbar_wait_bounded(&ctl.o_ready[s], ph_o[s], abort_flag, LIM)) { ok = false; break; }
-            ph_o[s] ^= 1;
-            tc_fence_after();
-            trace_stamp(p.trace, blk + j, s);
-            issue_PV(s, vslot, j > 0);
-            if (j == un.n[s] - 1) mma_commit(&ctl.o_full[s]);
-            // V_j is free once the last PV reading it completes: release it
-            // before the next S is issued so the refill starts earlier
-            if (s == 1 || j >= un.n[1]) mma_commit(&ctl.kv_empty[vslot]);
-            if (j + 1 < un.n[s]) {
+            if (un.active(s, j)) {
+              if (!mbar_wait_bounded(&ctl.p_full[s], ph_p[s], abort_flag, LIM)) { ok = false; break; }
+              ph_p[s] ^= 1;
+              if (!mbar_wait_bounded(&ctl.o_ready[s], ph_o[s], abort_flag, LIM)) { ok = false; break; }
+              ph_o[s] ^= 1;
+              tc_fence_after();
+              trace_stamp(p.trace, blk + j, s);
+              issue_PV(s, vslot, j > un.a[s]);
+              if (j == un.a[s] + un.n[s] - 1) mma_commit(&ctl.o_full[s]);
+              // V_j is free once the last PV reading it completes: release it
+              // before the next S is issued so the refill starts earlier
+              if (s == last_v) mma_commit(&ctl.kv_empty[vslot]);
+            }
+            if (nxt && un.active(s, j + 1)) {  // S of the next tile (a stage's first S when it starts there)
+              tc_fence_after();
               trace_stamp(p.trace, blk + j, 2 + s);
               issue_S(s, kslot);
               mma_commit(&ctl.s_full[s]);
@@ -635,6 +665,8 @@ cudaError_t launch_t(const Problem& pb, void* o, float* lse, cudaStream_t stream
   p.Nk = pb.Nk;
   p.group = pb.Hq / pb.Hkv;
   p.scale_log2 = pb.scale * 1.4426950408889634f;
+  p.wl = normalize_window(pb.window_left, pb.Nq, pb.Nk);
+  p.wr = pb.causal ? 0 : normalize_window(pb.window_right, pb.Nq, pb.Nk);
   p.n_mblocks = (pb.Nq + 255) / 256;
   p.n_units = p.n_mblocks * pb.B * pb.Hq;
   // Row-split tail: when the T = n_units mod G units of the last round fit
@@ -668,8 +700,9 @@ cudaError_t launch_t(const Problem& pb, void* o, float* lse, cudaStream_t stream
 }  // namespace fwd
 
 cudaError_t launch_fwd(const Problem& p, void* o, float* lse, cudaStream_t stream) {
-  if (p.d == 128) return p.causal ? fwd::launch_t<128, true>(p, o, lse, stream) : fwd::launch_t<128, false>(p, o, lse, stream);
-  return p.causal ? fwd::launch_t<64, true>(p, o, lse, stream) : fwd::launch_t<64, false>(p, o, lse, stream);
+  const bool m = p.masked();
+  if (p.d == 128) return m ? fwd::launch_t<128, true>(p, o, lse, stream) : fwd::launch_t<128, false>(p, o, lse, stream);
+  return m ? fwd::launch_t<64, true>(p, o, lse, stream) : fwd::launch_t<64, false>(p, o, lse, stream);
 }
 
 }  // namespace fa

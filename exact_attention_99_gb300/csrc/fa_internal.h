@@ -16,6 +16,10 @@ struct Problem {
   int B, Hq, Hkv, Nq, Nk, d;
   float scale;
   int causal;
+  // sliding window: key j visible to query i iff i + off - window_left <= j
+  // <= i + off + window_right (off = Nk - Nq); -1 = no limit on that side
+  int window_left = -1, window_right = -1;
+  bool masked() const { return causal || window_left >= 0 || window_right >= 0; }
 };
 
 struct DebugCfg {
@@ -45,6 +49,10 @@ bool make_bshd_map(CUtensorMap* m, const void* base, int B, int N, int H, int d,
 // dims 1..rank-1, zero fill out of range.
 bool encode_tiled(CUtensorMap* m, CUtensorMapDataType dtype, int rank, const void* base, const uint64_t* dims,
                   const uint64_t* strides, const uint32_t* box, CUtensorMapSwizzle swizzle);
+
+// Window bounds as the kernels take them: negative -> -1 (no limit); a
+// bound that reaches past every key (>= Nq + Nk) is no limit either.
+int normalize_window(int w, int Nq, int Nk);
 
 // Launchers. Return a cudaError_t (cudaSuccess on success).
 cudaError_t launch_fwd(const Problem& p, void* o, float* lse, cudaStream_t stream);

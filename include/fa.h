@@ -66,6 +66,20 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
            int d, float scale, int causal, void* stream);
 
 /*
+ * fa_fwd_window — the forward pass with a sliding-window (local) mask.
+ *   Key j is visible to query row i iff
+ *       i + off - window_left <= j <= i + off + window_right,  off = Nk - Nq
+ *   (the bottom-right alignment of the causal mask); a negative bound, or one
+ *   of at least Nq + Nk, means no limit on that side. window_right = 0 with
+ *   window_left < 0 is the causal mask; both negative is fa_fwd non-causal.
+ *   Rows that see no key get O = 0 and LSE = -inf. Key tiles outside every
+ *   row's window are skipped, so the work scales with the window.
+ *   Arguments, layouts, ownership and errors otherwise as fa_fwd.
+ */
+int fa_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Nq,
+                  int Nk, int d, float scale, int window_left, int window_right, void* stream);
+
+/*
  * fa_bwd — backward pass for L = sum(dout * o).
  *   in : q, k, v, o (bf16), lse (fp32, as written by fa_fwd for the same
  *        inputs), dout [B,Nq,Hq,d] (bf16)
