@@ -57,6 +57,8 @@ def lib() -> ctypes.CDLL:
         L.fa_fwd_window.restype = i
         L.fa_bwd.argtypes = [vp] * 9 + [i, i, i, i, i, i, f, i, vp]
         L.fa_bwd.restype = i
+        L.fa_bwd_window.argtypes = [vp] * 9 + [i, i, i, i, i, i, f, i, i, vp]
+        L.fa_bwd_window.restype = i
         L.fa_bwd_noalloc.argtypes = [vp] * 9 + [i, i, i, i, i, i, f, i, vp]
         L.fa_bwd_noalloc.restype = i
         L.fa_get_status.argtypes = [vp]
@@ -113,6 +115,13 @@ def _window_args(causal, window):
 def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Nq, Nk, d, scale, causal, stream=None) -> int:
     return lib().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
                         B, Hq, Hkv, Nq, Nk, d, float(scale), int(causal), _stream(stream))
+
+
+def fa_bwd_window(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Nq, Nk, d, scale, window_left, window_right,
+                  stream=None) -> int:
+    return lib().fa_bwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
+                               _ptr(dv), B, Hq, Hkv, Nq, Nk, d, float(scale), int(window_left), int(window_right),
+                               _stream(stream))
 
 
 def fa_bwd_noalloc(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Nq, Nk, d, scale, causal, stream=None) -> int:
@@ -183,8 +192,10 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None,
     return o, lse
 
 
-def backward(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None, out=None, stream=None):
-    """dQ, dK, dV for the forward that produced o and lse."""
+def backward(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None, out=None, stream=None,
+             window=None):
+    """dQ, dK, dV for the forward that produced o and lse (same causal flag
+    and window)."""
     import torch
     B, Nq, Hq, d = q.shape
     _, Nk, Hkv, _ = k.shape
@@ -196,7 +207,11 @@ def backward(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = 
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     else:
         dq, dk, dv = out
-    st = fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Nq, Nk, d, scale, causal, stream)
+    if window is None:
+        st = fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Nq, Nk, d, scale, causal, stream)
+    else:
+        st = fa_bwd_window(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Nq, Nk, d, scale,
+                           *_window_args(causal, window), stream)
     if st != 0:
         raise FAError(st, "fa_bwd")
     return dq, dk, dv

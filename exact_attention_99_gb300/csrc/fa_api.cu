@@ -234,18 +234,12 @@ extern "C" int fa_fwd_window(const void* q, const void* k, const void* v, void* 
   return launch_fwd(p, o, lse, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
-extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
-                      void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Nq, int Nk, int d, float scale,
-                      int causal, void* stream) {
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(dout) ||
-      !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
-    return FA_ERR_INVALID_ARG;
-  int st = check_sizes(B, Hq, Hkv, Nq, Nk, d, scale, causal);
-  if (st != FA_OK) return st;
-  st = check_device();
-  if (st != FA_OK) return st;
+namespace {
+// fa_bwd / fa_bwd_window after their checks: workspace from the pool,
+// launch, free, all on the caller's stream
+int bwd_pooled(const Problem& p, const void* o, const float* lse, const void* dout, void* dq, void* dk, void* dv,
+               void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  Problem p{q, k, v, B, Hq, Hkv, Nq, Nk, d, scale, causal};
   cudaMemPool_t pool = workspace_pool();
   void* ws = nullptr;
   if (pool == nullptr || cudaMallocFromPoolAsync(&ws, bwd_workspace_bytes(p), pool, s) != cudaSuccess) {
@@ -256,6 +250,37 @@ extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o
   const cudaError_t f = cudaFreeAsync(ws, s);
   if (e != cudaSuccess || f != cudaSuccess) return FA_ERR_LAUNCH;
   return FA_OK;
+}
+}  // namespace
+
+extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                      void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Nq, int Nk, int d, float scale,
+                      int causal, void* stream) {
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(dout) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return FA_ERR_INVALID_ARG;
+  int st = check_sizes(B, Hq, Hkv, Nq, Nk, d, scale, causal);
+  if (st != FA_OK) return st;
+  st = check_device();
+  if (st != FA_OK) return st;
+  const Problem p{q, k, v, B, Hq, Hkv, Nq, Nk, d, scale, causal};
+  return bwd_pooled(p, o, lse, dout, dq, dk, dv, stream);
+}
+
+extern "C" int fa_bwd_window(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                             const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Nq, int Nk,
+                             int d, float scale, int window_left, int window_right, void* stream) {
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(dout) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return FA_ERR_INVALID_ARG;
+  int st = check_sizes(B, Hq, Hkv, Nq, Nk, d, scale, 0);
+  if (st != FA_OK) return st;
+  st = check_device();
+  if (st != FA_OK) return st;
+  Problem p{q, k, v, B, Hq, Hkv, Nq, Nk, d, scale, 0};
+  p.window_left = normalize_window(window_left, Nq, Nk);
+  p.window_right = normalize_window(window_right, Nq, Nk);
+  return bwd_pooled(p, o, lse, dout, dq, dk, dv, stream);
 }
 
 extern "C" int fa_get_status(void* stream) {

@@ -100,6 +100,10 @@ struct Params {
   const float* lse2;    // [B*Hq, Nq_pad]: LSE*log2(e), +inf for padded / empty rows
   const float* delta;   // [B*Hq, Nq_pad]
   int B, Hq, Hkv, Nq, Nk, Nq_pad, group, n_ktiles, n_qtiles;
+  // masked kernels: key j visible to query row i iff i + off - wl <= j <=
+  // i + off + wr (off = Nk - Nq); a negative bound is no limit; causal is
+  // wl = -1, wr = 0
+  int wl, wr;
   float scale, scale_log2;
   unsigned long long wait_limit_ns;
   unsigned* status;
@@ -116,7 +120,7 @@ template <bool CAUSAL>
 __device__ __forceinline__ Work decode(const Params& p) {
   Work w;
   int r;
-  if (CAUSAL) {
+  if (CAUSAL && p.wl < 0) {
     // key tiles j and n-1-j share a CTA: the pair always has n+1 query-tile
     // steps (for Nq = Nk), so all CTAs carry the same work; heads in a row
     const int n_pairs = (p.n_ktiles + 1) / 2;
@@ -128,7 +132,8 @@ __device__ __forceinline__ Work decode(const Params& p) {
     w.n_items = j2 > pr ? 2 : 1;
   } else {
     // all key tiles of one head in a row, so concurrent CTAs share Q, dO and
-    // the dQ accumulator in L2
+    // the dQ accumulator in L2 (also for windows with a left bound, where
+    // every key tile has about the same number of query tiles)
     r = blockIdx.x / p.n_ktiles;
     w.it[0].j = blockIdx.x - r * p.n_ktiles;
     w.it[1].j = 0;
@@ -138,13 +143,17 @@ __device__ __forceinline__ Work decode(const Params& p) {
   w.kvh = r - w.b * p.Hkv;
 #pragma unroll
   for (int k = 0; k < 2; ++k) {
-    int i0 = 0;
-    if (CAUSAL) {
-      const int first_row = w.it[k].j * 128 - (p.Nk - p.Nq);  // first query row that sees the tile's first key
-      i0 = first_row <= 0 ? 0 : first_row / 128;
+    // query rows that see some key of the tile: [lo, hi]
+    const int off = p.Nk - p.Nq;
+    const int k0 = w.it[k].j * 128, k1 = min(k0 + 127, p.Nk - 1);
+    int lo = 0, hi = p.Nq - 1;
+    if (CAUSAL && p.wr >= 0) lo = max(lo, k0 - off - p.wr);
+    if (CAUSAL && p.wl >= 0) hi = min(hi, k1 - off + p.wl);
+    int i0 = 0, nq = 0;
+    if (lo <= hi && k < w.n_items) {
+      i0 = lo >> 7;
+      nq = (hi >> 7) - i0 + 1;
     }
-    int nq = p.n_qtiles - i0;
-    if (nq < 0 || k >= w.n_items) nq = 0;
     w.it[k].i0 = i0;
     w.it[k].nq = nq;
     w.it[k].steps = nq * p.group;
@@ -266,9 +275,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 4; ++c)
           tmem_ld32(t_lane + C::kColS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&x[c * 32]));
         tmem_wait_ld();
-        // causal: query row q sees this key iff q >= key - off
-        const bool need_mask = CAUSAL && (it * 128 < I.j * 128 + 127 - off);
-        const int qlim = key - off - it * 128;  // columns c < qlim are hidden
+        // query row q (column c = q - it*128) sees this key iff
+        // key - off - wr <= q <= key - off + wl: mask tiles that cross an edge
+        const bool need_mask = CAUSAL && ((p.wr >= 0 && it * 128 < I.j * 128 + 127 - off - p.wr) ||
+                                          (p.wl >= 0 && it * 128 + 127 > I.j * 128 - off + p.wl));
+        const int qlim = p.wr >= 0 ? key - off - p.wr - it * 128 : -(1 << 30);  // columns c < qlim are hidden
+        const int qmax = p.wl >= 0 ? key - off + p.wl - it * 128 : (1 << 30);   // and columns c > qmax
         float pv[128];
 #pragma unroll
         for (int c = 0; c < 128; c += 4) {
@@ -287,9 +299,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // pass so the common case carries no per-element selects
         if (need_mask || !kvalid) {
           const int lim = kvalid ? qlim : 128;
+          const int top = kvalid ? qmax : -1;
 #pragma unroll
           for (int c = 0; c < 128; ++c)
-            if (c < lim) pv[c] = 0.0f;
+            if (c < lim || c > top) pv[c] = 0.0f;
         }
         {
           uint32_t pk[64];
@@ -756,6 +769,8 @@ cudaError_t launch_t(const Problem& pb, const void* o, const float* lse, const v
   p.n_qtiles = Nq_pad / 128;
   p.scale = pb.scale;
   p.scale_log2 = pb.scale * 1.4426950408889634f;
+  p.wl = normalize_window(pb.window_left, pb.Nq, pb.Nk);
+  p.wr = pb.causal ? 0 : normalize_window(pb.window_right, pb.Nq, pb.Nk);
   const DebugCfg dc = debug_cfg();
   p.wait_limit_ns = dc.wait_limit_ns;
   p.trace = dc.trace;
@@ -766,7 +781,8 @@ cudaError_t launch_t(const Problem& pb, const void* o, const float* lse, const v
   auto kern = bwd_main_kernel<D, CAUSAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const unsigned grid = unsigned(pb.B) * pb.Hkv * (CAUSAL ? (p.n_ktiles + 1) / 2 : p.n_ktiles);
+  const bool paired = CAUSAL && p.wl < 0;  // decode: pairs of key tiles only for the plain causal mask
+  const unsigned grid = unsigned(pb.B) * pb.Hkv * (paired ? (p.n_ktiles + 1) / 2 : p.n_ktiles);
   if (dc.ev_begin) cudaEventRecord(dc.ev_begin, stream);
   kern<<<grid, kThreads, smem, stream>>>(mq, mk, mv, mdo, macc, p);
   e = cudaGetLastError();
@@ -790,9 +806,9 @@ size_t bwd_workspace_bytes(const Problem& p) {
 cudaError_t launch_bwd(const Problem& p, const void* o, const float* lse, const void* dout, void* dq, void* dk,
                        void* dv, float* ws, cudaStream_t stream) {
   if (p.d == 128)
-    return p.causal ? bwd::launch_t<128, true>(p, o, lse, dout, dq, dk, dv, ws, stream)
+    return p.masked() ? bwd::launch_t<128, true>(p, o, lse, dout, dq, dk, dv, ws, stream)
                     : bwd::launch_t<128, false>(p, o, lse, dout, dq, dk, dv, ws, stream);
-  return p.causal ? bwd::launch_t<64, true>(p, o, lse, dout, dq, dk, dv, ws, stream)
+  return p.masked() ? bwd::launch_t<64, true>(p, o, lse, dout, dq, dk, dv, ws, stream)
                   : bwd::launch_t<64, false>(p, o, lse, dout, dq, dk, dv, ws, stream);
 }
 

@@ -96,6 +96,16 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
            void* stream);
 
 /*
+ * fa_bwd_window — the backward pass of fa_fwd_window: the same window
+ *   bounds (and the o, lse that fa_fwd_window wrote); key tiles and query
+ *   tiles outside every window are skipped. Arguments, layouts, workspace
+ *   and errors otherwise as fa_bwd.
+ */
+int fa_bwd_window(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                  void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Nq, int Nk, int d, float scale,
+                  int window_left, int window_right, void* stream);
+
+/*
  * fa_bwd_noalloc — the same backward pass as fa_bwd, for callers that may
  * not allocate device memory during the call: serving loops that fix their
  * memory plan at start-up, and code that runs where the CUDA allocator must

@@ -151,3 +151,52 @@ def test_ragged_lengths_at_scale(fa, causal):
     assert_close("dq", to64(dq), rdq)
     assert_close("dk", to64(dk), rdk)
     assert_close("dv", to64(dv), rdv)
+
+
+BWD_WINDOWS = [
+    # B, Hq, Hkv, Nq, Nk, d, (left, right)
+    (1, 2, 2, 300, 300, 128, (64, 0)),
+    (1, 2, 1, 700, 700, 64, (200, 0)),
+    (1, 2, 2, 513, 513, 128, (128, 128)),
+    (1, 2, 2, 400, 900, 128, (300, 50)),    # Nq < Nk
+    (1, 2, 2, 900, 400, 128, (100, 0)),     # Nq > Nk: rows with no visible key
+    (1, 2, 2, 600, 600, 64, (-1, 300)),     # right bound only
+    (1, 3, 3, 1000, 1000, 128, (500, -1)),  # left bound only
+    (2, 4, 2, 1024, 1024, 128, (0, 0)),     # one key per row (GQA)
+]
+
+
+@pytest.mark.parametrize("shape", BWD_WINDOWS, ids=lambda s: "x".join(map(str, s[:6])) + f"-w{s[6][0]}_{s[6][1]}")
+def test_window(fa, shape):
+    B, Hq, Hkv, Nq, Nk, d, window = shape
+    x = workloads.make_inputs(B, Hq, Hkv, Nq, Nk, d, seed=sum(shape[:6]) + 3 * window[0] + window[1], with_dout=True)
+    scale = 1.0 / math.sqrt(d)
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
+    o, lse = fa.forward(q, k, v, scale=scale, window=window)
+    dq, dk, dv = fa.backward(q, k, v, o, lse, do, scale=scale, window=window)
+    torch.cuda.synchronize()
+    assert fa.fa_get_status() == 0
+    rdq, rdk, rdv = attn_ref.backward(*(x[n].double().numpy() for n in ("q", "k", "v", "do")), scale, False,
+                                      window=window)
+    assert_close("dq", to64(dq), rdq)
+    assert_close("dk", to64(dk), rdk)
+    assert_close("dv", to64(dv), rdv)
+
+
+def test_window_full_size_sampled_heads(fa):
+    """A causal local window of 1024 keys at N = 8192 (B=1, H=8): every
+    gradient of two heads against the oracle."""
+    B, H, N, d, window = 1, 8, 8192, 128, (1023, 0)
+    x = workloads.make_inputs(B, H, H, N, N, d, seed=43, with_dout=True)
+    scale = d ** -0.5
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
+    o, lse = fa.forward(q, k, v, scale=scale, window=window)
+    dq, dk, dv = fa.backward(q, k, v, o, lse, do, scale=scale, window=window)
+    torch.cuda.synchronize()
+    assert fa.fa_get_status() == 0
+    for h in (0, 5):
+        sl = lambda t: t[:, :, h:h + 1].double().numpy()
+        rdq, rdk, rdv = attn_ref.backward(sl(x["q"]), sl(x["k"]), sl(x["v"]), sl(x["do"]), scale, False, window=window)
+        assert_close(f"dq[h{h}]", to64(dq[:, :, h:h + 1]), rdq)
+        assert_close(f"dk[h{h}]", to64(dk[:, :, h:h + 1]), rdk)
+        assert_close(f"dv[h{h}]", to64(dv[:, :, h:h + 1]), rdv)
