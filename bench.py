@@ -279,6 +279,40 @@ def per_config(fa, flush, peak):
     return out
 
 
+WINDOW_CASE = dict(name="fwd_bwd_window1024_b2_h16_n8192_d128", B=2, H=16, N=8192, d=128, window=(1023, 0), seed=1042)
+
+
+def window_pairs(nq: int, nk: int, wl: int, wr: int) -> int:
+    """Visible (query, key) pairs of one head under a sliding window
+    (bounds as fa_fwd_window; negative = no limit)."""
+    import numpy as np
+    i = np.arange(nq, dtype=np.int64)
+    off = nk - nq
+    lo = np.maximum(0, i + off - wl) if wl >= 0 else np.zeros_like(i)
+    hi = np.minimum(nk - 1, i + off + wr) if wr >= 0 else np.full_like(i, nk - 1)
+    return int(np.maximum(0, hi - lo + 1).sum())
+
+
+def window_config(fa, flush, peak):
+    """Forward and backward TFLOP/s of a causal local window (1024 keys) at
+    B=2, H=16, N=8192, d=128, counting only the visible pairs: 4*d flops per
+    pair forward, 2.5x that backward."""
+    import torch
+    c = WINDOW_CASE
+    x = workloads.make_inputs(c["B"], c["H"], c["H"], c["N"], c["N"], c["d"], c["seed"], with_dout=True)
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
+    o, dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    lse = torch.empty((c["B"], c["H"], c["N"]), device="cuda", dtype=torch.float32)
+    a = (c["B"], c["H"], c["H"], c["N"], c["N"], c["d"], c["d"] ** -0.5, *c["window"])
+    fwd_fl = 4.0 * c["d"] * c["B"] * c["H"] * window_pairs(c["N"], c["N"], *c["window"])
+    fms = time_one(lambda: fa.fa_fwd_window(q, k, v, o, lse, *a), flush)
+    bms = time_one(lambda: fa.fa_bwd_window(q, k, v, o, lse, do, dq, dk, dv, *a), flush)
+    assert fa.fa_get_status() == 0
+    return {"window": list(c["window"]), "fwd_ms": round(fms, 4), "fwd_tflops": round(fwd_fl / fms / 1e9, 4),
+            "fwd_frac_of_peak": round(fwd_fl / fms / 1e9 / peak, 4), "bwd_ms": round(bms, 4),
+            "bwd_tflops": round(2.5 * fwd_fl / bms / 1e9, 4), "bwd_frac_of_peak": round(2.5 * fwd_fl / bms / 1e9 / peak, 4)}
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -394,6 +428,7 @@ def run_ours(args):
                 "flops_per_launch": kflops}
 
     configs = per_config(fa, flush, peak)
+    configs[WINDOW_CASE["name"]] = window_config(fa, flush, peak)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(total_ms / K, 4), "higher_is_better": True, "scaling": "weak",

@@ -116,11 +116,18 @@ struct Params {
 //   drain    10 dQ^T ready, 11 dQ^T columns released, 12 reductions issued
 //   producer 13 Q slot free, 14 dO slot free
 
-template <bool CAUSAL>
+// Window bounds as a kernel sees them: the plain causal kernels (WIN false)
+// fix them at compile time (no left bound, right bound 0).
+template <bool WIN>
+__device__ __forceinline__ int win_l(const Params& p) { return WIN ? p.wl : -1; }
+template <bool WIN>
+__device__ __forceinline__ int win_r(const Params& p) { return WIN ? p.wr : 0; }
+
+template <bool CAUSAL, bool WIN>
 __device__ __forceinline__ Work decode(const Params& p) {
   Work w;
   int r;
-  if (CAUSAL && p.wl < 0) {
+  if (CAUSAL && win_l<WIN>(p) < 0) {
     // key tiles j and n-1-j share a CTA: the pair always has n+1 query-tile
     // steps (for Nq = Nk), so all CTAs carry the same work; heads in a row
     const int n_pairs = (p.n_ktiles + 1) / 2;
@@ -147,8 +154,8 @@ __device__ __forceinline__ Work decode(const Params& p) {
     const int off = p.Nk - p.Nq;
     const int k0 = w.it[k].j * 128, k1 = min(k0 + 127, p.Nk - 1);
     int lo = 0, hi = p.Nq - 1;
-    if (CAUSAL && p.wr >= 0) lo = max(lo, k0 - off - p.wr);
-    if (CAUSAL && p.wl >= 0) hi = min(hi, k1 - off + p.wl);
+    if (CAUSAL && win_r<WIN>(p) >= 0) lo = max(lo, k0 - off - win_r<WIN>(p));
+    if (CAUSAL && win_l<WIN>(p) >= 0) hi = min(hi, k1 - off + win_l<WIN>(p));
     int i0 = 0, nq = 0;
     if (lo <= hi && k < w.n_items) {
       i0 = lo >> 7;
@@ -185,7 +192,7 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
                : "memory");
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool WIN>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -206,7 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (threadIdx.x == 0) {
     ctl.abort = 0;
-    ctl.work = decode<CAUSAL>(p);
+    ctl.work = decode<CAUSAL, WIN>(p);
     mbar_init(&ctl.kv_full, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ctl.q_full[i], 1);
@@ -277,10 +284,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_ld();
         // query row q (column c = q - it*128) sees this key iff
         // key - off - wr <= q <= key - off + wl: mask tiles that cross an edge
-        const bool need_mask = CAUSAL && ((p.wr >= 0 && it * 128 < I.j * 128 + 127 - off - p.wr) ||
-                                          (p.wl >= 0 && it * 128 + 127 > I.j * 128 - off + p.wl));
-        const int qlim = p.wr >= 0 ? key - off - p.wr - it * 128 : -(1 << 30);  // columns c < qlim are hidden
-        const int qmax = p.wl >= 0 ? key - off + p.wl - it * 128 : (1 << 30);   // and columns c > qmax
+        const int wl = win_l<WIN>(p), wr = win_r<WIN>(p);
+        const bool need_mask = CAUSAL && ((wr >= 0 && it * 128 < I.j * 128 + 127 - off - wr) ||
+                                          (wl >= 0 && it * 128 + 127 > I.j * 128 - off + wl));
+        const int qlim = wr >= 0 ? key - off - wr - it * 128 : -(1 << 30);  // columns c < qlim are hidden
+        const int qmax = wl >= 0 ? key - off + wl - it * 128 : (1 << 30);   // and columns c > qmax
         float pv[128];
 #pragma unroll
         for (int c = 0; c < 128; c += 4) {
@@ -299,10 +307,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         // pass so the common case carries no per-element selects
         if (need_mask || !kvalid) {
           const int lim = kvalid ? qlim : 128;
-          const int top = kvalid ? qmax : -1;
+          if (WIN) {
+            const int top = kvalid ? qmax : -1;
 #pragma unroll
-          for (int c = 0; c < 128; ++c)
-            if (c < lim || c > top) pv[c] = 0.0f;
+            for (int c = 0; c < 128; ++c)
+              if (c < lim || c > top) pv[c] = 0.0f;
+          } else {
+#pragma unroll
+            for (int c = 0; c < 128; ++c)
+              if (c < lim) pv[c] = 0.0f;
+          }
         }
         {
           uint32_t pk[64];
@@ -719,7 +733,7 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(const float* dq_acc, __nv
   }
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool WIN>
 cudaError_t launch_t(const Problem& pb, const void* o, const float* lse, const void* dout, void* dq, void* dk, void* dv,
                      float* ws, cudaStream_t stream) {
   const int Nq_pad = (pb.Nq + 127) / 128 * 128;
@@ -778,10 +792,10 @@ cudaError_t launch_t(const Problem& pb, const void* o, const float* lse, const v
   if (!p.status) return cudaErrorMemoryAllocation;
   using C = Cfg<D>;
   constexpr int smem = C::kOffCtl + int(sizeof(Ctl));
-  auto kern = bwd_main_kernel<D, CAUSAL>;
+  auto kern = bwd_main_kernel<D, CAUSAL, WIN>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const bool paired = CAUSAL && p.wl < 0;  // decode: pairs of key tiles only for the plain causal mask
+  const bool paired = CAUSAL && (WIN ? p.wl : -1) < 0;  // decode: pairs of key tiles only without a left bound
   const unsigned grid = unsigned(pb.B) * pb.Hkv * (paired ? (p.n_ktiles + 1) / 2 : p.n_ktiles);
   if (dc.ev_begin) cudaEventRecord(dc.ev_begin, stream);
   kern<<<grid, kThreads, smem, stream>>>(mq, mk, mv, mdo, macc, p);
@@ -806,10 +820,12 @@ size_t bwd_workspace_bytes(const Problem& p) {
 cudaError_t launch_bwd(const Problem& p, const void* o, const float* lse, const void* dout, void* dq, void* dk,
                        void* dv, float* ws, cudaStream_t stream) {
   if (p.d == 128)
-    return p.masked() ? bwd::launch_t<128, true>(p, o, lse, dout, dq, dk, dv, ws, stream)
-                    : bwd::launch_t<128, false>(p, o, lse, dout, dq, dk, dv, ws, stream);
-  return p.masked() ? bwd::launch_t<64, true>(p, o, lse, dout, dq, dk, dv, ws, stream)
-                  : bwd::launch_t<64, false>(p, o, lse, dout, dq, dk, dv, ws, stream);
+    return !p.masked()        ? bwd::launch_t<128, false, false>(p, o, lse, dout, dq, dk, dv, ws, stream)
+           : p.plain_causal() ? bwd::launch_t<128, true, false>(p, o, lse, dout, dq, dk, dv, ws, stream)
+                              : bwd::launch_t<128, true, true>(p, o, lse, dout, dq, dk, dv, ws, stream);
+  return !p.masked()        ? bwd::launch_t<64, false, false>(p, o, lse, dout, dq, dk, dv, ws, stream)
+         : p.plain_causal() ? bwd::launch_t<64, true, false>(p, o, lse, dout, dq, dk, dv, ws, stream)
+                            : bwd::launch_t<64, true, true>(p, o, lse, dout, dq, dk, dv, ws, stream);
 }
 
 }  // namespace fa

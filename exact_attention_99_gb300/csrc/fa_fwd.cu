@@ -139,7 +139,14 @@ struct Unit {
   __device__ __forceinline__ bool active(int s, int j) const { return j >= a[s] && j < a[s] + n[s]; }
 };
 
-template <bool CAUSAL>
+// Window bounds as a kernel sees them: the plain causal kernels (WIN false)
+// fix them at compile time (no left bound, right bound 0).
+template <bool WIN>
+__device__ __forceinline__ int win_l(const Params& p) { return WIN ? p.wl : -1; }
+template <bool WIN>
+__device__ __forceinline__ int win_r(const Params& p) { return WIN ? p.wr : 0; }
+
+template <bool CAUSAL, bool WIN>
 __device__ __forceinline__ Unit decode_unit(const Params& p, int item) {
   Unit x;
   int u = item, half = -1;
@@ -180,8 +187,9 @@ __device__ __forceinline__ Unit decode_unit(const Params& p, int item) {
     } else {
       // keys seen by any row of the stage: [lo, hi]
       const int rl = min(r0 + 127, p.Nq - 1);
-      const int lo = p.wl >= 0 ? max(0, r0 + off - p.wl) : 0;
-      const int hi = p.wr >= 0 ? min(p.Nk - 1, rl + off + p.wr) : p.Nk - 1;
+      const int wl = win_l<WIN>(p), wr = win_r<WIN>(p);
+      const int lo = wl >= 0 ? max(0, r0 + off - wl) : 0;
+      const int hi = wr >= 0 ? min(p.Nk - 1, rl + off + wr) : p.Nk - 1;
       if (hi < lo) {
         x.n[s] = 0;
       } else {
@@ -210,7 +218,7 @@ __device__ __forceinline__ int unit_at(int round, int c) {
   return round * G + ((round & 1) ? (G - 1 - c) : c);
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool WIN>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -278,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int rnd = 0; ok; ++rnd) {
       const int u = unit_at(rnd, blockIdx.x);
       if (u >= p.n_items) break;
-      const Unit un = decode_unit<CAUSAL>(p, u);
+      const Unit un = decode_unit<CAUSAL, WIN>(p, u);
       const int n = un.n[s];
       const int blk0 = blk;
       blk += un.nb;
@@ -286,6 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int rg = un.row0 + s * 128 + row;  // global query row
       const int off = p.Nk - p.Nq;
       const int r0 = un.row0 + s * 128, rl = min(r0 + 127, p.Nq - 1);  // the stage's rows
+      const int wl = win_l<WIN>(p), wr = win_r<WIN>(p);
       float m_run = -INFINITY, l_run = 0.0f;
       for (int j = 0; j < n; ++j) {
         if (!mbar_wait_bounded(&ctl.s_full[s], ph_s, abort_flag, LIM)) { ok = false; break; }
@@ -300,12 +309,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // a tile needs masking when it reaches past the keys or crosses a
         // window edge of some row of the stage
         const bool need_mask = (kb + 127 >= p.Nk) ||
-                               (CAUSAL && ((p.wr >= 0 && kb + 127 > r0 + off + p.wr) || (p.wl >= 0 && kb < rl + off - p.wl)));
+                               (CAUSAL && ((wr >= 0 && kb + 127 > r0 + off + wr) || (wl >= 0 && kb < rl + off - wl)));
         if (need_mask) {
           int lim = p.Nk - kb;  // columns [lo_c, lim) of this row are visible
           int lo_c = 0;
-          if (CAUSAL && p.wr >= 0) lim = min(lim, rg + off + p.wr + 1 - kb);
-          if (CAUSAL && p.wl >= 0) lo_c = rg + off - p.wl - kb;
+          if (CAUSAL && wr >= 0) lim = min(lim, rg + off + wr + 1 - kb);
+          if (CAUSAL && wl >= 0) lo_c = rg + off - wl - kb;
 #pragma unroll
           for (int c = 0; c < 128; ++c)
             if (c >= lim || c < lo_c) x[c] = f2u(-INFINITY);
@@ -384,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int rnd = 0; ok; ++rnd) {
       const int u = unit_at(rnd, blockIdx.x);
       if (u >= p.n_items) break;
-      const Unit un = decode_unit<CAUSAL>(p, u);
+      const Unit un = decode_unit<CAUSAL, WIN>(p, u);
       const int blk0 = blk;
       blk += un.nb;
       for (int j = 0; j < un.nb && ok; ++j) {
@@ -496,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int rnd = 0; ok; ++rnd) {
         const int u = unit_at(rnd, blockIdx.x);
         if (u >= p.n_items) break;
-        const Unit un = decode_unit<CAUSAL>(p, u);
+        const Unit un = decode_unit<CAUSAL, WIN>(p, u);
         if (un.nb == 0) continue;
         if (!first) {
           if (!mbar_wait_bounded(&ctl.q_empty, ph_qe, abort_flag, LIM)) { ok = false; break; }
@@ -579,7 +588,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int rnd = 0; ok; ++rnd) {
         const int u = unit_at(rnd, blockIdx.x);
         if (u >= p.n_items) break;
-        const Unit un = decode_unit<CAUSAL>(p, u);
+        const Unit un = decode_unit<CAUSAL, WIN>(p, u);
         if (un.nb == 0) continue;
         for (int s = 0; s < 2 && ok; ++s) {
           if (un.n[s] == 0) continue;
@@ -649,7 +658,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) trace_stamp(p.trace, kEv, 7);
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool WIN>
 cudaError_t launch_t(const Problem& pb, void* o, float* lse, cudaStream_t stream) {
   CUtensorMap mq, mk, mv, mo;
   if (!make_bshd_map(&mq, pb.q, pb.B, pb.Nq, pb.Hq, D, 128) || !make_bshd_map(&mk, pb.k, pb.B, pb.Nk, pb.Hkv, D, 128) ||
@@ -686,7 +695,7 @@ cudaError_t launch_t(const Problem& pb, void* o, float* lse, cudaStream_t stream
   p.trace = dc.trace;
   p.status = status_word();
   if (!p.status) return cudaErrorMemoryAllocation;
-  auto kern = fa_fwd_kernel<D, CAUSAL>;
+  auto kern = fa_fwd_kernel<D, CAUSAL, WIN>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmemDyn);
   if (e != cudaSuccess) return e;
   const int grid = p.n_items < G ? p.n_items : G;
@@ -700,9 +709,15 @@ cudaError_t launch_t(const Problem& pb, void* o, float* lse, cudaStream_t stream
 }  // namespace fwd
 
 cudaError_t launch_fwd(const Problem& p, void* o, float* lse, cudaStream_t stream) {
+  // three kernels per head dim: no mask, the plain causal mask, any window
   const bool m = p.masked();
-  if (p.d == 128) return m ? fwd::launch_t<128, true>(p, o, lse, stream) : fwd::launch_t<128, false>(p, o, lse, stream);
-  return m ? fwd::launch_t<64, true>(p, o, lse, stream) : fwd::launch_t<64, false>(p, o, lse, stream);
+  const bool win = m && !p.plain_causal();
+  if (p.d == 128) {
+    if (!m) return fwd::launch_t<128, false, false>(p, o, lse, stream);
+    return win ? fwd::launch_t<128, true, true>(p, o, lse, stream) : fwd::launch_t<128, true, false>(p, o, lse, stream);
+  }
+  if (!m) return fwd::launch_t<64, false, false>(p, o, lse, stream);
+  return win ? fwd::launch_t<64, true, true>(p, o, lse, stream) : fwd::launch_t<64, true, false>(p, o, lse, stream);
 }
 
 }  // namespace fa

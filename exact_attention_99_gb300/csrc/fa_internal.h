@@ -20,6 +20,8 @@ struct Problem {
   // <= i + off + window_right (off = Nk - Nq); -1 = no limit on that side
   int window_left = -1, window_right = -1;
   bool masked() const { return causal || window_left >= 0 || window_right >= 0; }
+  // the causal mask and nothing else (window bounds already normalised)
+  bool plain_causal() const { return window_left < 0 && (causal || window_right == 0); }
 };
 
 struct DebugCfg {
