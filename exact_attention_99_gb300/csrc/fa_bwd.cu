@@ -519,18 +519,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < D / 64; ++c)
             tma_load_4d(sQ + qs * C::kTile + c * 16384, &tmQ, &ctl.q_full[qs], c * 64, h, it * 128, w.b);
-          if (!mbar_wait_bounded(&ctl.do_empty, (g & 1) ^ 1, abort_flag, LIM)) { ok = false; break; }
-          trace_stamp(p.trace, g, 14);
-          mbar_arrive_expect_tx(&ctl.do_full, C::kTile);
-#pragma unroll
-          for (int c = 0; c < D / 64; ++c)
-            tma_load_4d(sDO + c * 16384, &tmDO, &ctl.do_full, c * 64, h, it * 128, w.b);
+          // LSE/D rows before dO: the compute warps need them as soon as
+          // S is ready, while dO (one slot) waits for the previous dV
           const int vs = g & 1;
           if (!mbar_wait_bounded(&ctl.vec_empty[vs], ((g >> 1) & 1) ^ 1, abort_flag, LIM)) { ok = false; break; }
           mbar_arrive_expect_tx(&ctl.vec_full[vs], 1024);
           const size_t roff = (size_t(w.b) * p.Hq + h) * p.Nq_pad + size_t(it) * 128;
           bulk_load(sVec + vs * 256, p.lse2 + roff, 512, &ctl.vec_full[vs]);
           bulk_load(sVec + vs * 256 + 128, p.delta + roff, 512, &ctl.vec_full[vs]);
+          if (!mbar_wait_bounded(&ctl.do_empty, (g & 1) ^ 1, abort_flag, LIM)) { ok = false; break; }
+          trace_stamp(p.trace, g, 14);
+          mbar_arrive_expect_tx(&ctl.do_full, C::kTile);
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_4d(sDO + c * 16384, &tmDO, &ctl.do_full, c * 64, h, it * 128, w.b);
         }
       }
       if (*abort_flag) {
