@@ -467,18 +467,27 @@ def run_profile_target(args):
     __graft_entry__.build()
     import exact_attention_99_gb300 as fa
     fa.fa_debug_set(0, 0)
-    byname = {w.name: w for w in workloads.WORKLOADS}
-    w = byname[args.profile_workload]
-    x = workloads.workload_inputs(w, with_dout=True)
+    if args.profile_workload == WINDOW_CASE["name"]:
+        c = WINDOW_CASE
+        x = workloads.make_inputs(c["B"], c["H"], c["H"], c["N"], c["N"], c["d"], c["seed"], with_dout=True)
+        a = (c["B"], c["H"], c["H"], c["N"], c["N"], c["d"], c["d"] ** -0.5, *c["window"])
+        fwd_call, bwd_call = fa.fa_fwd_window, fa.fa_bwd_window
+        B, H, N = c["B"], c["H"], c["N"]
+    else:
+        byname = {w.name: w for w in workloads.WORKLOADS}
+        w = byname[args.profile_workload]
+        x = workloads.workload_inputs(w, with_dout=True)
+        a = (w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.d, w.scale, int(w.causal))
+        fwd_call, bwd_call = fa.fa_fwd, fa.fa_bwd
+        B, H, N = w.B, w.Hq, w.Nq
     q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
     o, dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    lse = torch.empty((w.B, w.Hq, w.Nq), device="cuda", dtype=torch.float32)
-    a = (w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.d, w.scale, int(w.causal))
-    if fa.fa_fwd(q, k, v, o, lse, *a):
-        raise RuntimeError("fa_fwd failed")
+    lse = torch.empty((B, H, N), device="cuda", dtype=torch.float32)
+    if fwd_call(q, k, v, o, lse, *a):
+        raise RuntimeError("forward failed")
     for _ in range(args.warmup + args.steps):
-        st = fa.fa_fwd(q, k, v, o, lse, *a) if args.profile_pass == "fwd" else \
-            fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, *a)
+        st = fwd_call(q, k, v, o, lse, *a) if args.profile_pass == "fwd" else \
+            bwd_call(q, k, v, o, lse, do, dq, dk, dv, *a)
         if st:
             raise RuntimeError(f"launch failed: {st}")
     torch.cuda.synchronize()
