@@ -313,6 +313,41 @@ def window_config(fa, flush, peak):
             "bwd_tflops": round(2.5 * fwd_fl / bms / 1e9, 4), "bwd_frac_of_peak": round(2.5 * fwd_fl / bms / 1e9 / peak, 4)}
 
 
+def fp8_config(fa, flush, peak):
+    """The e4m3 forward (incoherent transform on) of the two d = 128 forward
+    workloads: whole call (quantisation included) and the attention kernel
+    alone, against twice the measured bf16 peak (the nominal fp8:bf16 ratio
+    of the tensor cores)."""
+    import torch
+    out = {}
+    for w in (workloads.WORKLOADS[1], workloads.WORKLOADS[2]):
+        x = workloads.workload_inputs(w)
+        q, k, v = (x[n].cuda() for n in ("q", "k", "v"))
+        o = torch.empty_like(q)
+        lse = torch.empty((w.B, w.Hq, w.Nq), device="cuda", dtype=torch.float32)
+        a = (w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.d, w.scale, int(w.causal), 1)
+        ms = time_one(lambda: fa.fa_fwd_fp8(q, k, v, o, lse, *a), flush)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(); e1.record()
+        ks = []
+        for _ in range(5):
+            flush.zero_()
+            fa.fa_profile_events(e0, e1)
+            fa.fa_fwd_fp8(q, k, v, o, lse, *a)
+            fa.fa_profile_events(None, None)
+            torch.cuda.synchronize()
+            ks.append(e0.elapsed_time(e1))
+        kms = statistics.median(ks)
+        fl = w.fwd_flops()
+        out["fp8_" + w.name] = {"call_ms": round(ms, 4), "call_tflops": round(fl / ms / 1e9, 2),
+                                "kernel_ms": round(kms, 4), "kernel_tflops": round(fl / kms / 1e9, 2),
+                                "kernel_frac_of_fp8_peak": round(fl / kms / 1e9 / (2 * peak), 4),
+                                "fp8_peak": "2 x measured bf16 (nominal ratio)"}
+        del q, k, v, o, lse
+    assert fa.fa_get_status() == 0
+    return out
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -429,6 +464,7 @@ def run_ours(args):
 
     configs = per_config(fa, flush, peak)
     configs[WINDOW_CASE["name"]] = window_config(fa, flush, peak)
+    configs.update(fp8_config(fa, flush, peak))
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(total_ms / K, 4), "higher_is_better": True, "scaling": "weak",

@@ -55,6 +55,8 @@ def lib() -> ctypes.CDLL:
         L.fa_fwd.restype = i
         L.fa_fwd_window.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, vp]
         L.fa_fwd_window.restype = i
+        L.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, vp]
+        L.fa_fwd_fp8.restype = i
         L.fa_bwd.argtypes = [vp] * 9 + [i, i, i, i, i, i, f, i, vp]
         L.fa_bwd.restype = i
         L.fa_bwd_window.argtypes = [vp] * 9 + [i, i, i, i, i, i, f, i, i, vp]
@@ -102,6 +104,28 @@ def fa_fwd(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, stream=None) -
 def fa_fwd_window(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, window_left, window_right, stream=None) -> int:
     return lib().fa_fwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Nq, Nk, d, float(scale),
                                int(window_left), int(window_right), _stream(stream))
+
+
+def fa_fwd_fp8(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, incoherent=1, stream=None) -> int:
+    return lib().fa_fwd_fp8(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Nq, Nk, d, float(scale),
+                            int(causal), int(incoherent), _stream(stream))
+
+
+def forward_fp8(q, k, v, causal: bool = False, scale: float | None = None, incoherent: bool = True, stream=None):
+    """O, LSE of the e4m3 forward (d = 128; see fa.h fa_fwd_fp8)."""
+    import torch
+    B, Nq, Hq, d = q.shape
+    _, Nk, Hkv, _ = k.shape
+    _check_bshd("q", q, B, Nq, Hq, d)
+    _check_bshd("k", k, B, Nk, Hkv, d)
+    _check_bshd("v", v, B, Nk, Hkv, d)
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, Nq), device=q.device, dtype=torch.float32)
+    st = fa_fwd_fp8(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, int(incoherent), stream)
+    if st != 0:
+        raise FAError(st, "fa_fwd_fp8")
+    return o, lse
 
 
 def _window_args(causal, window):

@@ -234,6 +234,24 @@ extern "C" int fa_fwd_window(const void* q, const void* k, const void* v, void* 
   return launch_fwd(p, o, lse, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
+extern "C" int fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                          int Nq, int Nk, int d, float scale, int causal, int incoherent, void* stream) {
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return FA_ERR_INVALID_ARG;
+  if (incoherent != 0 && incoherent != 1) return FA_ERR_INVALID_ARG;
+  int st = check_sizes(B, Hq, Hkv, Nq, Nk, d, scale, causal);
+  if (st != FA_OK) return st;
+  if (d != 128) return FA_ERR_UNSUPPORTED;
+  st = check_device();
+  if (st != FA_OK) return st;
+  const Problem p{q, k, v, B, Hq, Hkv, Nq, Nk, d, scale, causal};
+  const cudaError_t e = launch_fwd8(p, o, lse, incoherent, static_cast<cudaStream_t>(stream));
+  if (e == cudaErrorMemoryAllocation) {
+    cudaGetLastError();
+    return FA_ERR_ALLOC;
+  }
+  return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
 namespace {
 // fa_bwd / fa_bwd_window after their checks: workspace from the pool,
 // launch, free, all on the caller's stream

@@ -58,6 +58,9 @@ int normalize_window(int w, int Nq, int Nk);
 
 // Launchers. Return a cudaError_t (cudaSuccess on success).
 cudaError_t launch_fwd(const Problem& p, void* o, float* lse, cudaStream_t stream);
+// FP8 (e4m3) forward, d = 128 only; incoherent != 0 applies the Hadamard
+// transform to Q and K before quantisation. Workspace from the pool.
+cudaError_t launch_fwd8(const Problem& p, void* o, float* lse, int incoherent, cudaStream_t stream);
 // The host-side checks fa_bwd performs (pointers, sizes, device), as one call.
 int check_bwd_args(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
                    void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Nq, int Nk, int d, float scale,

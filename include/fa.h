@@ -80,6 +80,27 @@ int fa_fwd_window(const void* q, const void* k, const void* v, void* o, float* l
                   int Nk, int d, float scale, int window_left, int window_right, void* stream);
 
 /*
+ * fa_fwd_fp8 — the forward pass with e4m3 (FP8) tensor-core GEMMs, d = 128.
+ *   Inputs, outputs, layouts and the causal flag as fa_fwd (bf16 q, k, v in,
+ *   bf16 o and fp32 lse out). incoherent = 1 first multiplies Q and K along
+ *   d by diag(signs) H_128 / sqrt(128) (H the Sylvester-Hadamard matrix;
+ *   sign_i = -1 where bit 31 of 2654435769 * (i + 1) mod 2^32 is set), which
+ *   leaves Q K^T unchanged and spreads outlier channels; incoherent = 0
+ *   skips it. Q (transformed), K (transformed) and V are then scaled per
+ *   (batch, head) so their largest magnitude maps to 448 and rounded to e4m3
+ *   (nearest, ties to even); P is rounded to e4m3 for the P V GEMM. The
+ *   result approximates fa_fwd's: O is the attention of the dequantised
+ *   tensors up to the rounding of P.
+ *   Workspace: the e4m3 copies (B*(Nq*Hq + Nk*Hkv)*128 bytes plus
+ *   B*Hkv*128*ceil(Nk/128)*128 for V transposed) and per-head maxima, from
+ *   the per-device pool fa_bwd uses, on `stream`.
+ *   Errors as fa_fwd; d != 128 returns FA_ERR_UNSUPPORTED; incoherent other
+ *   than 0/1 returns FA_ERR_INVALID_ARG.
+ */
+int fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Nq,
+               int Nk, int d, float scale, int causal, int incoherent, void* stream);
+
+/*
  * fa_bwd — backward pass for L = sum(dout * o).
  *   in : q, k, v, o (bf16), lse (fp32, as written by fa_fwd for the same
  *        inputs), dout [B,Nq,Hq,d] (bf16)

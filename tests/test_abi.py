@@ -69,6 +69,24 @@ def test_bad_sizes_rejected_on_host(fa, call, bad, code):
     assert call(fa, **bad) == code
 
 
+def fwd8(fa, ptrs=(P16,) * 5, incoherent=1, **kw):
+    a = dict(GOOD, **kw)
+    return fa.fa_fwd_fp8(*ptrs, a["B"], a["Hq"], a["Hkv"], a["Nq"], a["Nk"], a["d"], a["scale"], a["causal"],
+                         incoherent, 0)
+
+
+@pytest.mark.parametrize("bad,code", [
+    (dict(d=64), 2), (dict(d=96), 2), (dict(Hq=3, Hkv=2), 1), (dict(Nq=0), 1), (dict(causal=2), 1),
+    (dict(scale=float("nan")), 1), (dict(incoherent=2), 1), (dict(incoherent=-1), 1),
+])
+def test_fp8_bad_arguments_rejected_on_host(fa, bad, code):
+    assert fwd8(fa, **bad) == code
+    for which in range(5):
+        ptrs = [P16] * 5
+        ptrs[which] = P16 + 4
+        assert fwd8(fa, ptrs=tuple(ptrs)) == 1
+
+
 @pytest.mark.parametrize("which", range(5))
 def test_bad_pointers_fwd(fa, which):
     for bad in (0, P16 + 8):  # null, misaligned
@@ -90,6 +108,7 @@ def test_no_device_fails_loudly(fa):
     # valid arguments without a usable device: an error, never a silent fallback
     assert fwd(fa) == 6
     assert bwd(fa) == 6
+    assert fwd8(fa) == 6
     with pytest.raises((RuntimeError, ValueError)):
         fa.forward(torch.zeros(1, 8, 1, 64, dtype=torch.bfloat16), torch.zeros(1, 8, 1, 64, dtype=torch.bfloat16),
                    torch.zeros(1, 8, 1, 64, dtype=torch.bfloat16))

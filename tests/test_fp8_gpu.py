@@ -1,0 +1,120 @@
+"""FP8 (e4m3) forward on a GB300 against the FP8 oracle: the attention of
+the dequantised e4m3 tensors (oracle/attn_fp8_ref.py), elementwise within
+the bound that rounding P to e4m3 allows, plus the incoherent transform's
+effect on inputs with outlier channels."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from oracle import attn_fp8_ref as f8
+from oracle import attn_ref
+from tests.gpu_util import to64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fa():
+    import __graft_entry__
+    __graft_entry__.build()
+    import exact_attention_99_gb300 as m
+    assert torch.cuda.is_available(), "GPU tests need a GPU"
+    m.fa_debug_set(0, 0)
+    return m
+
+
+def fp8_case(fa, x, causal, incoherent, scale):
+    q, k, v = (x[n].cuda() for n in ("q", "k", "v"))
+    o, lse = fa.forward_fp8(q, k, v, causal=causal, scale=scale, incoherent=incoherent)
+    torch.cuda.synchronize()
+    assert fa.fa_get_status() == 0
+    return to64(o), to64(lse)
+
+
+def rounding_sd(qd, kd, vd, scale, causal):
+    """Standard deviation of O's error if every P_ij is rounded to e4m3 with
+    an independent error uniform in +-half an ulp (2^-4 relative):
+    (2^-4 / sqrt(3)) * sqrt(sum_j P_ij^2 V_jc^2), per output element."""
+    B, Nq, Hq, d = qd.shape
+    g = Hq // kd.shape[2]
+    out = np.zeros_like(qd)
+    for b in range(B):
+        for h in range(Hq):
+            P = attn_ref.probabilities(qd[b, :, h], kd[b, :, h // g], scale, causal)
+            out[b, :, h] = np.sqrt((P ** 2) @ (vd[b, :, h // g] ** 2))
+    return 2.0 ** -4 / np.sqrt(3.0) * out
+
+
+def check_against_oracle(go, glse, x, causal, incoherent, scale, mean_check=True):
+    """Elementwise: |err| <= 2^-4 sum_j P_ij |V_jc| (P rounding, worst case)
+    + 2^-8 |O| (bf16 output) + 4e-3 (e4m3 codes that the fp32 transform and
+    scale put on the other side of a rounding tie than fp64 does). Mean:
+    at most twice the expected |error| of independent P rounding."""
+    qn, kn, vn = (x[n].double().numpy() for n in ("q", "k", "v"))
+    ro, rlse, (qd, kd, vd) = f8.forward_fp8(qn, kn, vn, scale, causal, incoherent=incoherent)
+    bound = 2.0 ** -4 * f8.pv_abs(qd, kd, vd, scale, causal) + 2.0 ** -8 * np.abs(ro) + 4e-3
+    err = np.abs(go - ro)
+    worst = np.unravel_index(np.argmax(err - bound), err.shape)
+    assert np.all(err <= bound), (f"worst |err| {err[worst]:.3e} > bound {bound[worst]:.3e} at {worst}; "
+                                  f"max-abs {err.max():.3e}, mean-abs {err.mean():.3e}")
+    if mean_check:
+        expect = float(np.mean(rounding_sd(qd, kd, vd, scale, causal))) * np.sqrt(2 / np.pi)
+        assert float(err.mean()) <= 2 * expect + 5e-4, (err.mean(), expect)
+    fin = np.isfinite(rlse)  # rows that see no key: -inf on both sides
+    assert np.array_equal(np.isfinite(glse), fin) and np.all(glse[~fin] == rlse[~fin])
+    lerr = np.abs(glse[fin] - rlse[fin])
+    assert float(lerr.max()) <= 2e-2 and float(lerr.mean()) <= 2e-3, (lerr.max(), lerr.mean())
+
+
+SHAPES = [
+    # B, Hq, Hkv, Nq, Nk
+    (1, 2, 2, 256, 256),
+    (1, 4, 2, 300, 300),
+    (2, 2, 1, 129, 700),
+    (1, 2, 2, 700, 129),
+]
+
+
+@pytest.mark.parametrize("incoherent", [True, False])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_fp8_matches_oracle(fa, shape, causal, incoherent):
+    B, Hq, Hkv, Nq, Nk = shape
+    x = workloads.make_inputs(B, Hq, Hkv, Nq, Nk, 128, seed=sum(shape) + 2 * causal + incoherent)
+    scale = 1.0 / math.sqrt(128)
+    go, glse = fp8_case(fa, x, causal, incoherent, scale)
+    check_against_oracle(go, glse, x, causal, incoherent, scale)
+
+
+def test_fp8_full_size_sampled(fa):
+    """The non-causal B=4, H=16, N=2048 workload through the FP8 path: finite
+    everywhere, two heads against the oracle."""
+    w = workloads.WORKLOADS[1]
+    x = workloads.workload_inputs(w)
+    go, glse = fp8_case(fa, x, False, True, w.scale)
+    assert np.isfinite(go).all() and np.isfinite(glse).all()
+    for b, h in [(0, 0), (3, 15)]:
+        sl = {n: x[n][b:b + 1, :, h:h + 1] for n in ("q", "k", "v")}
+        check_against_oracle(go[b:b + 1, :, h:h + 1], glse[b:b + 1, h:h + 1], sl, False, True, w.scale,
+                             mean_check=False)
+
+
+def test_fp8_incoherent_lowers_error_with_outliers(fa):
+    """Against the exact bf16-input attention: with outlier channels in Q
+    and K, the incoherent transform lowers the FP8 error."""
+    B, H, N, d = 1, 4, 512, 128
+    x = workloads.make_inputs(B, H, H, N, N, d, seed=77)
+    for n in ("q", "k"):
+        t = x[n].float()
+        t[..., [5, 90]] *= 20.0
+        x[n] = t.to(torch.bfloat16)
+    scale = 0.5 / math.sqrt(d)
+    exact, _ = attn_ref.forward(*(x[n].double().numpy() for n in ("q", "k", "v")), scale, False)
+    err = {}
+    for inc in (False, True):
+        go, _ = fp8_case(fa, x, False, inc, scale)
+        err[inc] = float(np.sqrt(np.mean((go - exact) ** 2)))
+    assert err[True] * 1.5 < err[False], err
