@@ -495,9 +495,11 @@ def run_ours(args):
 
 
 def run_profile_target(args):
-    """Profiling target: runs only the forward or only the backward of one
-    named workload, --warmup + --steps times, and prints nothing else. Used
-    to capture one kernel of one workload under ncu; prints no bench line."""
+    """Profiling target: runs only the forward (fwd), the e4m3 forward with
+    the incoherent transform (fwd8, d = 128 workloads) or only the backward
+    of one named workload, --warmup + --steps times, and prints nothing else.
+    Used to capture one kernel of one workload under ncu; prints no bench
+    line."""
     import torch
     import __graft_entry__
     __graft_entry__.build()
@@ -521,8 +523,12 @@ def run_profile_target(args):
     lse = torch.empty((B, H, N), device="cuda", dtype=torch.float32)
     if fwd_call(q, k, v, o, lse, *a):
         raise RuntimeError("forward failed")
+    if args.profile_pass == "fwd8":
+        if fwd_call is not fa.fa_fwd:
+            raise ValueError("fwd8 profiles the unmasked or causal forward only")
+        fwd_call = lambda *xs: fa.fa_fwd_fp8(*xs, 1)
     for _ in range(args.warmup + args.steps):
-        st = fwd_call(q, k, v, o, lse, *a) if args.profile_pass == "fwd" else \
+        st = fwd_call(q, k, v, o, lse, *a) if args.profile_pass in ("fwd", "fwd8") else \
             bwd_call(q, k, v, o, lse, do, dq, dk, dv, *a)
         if st:
             raise RuntimeError(f"launch failed: {st}")
@@ -539,7 +545,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--profile-workload", default=None, help="profiling target: run one workload's pass only")
-    ap.add_argument("--profile-pass", choices=["fwd", "bwd"], default="fwd")
+    ap.add_argument("--profile-pass", choices=["fwd", "fwd8", "bwd"], default="fwd")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     if args.profile_workload:
