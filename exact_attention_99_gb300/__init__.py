@@ -58,6 +58,8 @@ def lib() -> ctypes.CDLL:
         L.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, vp]
         L.fa_fwd_fp8.restype = i
         L.fa_bwd.argtypes = [vp] * 9 + [i, i, i, i, i, i, f, i, vp]
+        L.fa_step_host.argtypes = [vp] * 9 + [i, i, i, i, i, i, f, i, vp]
+        L.fa_step_host.restype = i
         L.fa_bwd.restype = i
         L.fa_bwd_window.argtypes = [vp] * 9 + [i, i, i, i, i, i, f, i, i, vp]
         L.fa_bwd_window.restype = i
@@ -104,6 +106,12 @@ def fa_fwd(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, stream=None) -
 def fa_fwd_window(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, window_left, window_right, stream=None) -> int:
     return lib().fa_fwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Nq, Nk, d, float(scale),
                                int(window_left), int(window_right), _stream(stream))
+
+
+def fa_step_host(q, k, v, dout, o, lse, dq, dk, dv, B, Hq, Hkv, Nq, Nk, d, scale, causal, stream=None) -> int:
+    """Forward + backward on host (CPU, preferably pinned) tensors; see fa.h fa_step_host."""
+    return lib().fa_step_host(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(o), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
+                              B, Hq, Hkv, Nq, Nk, d, float(scale), int(causal), _stream(stream))
 
 
 def fa_fwd_fp8(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, incoherent=1, stream=None) -> int:

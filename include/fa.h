@@ -127,6 +127,33 @@ int fa_bwd_window(const void* q, const void* k, const void* v, const void* o, co
                   int window_left, int window_right, void* stream);
 
 /*
+ * fa_step_host — one forward and backward pass on HOST buffers: the
+ * end-to-end call for a caller whose tensors live in host memory. The
+ * operations are those of fa_fwd followed by fa_bwd (same arguments, layouts
+ * and results), with every pointer a host address:
+ *   in : q [B,Nq,Hq,d], k, v [B,Nk,Hkv,d], dout [B,Nq,Hq,d] (bf16)
+ *   out: o [B,Nq,Hq,d] (bf16), lse [B,Hq,Nq] (fp32), dq, dk, dv (bf16).
+ * The batch is processed one element at a time and pipelined: the inputs of
+ * element b are copied in on a library-owned copy stream while element b-1
+ * computes on `stream` and the results of element b-2 are copied out on a
+ * second copy stream. The call only enqueues; `stream` is ordered after all
+ * of it, so synchronise `stream` before reading the outputs, and keep every
+ * host buffer alive (and the inputs unchanged) until then. Page-locked host
+ * memory gives asynchronous, full-speed copies; pageable memory works but
+ * the copies are staged by the driver.
+ * Device memory: a copy of every tensor of the batch (about the size of
+ * all inputs and outputs) from the same stream-ordered pool as fa_bwd,
+ * freed on `stream` at the end, plus the backward's own workspace.
+ * Errors: a null pointer or a bad size gives FA_ERR_INVALID_ARG /
+ * FA_ERR_UNSUPPORTED before anything is enqueued; FA_ERR_ALLOC if the device
+ * copy cannot be allocated; FA_ERR_LAUNCH if a copy, launch or event call
+ * fails (work already enqueued still completes in order on `stream`).
+ */
+int fa_step_host(const void* q, const void* k, const void* v, const void* dout, void* o, float* lse, void* dq,
+                 void* dk, void* dv, int B, int Hq, int Hkv, int Nq, int Nk, int d, float scale, int causal,
+                 void* stream);
+
+/*
  * fa_bwd_noalloc — the same backward pass as fa_bwd, for callers that may
  * not allocate device memory during the call: serving loops that fix their
  * memory plan at start-up, and code that runs where the CUDA allocator must

@@ -87,6 +87,21 @@ def test_fp8_bad_arguments_rejected_on_host(fa, bad, code):
         assert fwd8(fa, ptrs=tuple(ptrs)) == 1
 
 
+def step_host(fa, ptrs=(P16,) * 9, **kw):
+    a = dict(GOOD, **kw)
+    return fa.fa_step_host(*ptrs, a["B"], a["Hq"], a["Hkv"], a["Nq"], a["Nk"], a["d"], a["scale"], a["causal"], 0)
+
+
+def test_step_host_rejects_bad_arguments(fa):
+    for which in range(9):
+        ptrs = [P16] * 9
+        ptrs[which] = 0
+        assert step_host(fa, ptrs=tuple(ptrs)) == 1
+    assert step_host(fa, d=96) == 2
+    assert step_host(fa, Hq=3, Hkv=2) == 1
+    assert step_host(fa, Nq=0) == 1
+
+
 @pytest.mark.parametrize("which", range(5))
 def test_bad_pointers_fwd(fa, which):
     for bad in (0, P16 + 8):  # null, misaligned
@@ -109,6 +124,7 @@ def test_no_device_fails_loudly(fa):
     assert fwd(fa) == 6
     assert bwd(fa) == 6
     assert fwd8(fa) == 6
+    assert step_host(fa) == 6
     with pytest.raises((RuntimeError, ValueError)):
         fa.forward(torch.zeros(1, 8, 1, 64, dtype=torch.bfloat16), torch.zeros(1, 8, 1, 64, dtype=torch.bfloat16),
                    torch.zeros(1, 8, 1, 64, dtype=torch.bfloat16))
