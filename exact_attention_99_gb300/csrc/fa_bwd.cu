@@ -658,78 +658,105 @@ template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* o, const __nv_bfloat16* dout,
                                                       const float* lse, float* lse2, float* delta, float* dq_acc,
                                                       int B, int Hq, int Nq, int Nq_pad) {
-  constexpr int TPR = D / 8;  // threads per row, 8 elements (16 bytes) each
+  constexpr int TPR = D / 8;     // threads per row, 8 elements (16 bytes) each
+  constexpr int RPW = 32 / TPR;  // rows a warp covers per pass
+  constexpr int R = 4;           // passes whose loads are issued before any is reduced
   const long long rows = 1LL * B * Nq * Hq;
+  const int lane = threadIdx.x & 31;
+  const int part = lane % TPR, sub = lane / TPR;
   const long long tid = 1LL * blockIdx.x * blockDim.x + threadIdx.x;
-  const long long r = tid / TPR;
-  const int part = int(tid % TPR);
-  float acc = 0.0f;
-  if (r < rows) {
-    const uint4 a = *reinterpret_cast<const uint4*>(o + r * D + part * 8);
-    const uint4 g = *reinterpret_cast<const uint4*>(dout + r * D + part * 8);
-    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
-    const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&g);
+  const long long nthreads = 1LL * gridDim.x * blockDim.x;
+  const long long wstep = (nthreads >> 5) * RPW * R;
+  // the loop bound is the same for all lanes of a warp (the shuffles need all 32)
+  for (long long r0 = (tid >> 5) * RPW * R; r0 < rows; r0 += wstep) {
+    uint4 a[R], g[R];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float2 fa = __bfloat1622float2(a2[i]), fg = __bfloat1622float2(g2[i]);
-      acc = fmaf(fa.x, fg.x, acc);
-      acc = fmaf(fa.y, fg.y, acc);
+    for (int i = 0; i < R; ++i) {
+      const long long r = r0 + i * RPW + sub;
+      a[i] = g[i] = make_uint4(0, 0, 0, 0);
+      if (r < rows) {
+        a[i] = *reinterpret_cast<const uint4*>(o + r * D + part * 8);
+        g[i] = *reinterpret_cast<const uint4*>(dout + r * D + part * 8);
+      }
     }
-  }
 #pragma unroll
-  for (int s = TPR / 2; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
-  if (r < rows && part == 0) {
-    // r indexes [B, Nq, Hq]
-    const int h = int(r % Hq);
-    const long long bq = r / Hq;
-    const int q = int(bq % Nq);
-    const int b = int(bq / Nq);
-    const size_t dst = (size_t(b) * Hq + h) * Nq_pad + q;
-    const float l = lse[(size_t(b) * Hq + h) * Nq + q];
-    lse2[dst] = l == -INFINITY ? INFINITY : l * 1.4426950408889634f;
-    delta[dst] = acc;
+    for (int i = 0; i < R; ++i) {
+      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a[i]);
+      const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&g[i]);
+      float acc = 0.0f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 fa = __bfloat1622float2(a2[e]), fg = __bfloat1622float2(g2[e]);
+        acc = fmaf(fa.x, fg.x, acc);
+        acc = fmaf(fa.y, fg.y, acc);
+      }
+#pragma unroll
+      for (int m = TPR / 2; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
+      const long long r = r0 + i * RPW + sub;
+      if (r < rows && part == 0) {
+        // r indexes [B, Nq, Hq]
+        const int h = int(r % Hq);
+        const long long bq = r / Hq;
+        const int q = int(bq % Nq);
+        const int b = int(bq / Nq);
+        const size_t dst = (size_t(b) * Hq + h) * Nq_pad + q;
+        const float l = lse[(size_t(b) * Hq + h) * Nq + q];
+        lse2[dst] = l == -INFINITY ? INFINITY : l * 1.4426950408889634f;
+        delta[dst] = acc;
+      }
+    }
   }
   // padded rows
   const long long pad = 1LL * B * Hq * (Nq_pad - Nq);
-  const long long nthreads = 1LL * gridDim.x * blockDim.x;
   for (long long i = tid; i < pad; i += nthreads) {
     const long long bh = i / (Nq_pad - Nq);
     const int q = Nq + int(i % (Nq_pad - Nq));
     lse2[bh * Nq_pad + q] = INFINITY;
     delta[bh * Nq_pad + q] = 0.0f;
   }
-  // zero the dQ accumulator
+  // zero the dQ accumulator, four 16-byte stores per thread per pass
   const long long n4 = 1LL * B * Hq * D * Nq_pad / 4;
-  for (long long i = tid; i < n4; i += nthreads) reinterpret_cast<float4*>(dq_acc)[i] = make_float4(0, 0, 0, 0);
+  float4* acc4 = reinterpret_cast<float4*>(dq_acc);
+  const float4 z = make_float4(0, 0, 0, 0);
+  for (long long i = tid; i < n4; i += 4 * nthreads) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (i + u * nthreads < n4) acc4[i + u * nthreads] = z;
+  }
 }
 
-// dq[b, q, h, :] = bf16(scale * acc[b*Hq + h, :, q]). One thread per 8 d x
-// 4 q block: eight float4 loads (the two half-warps read the two halves of
-// each 32-byte sector), four 16-byte bf16 stores (16 consecutive threads
-// write one 256-byte row of dq).
+// dq[b, q, h, :] = bf16(scale * acc[b*Hq + h, :, q]), through a shared
+// tile: a block takes 64 queries of one (batch, head); each warp reads whole
+// 256-byte runs of accumulator rows (one d, 64 q), then every thread writes
+// 16-byte pieces of dq rows (16 consecutive threads write one 256-byte row
+// for d = 128).
 template <int D>
 __global__ void __launch_bounds__(256) bwd_post_kernel(const float* dq_acc, __nv_bfloat16* dq, int BH, int Hq, int Nq,
                                                        int Nq_pad, float scale) {
-  constexpr int kD8 = D / 8;
-  const long long t = 1LL * blockIdx.x * blockDim.x + threadIdx.x;
-  const long long per_bh = 1LL * kD8 * (Nq_pad / 4);
-  if (t >= per_bh * BH) return;
-  const int bh = int(t / per_bh);
-  const int r = int(t - bh * per_bh);
-  const int q4 = (r / kD8) * 4;
-  const int d8 = (r % kD8) * 8;
-  const float* src = dq_acc + (size_t(bh) * D + d8) * Nq_pad + q4;
-  float4 v[8];
+  __shared__ float tile[D][65];
+  const int nqt = Nq_pad / 64;
+  const int bh = blockIdx.x / nqt, qt = blockIdx.x - bh * nqt;
+  if (bh >= BH) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const float* src = dq_acc + size_t(bh) * D * Nq_pad + qt * 64 + 2 * lane;
+  float2 x[D / 8];
 #pragma unroll
-  for (int k = 0; k < 8; ++k) v[k] = *reinterpret_cast<const float4*>(src + size_t(k) * Nq_pad);
+  for (int i = 0; i < D / 8; ++i) x[i] = *reinterpret_cast<const float2*>(src + size_t(warp + 8 * i) * Nq_pad);
+#pragma unroll
+  for (int i = 0; i < D / 8; ++i) {
+    tile[warp + 8 * i][2 * lane] = x[i].x;
+    tile[warp + 8 * i][2 * lane + 1] = x[i].y;
+  }
+  __syncthreads();
   const int b = bh / Hq, h = bh - b * Hq;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int q = q4 + j;
-    if (q >= Nq) break;
+  constexpr int kD8 = D / 8;
+  for (int it = threadIdx.x; it < 64 * kD8; it += 256) {
+    const int ql = it / kD8, d8 = (it - ql * kD8) * 8;
+    const int q = qt * 64 + ql;
+    if (q >= Nq) continue;
     float f[8];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) f[k] = (j == 0 ? v[k].x : j == 1 ? v[k].y : j == 2 ? v[k].z : v[k].w) * scale;
+    for (int e = 0; e < 8; ++e) f[e] = tile[d8 + e][ql] * scale;
     *reinterpret_cast<uint4*>(dq + ((size_t(b) * Nq + q) * Hq + h) * D + d8) =
         make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
   }
@@ -744,10 +771,12 @@ cudaError_t launch_t(const Problem& pb, const void* o, const float* lse, const v
   float* lse2 = ws + acc_elems;
   float* delta = lse2 + size_t(pb.B) * pb.Hq * Nq_pad;
   {
-    const long long threads = 1LL * pb.B * pb.Nq * pb.Hq * (D / 8);
-    long long blocks = (threads + 255) / 256;
-    const long long minb = 4LL * num_sms();
+    // 8 warps a block, 32 / (D / 8) rows a warp per pass, 4 passes per load batch
+    const long long rows_per_block = 8LL * (32 / (D / 8)) * 4;
+    long long blocks = (1LL * pb.B * pb.Nq * pb.Hq + rows_per_block - 1) / rows_per_block;
+    const long long minb = 4LL * num_sms(), maxb = 32LL * num_sms();
     if (blocks < minb) blocks = minb;
+    if (blocks > maxb) blocks = maxb;
     bwd_pre_kernel<D><<<unsigned(blocks), 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(o),
                                                              static_cast<const __nv_bfloat16*>(dout), lse, lse2, delta,
                                                              dq_acc, pb.B, pb.Hq, pb.Nq, Nq_pad);
@@ -805,8 +834,8 @@ cudaError_t launch_t(const Problem& pb, const void* o, const float* lse, const v
   if (dc.ev_end) cudaEventRecord(dc.ev_end, stream);
   if (e != cudaSuccess) return e;
   {
-    const long long threads = 1LL * pb.B * pb.Hq * (D / 8) * (Nq_pad / 4);
-    bwd_post_kernel<D><<<unsigned((threads + 255) / 256), 256, 0, stream>>>(
+    const long long blocks = 1LL * pb.B * pb.Hq * (Nq_pad / 64);
+    bwd_post_kernel<D><<<unsigned(blocks), 256, 0, stream>>>(
         dq_acc, static_cast<__nv_bfloat16*>(dq), pb.B * pb.Hq, pb.Hq, pb.Nq, Nq_pad, pb.scale);
   }
   return cudaGetLastError();
