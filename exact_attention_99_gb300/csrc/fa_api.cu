@@ -402,9 +402,10 @@ extern "C" int fa_step_host(const void* q, const void* k, const void* v, const v
     cudaGetLastError();
     return FA_ERR_ALLOC;
   }
-  // events: [0] start; per element b, kCopyLanes "inputs in" and one
-  // "results ready"; then one "done" per copy stream
-  const size_t per_b = kCopyLanes + 1;
+  // events: [0] start; per element b, per copy lane "q, k, v in" and "dout
+  // in", then "forward done" and "backward done"; then one "done" per copy
+  // stream
+  const size_t per_b = 2 * kCopyLanes + 2;
   std::vector<cudaEvent_t> ev(1 + per_b * size_t(B) + 2 * kCopyLanes, nullptr);
   bool ok = true;
   for (auto& e : ev) ok = ok && cudaEventCreateWithFlags(&e, cudaEventDisableTiming) == cudaSuccess;
@@ -444,17 +445,25 @@ extern "C" int fa_step_host(const void* q, const void* k, const void* v, const v
     float* wl = reinterpret_cast<float*>(wk + 4 * bk);
     const size_t b_ = size_t(b);
     cudaEvent_t* eb = ev.data() + 1 + per_b * b_;
-    ok = copy(wq, hq + b_ * bq, bq, h2d, 0) && copy(wk, hk + b_ * bk, bk, h2d, 0) && copy(wv, hv + b_ * bk, bk, h2d, 0) &&
-         copy(wdo, hdo + b_ * bq, bq, h2d, 0);
+    // the forward needs q, k, v; dout follows while it runs
+    ok = copy(wq, hq + b_ * bq, bq, h2d, 0) && copy(wk, hk + b_ * bk, bk, h2d, 0) && copy(wv, hv + b_ * bk, bk, h2d, 0);
     for (int l = 0; l < kCopyLanes && ok; ++l)
       ok = cudaEventRecord(eb[l], cs[2 * l]) == cudaSuccess && cudaStreamWaitEvent(s, eb[l], 0) == cudaSuccess;
+    ok = ok && copy(wdo, hdo + b_ * bq, bq, h2d, 0);
+    for (int l = 0; l < kCopyLanes && ok; ++l) ok = cudaEventRecord(eb[kCopyLanes + l], cs[2 * l]) == cudaSuccess;
     if (!ok) break;
     const Problem p{wq, wk, wv, 1, Hq, Hkv, Nq, Nk, d, scale, causal};
-    ok = launch_fwd(p, wo, wl, s) == cudaSuccess && bwd_pooled(p, wo, wl, wdo, wdq, wdk, wdv, stream) == FA_OK &&
-         cudaEventRecord(eb[kCopyLanes], s) == cudaSuccess;
-    for (int l = 0; l < kCopyLanes && ok; ++l) ok = cudaStreamWaitEvent(cs[2 * l + 1], eb[kCopyLanes], 0) == cudaSuccess;
-    ok = ok && copy(ho + b_ * bq, wo, bq, d2h, 1) && copy(hl + b_ * nl * 4, wl, nl * 4, d2h, 1) &&
-         copy(hdq + b_ * bq, wdq, bq, d2h, 1) && copy(hdk + b_ * bk, wdk, bk, d2h, 1) &&
+    ok = launch_fwd(p, wo, wl, s) == cudaSuccess && cudaEventRecord(eb[2 * kCopyLanes], s) == cudaSuccess;
+    // o and lse go out while the backward runs
+    for (int l = 0; l < kCopyLanes && ok; ++l)
+      ok = cudaStreamWaitEvent(cs[2 * l + 1], eb[2 * kCopyLanes], 0) == cudaSuccess;
+    ok = ok && copy(ho + b_ * bq, wo, bq, d2h, 1) && copy(hl + b_ * nl * 4, wl, nl * 4, d2h, 1);
+    for (int l = 0; l < kCopyLanes && ok; ++l) ok = cudaStreamWaitEvent(s, eb[kCopyLanes + l], 0) == cudaSuccess;
+    ok = ok && bwd_pooled(p, wo, wl, wdo, wdq, wdk, wdv, stream) == FA_OK &&
+         cudaEventRecord(eb[2 * kCopyLanes + 1], s) == cudaSuccess;
+    for (int l = 0; l < kCopyLanes && ok; ++l)
+      ok = cudaStreamWaitEvent(cs[2 * l + 1], eb[2 * kCopyLanes + 1], 0) == cudaSuccess;
+    ok = ok && copy(hdq + b_ * bq, wdq, bq, d2h, 1) && copy(hdk + b_ * bk, wdk, bk, d2h, 1) &&
          copy(hdv + b_ * bk, wdv, bk, d2h, 1);
   }
   // the caller's stream waits for every copy stream, then frees the workspace
