@@ -461,9 +461,9 @@ def run_ours(args):
                 "traffic": profiled_traffic(kname, w.name), "avg_launch_ms": round(kms, 4),
                 "flops_per_launch": kflops}
 
-    configs = per_config(fa, flush, peak)
-    configs[WINDOW_CASE["name"]] = window_config(fa, flush, peak)
-    configs.update(fp8_config(fa, flush, peak))
+    per_workload = per_config(fa, flush, peak)
+    per_workload.update({WINDOW_CASE["name"]: window_config(fa, flush, peak)})
+    per_workload.update(fp8_config(fa, flush, peak))
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(total_ms / K, 4), "higher_is_better": True, "scaling": "weak",
@@ -479,7 +479,7 @@ def run_ours(args):
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
         "gpu_launches": 4 * K,
-        "configs": configs,
+        "configs": per_workload,
     }
     if world == 1:
         flops_done, el, heads = oracle_sample(w, x, args.cpu_seconds)
