@@ -197,6 +197,22 @@ def oracle_sample(w, x, seconds: float, max_heads: int | None = None, first: int
     return done * flops_per_head, el, done
 
 
+def oracle_single_thread(seconds: float = 2.0):
+    """The same oracle sample on one host thread (BLAS limited to 1 thread
+    in a fresh interpreter): one (batch, head) slice of the main workload.
+    Returns (TFLOP/s, elapsed s) or None if the child fails."""
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = ("import bench, workloads; w = bench.MAIN; x = workloads.workload_inputs(w, with_dout=True); "
+            f"f, el, n = bench.oracle_sample(w, x, {seconds}, max_heads=1); print(f / el / 1e12, el)")
+    try:
+        out = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True, text=True,
+                             timeout=600)
+        v, el = out.stdout.strip().splitlines()[-1].split()
+        return float(v), float(el)
+    except (subprocess.SubprocessError, ValueError, IndexError):
+        return None
+
+
 def blas_threads() -> int:
     for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
         if os.environ.get(var):
@@ -487,6 +503,11 @@ def run_ours(args):
                                 "kind": "oracle",
                                 "sample": f"{heads} of {w.B * w.Hq} (batch, head) slices of {w.name}, fp64 "
                                           f"forward + backward, {el:.1f} s"}
+        one = oracle_single_thread()
+        if one is not None:
+            line["cpu_baseline"]["single_thread"] = {
+                "value": one[0], "unit": "TFLOP/s", "cores": 1,
+                "sample": f"1 (batch, head) slice of {w.name}, fp64 forward + backward, {one[1]:.1f} s"}
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()
