@@ -81,7 +81,8 @@ struct Params {
   float* lse;
   int B, Hq, Hkv, Nq, Nk;
   int group;
-  float scale_log2;
+  float scale_log2;  // |scale| * log2(e) (2^-100 for a zero scale)
+  uint32_t neg_s;     // 1 for a negative scale: S is computed as (-Q) K^T
   int n_mblocks;
   int n_units;
   // Row-split tail (non-causal): the units [n_full, n_units) of the last,
@@ -551,7 +552,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 13) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idS = idesc_bf16_f32(128, 128, 0, 0);
+      // a negative scale negates A (Q) in S = Q K^T: bit 13 of the instruction descriptor
+      const uint32_t idS = idesc_bf16_f32(128, 128, 0, 0) | (p.neg_s << 13);
       constexpr uint32_t idPV = idesc_bf16_f32(128, D, 0, 1);
       const uint32_t sQa = smem_u32(sQ), sKVa = smem_u32(sKV);
       uint32_t kv_it = 0, ph_q[2] = {0, 0}, ph_p[2] = {0, 0}, ph_o[2] = {0, 0};
@@ -673,7 +675,8 @@ cudaError_t launch_t(const Problem& pb, void* o, float* lse, cudaStream_t stream
   p.Nq = pb.Nq;
   p.Nk = pb.Nk;
   p.group = pb.Hq / pb.Hkv;
-  p.scale_log2 = pb.scale * 1.4426950408889634f;
+  p.scale_log2 = fabsf(exp_scale_log2(pb.scale));
+  p.neg_s = pb.scale < 0.0f ? 1u : 0u;
   p.wl = normalize_window(pb.window_left, pb.Nq, pb.Nk);
   p.wr = pb.causal ? 0 : normalize_window(pb.window_right, pb.Nq, pb.Nk);
   p.n_mblocks = (pb.Nq + 255) / 256;

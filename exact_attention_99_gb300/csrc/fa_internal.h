@@ -56,6 +56,14 @@ bool encode_tiled(CUtensorMap* m, CUtensorMapDataType dtype, int rank, const voi
 // bound that reaches past every key (>= Nq + Nk) is no limit either.
 int normalize_window(int w, int Nq, int Nk);
 
+// The forward's exponent scale, scale * log2(e). A zero scale (every visible
+// key equally weighted) becomes 2^-100: the scaled scores are then 0 to
+// within fp32 rounding while a masked score (-inf) still gives probability 0,
+// which 0 * -inf would not.
+inline float exp_scale_log2(float scale) {
+  return scale == 0.0f ? 7.888609052210118e-31f : scale * 1.4426950408889634f;
+}
+
 // Launchers. Return a cudaError_t (cudaSuccess on success).
 cudaError_t launch_fwd(const Problem& p, void* o, float* lse, cudaStream_t stream);
 // FP8 (e4m3) forward, d = 128 only; incoherent != 0 applies the Hadamard

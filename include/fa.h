@@ -23,9 +23,11 @@
  *   Causal   : causal = 1 hides key j from query i when j > i + (Nk - Nq)
  *              (bottom-right alignment; with Nq == Nk this is j > i). A row
  *              that sees no key gets o = 0 and lse = -inf.
- *   Sizes    : B, Hq, Hkv, Nq, Nk >= 1; d in {64, 128}; scale finite and
- *              > 0; every element count and B*Hq*Nq*d fit in int32 indices
- *              per the limits checked below.
+ *   Sizes    : B, Hq, Hkv, Nq, Nk >= 1; d in {64, 128}; scale any finite
+ *              value (negative: the softmax of the negated scores; zero:
+ *              every visible key weighted equally); every element count
+ *              and B*Hq*Nq*d fit in int32 indices per the limits checked
+ *              below.
  *   Pointers : device pointers owned by the caller, 16-byte aligned. The
  *              library keeps no pointer after a call returns.
  *   Stream   : `stream` is a cudaStream_t (NULL = legacy default stream).

@@ -61,8 +61,8 @@ def bwd(fa, ptrs=(P16,) * 9, **kw):
 @pytest.mark.parametrize("call", [fwd, bwd])
 @pytest.mark.parametrize("bad,code", [
     (dict(d=96), 2), (dict(d=256), 2), (dict(d=0), 1), (dict(Hq=3, Hkv=2), 1), (dict(B=0), 1),
-    (dict(Nq=0), 1), (dict(Nk=-5), 1), (dict(Hkv=0), 1), (dict(causal=2), 1), (dict(scale=0.0), 1),
-    (dict(scale=-1.0), 1), (dict(scale=float("nan")), 1), (dict(scale=float("inf")), 1),
+    (dict(Nq=0), 1), (dict(Nk=-5), 1), (dict(Hkv=0), 1), (dict(causal=2), 1),
+    (dict(scale=float("nan")), 1), (dict(scale=float("inf")), 1), (dict(scale=float("-inf")), 1),
     (dict(Nq=1 << 29), 2),
 ])
 def test_bad_sizes_rejected_on_host(fa, call, bad, code):
@@ -116,6 +116,14 @@ def test_bad_pointers_bwd(fa, which):
         ptrs = [P16] * 9
         ptrs[which] = bad
         assert bwd(fa, ptrs=tuple(ptrs)) == 1
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
+def test_any_finite_scale_passes_the_argument_check(fa):
+    # zero and negative scales are valid: the call gets past the checks to the device look-up
+    for sc in (0.0, -0.0, -1.0, -1e30, 1e-30):
+        assert fwd(fa, scale=sc) == 6
+        assert bwd(fa, scale=sc) == 6
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")

@@ -59,6 +59,33 @@ def test_small_shapes(fa, shape, causal):
     assert_close("dv", to64(dv), rdv)
 
 
+@pytest.mark.parametrize("scale", [-0.088, 0.0])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", [(1, 4, 2, 300, 300, 128), (1, 2, 2, 100, 400, 64)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_any_finite_scale(fa, shape, causal, scale):
+    """scale is any finite number: negative (the row max is taken over
+    scale * s, not s) and zero (every visible key weighted equally)."""
+    B, Hq, Hkv, Nq, Nk, d = shape
+    x = workloads.make_inputs(B, Hq, Hkv, Nq, Nk, d, seed=int(1000 * scale) % 997 + Nq, with_dout=True)
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
+    o, lse = fa.forward(q, k, v, causal=causal, scale=scale)
+    dq, dk, dv = fa.backward(q, k, v, o, lse, do, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    assert fa.fa_get_status() == 0
+    xs = [x[n].double().numpy() for n in ("q", "k", "v", "do")]
+    ro, rlse = attn_ref.forward(*xs[:3], scale, causal)
+    assert_close("o", to64(o), ro)
+    fin = np.isfinite(rlse)
+    glse = to64(lse)
+    assert np.array_equal(np.isfinite(glse), fin)
+    assert float(np.abs(glse[fin] - rlse[fin]).max(initial=0.0)) <= 1e-3
+    rdq, rdk, rdv = attn_ref.backward(*xs, scale, causal)
+    assert_close("dq", to64(dq), rdq)
+    assert_close("dk", to64(dk), rdk)
+    assert_close("dv", to64(dv), rdv)
+
+
 def test_workload_full_size_sampled_heads(fa):
     """Full-size backward workload (the benchmark's launch configuration);
     the oracle recomputes every gradient of a few (batch, head) slices."""

@@ -89,6 +89,15 @@ def test_fp8_matches_oracle(fa, shape, causal, incoherent):
     check_against_oracle(go, glse, x, causal, incoherent, scale)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_negative_scale(fa, causal):
+    """A negative scale: S = (-Q) K^T through the instruction descriptor."""
+    x = workloads.make_inputs(1, 4, 2, 300, 300, 128, seed=321 + causal)
+    scale = -1.0 / math.sqrt(128)
+    go, glse = fp8_case(fa, x, causal, True, scale)
+    check_against_oracle(go, glse, x, causal, True, scale)
+
+
 def test_fp8_full_size_sampled(fa):
     """The non-causal B=4, H=16, N=2048 workload through the FP8 path: finite
     everywhere, two heads against the oracle."""

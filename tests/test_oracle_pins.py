@@ -411,3 +411,35 @@ def test_planted_backward_mistake_is_caught(name, monkeypatch):
     monkeypatch.setattr(attn_ref, "_softmax_grad", BWD_MUTANTS[name](attn_ref._softmax_grad))
     failed = _fails_some(BACKWARD_PINS, attn_ref.backward)
     assert failed, f"mutant {name} passed every backward pin"
+
+
+def test_zero_scale_weights_visible_keys_equally():
+    """scale = 0: O_i is the mean of the visible V rows and LSE_i = ln(count)."""
+    rng = np.random.default_rng(41)
+    q, k, v = (rng.normal(size=(1, n, 2, 16)) for n in (7, 9, 9))
+    for causal in (False, True):
+        o, lse = attn_ref.forward(q, k, v, 0.0, causal)
+        off = 9 - 7
+        for i in range(7):
+            cnt = (i + off + 1) if causal else 9
+            np.testing.assert_allclose(o[0, i], v[0, :cnt].mean(axis=0), atol=1e-12)
+            np.testing.assert_allclose(lse[0, :, i], np.log(cnt), atol=1e-12)
+
+
+def test_negative_scale_is_positive_scale_with_negated_keys():
+    """softmax(-c Q K^T) = softmax(c Q (-K)^T): the row max must be that of
+    the scaled scores, not of the raw ones."""
+    rng = np.random.default_rng(42)
+    q, k, v = (rng.normal(size=(1, 11, 2, 8)) * 3 for _ in range(3))
+    for causal in (False, True):
+        o1, l1 = attn_ref.forward(q, k, v, -0.7, causal)
+        o2, l2 = attn_ref.forward(q, -k, v, 0.7, causal)
+        np.testing.assert_allclose(o1, o2, atol=1e-12)
+        np.testing.assert_allclose(l1, l2, atol=1e-12)
+        # against a scalar loop
+        for i in (0, 5, 10):
+            s = [-0.7 * float(q[0, i, 1] @ k[0, j, 1]) for j in range(11) if not causal or j <= i]
+            m = max(s)
+            w = [math.exp(t - m) for t in s]
+            ref = sum(wj * v[0, j, 1] for j, wj in enumerate(w)) / sum(w)
+            np.testing.assert_allclose(o1[0, i, 1], ref, atol=1e-12)
