@@ -111,6 +111,19 @@ def test_fp8_full_size_sampled(fa):
                              mean_check=False)
 
 
+def test_fp8_causal_full_size_sampled(fa):
+    """The causal B=2, H=16, N=8192 workload through the FP8 path: finite
+    everywhere, two heads against the oracle."""
+    w = workloads.WORKLOADS[2]
+    x = workloads.workload_inputs(w)
+    go, glse = fp8_case(fa, x, True, True, w.scale)
+    assert np.isfinite(go).all() and np.isfinite(glse).all()
+    for b, h in [(0, 3), (1, 12)]:
+        sl = {n: x[n][b:b + 1, :, h:h + 1] for n in ("q", "k", "v")}
+        check_against_oracle(go[b:b + 1, :, h:h + 1], glse[b:b + 1, h:h + 1], sl, True, True, w.scale,
+                             mean_check=False)
+
+
 def test_fp8_incoherent_lowers_error_with_outliers(fa):
     """Against the exact bf16-input attention: with outlier channels in Q
     and K, the incoherent transform lowers the FP8 error."""
