@@ -169,6 +169,32 @@ def test_deterministic_and_offset_invariant(fa, causal):
     assert torch.equal(o1, o3) and torch.equal(l1, l3)
 
 
+def test_memory_linear_in_n(fa):
+    """The score matrix never reaches device memory: a forward + backward at
+    N = 16384 (one head, d = 64) may take the O(N) workspace of the backward
+    (4 * Nq * (d + 2) bytes per head, about 4 MB here) but nothing near the
+    N^2 * 4 bytes = 1 GiB a materialised S would need."""
+    N, d = 16384, 64
+    x = workloads.make_inputs(1, 1, 1, N, N, d, seed=5, with_dout=True)
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
+    o, lse = torch.empty_like(q), torch.empty((1, 1, N), device="cuda", dtype=torch.float32)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    args = (1, 1, 1, N, N, d, d ** -0.5, 1)
+    # once at a small size first: loading the library's device code and its
+    # fixed arrays (the 64 MiB scratch of fa_bwd_noalloc) is not part of a call
+    small = (1, 1, 1, 256, 256, d, d ** -0.5, 1)
+    assert fa.fa_fwd(q, k, v, o, lse, *small) == 0
+    assert fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, *small) == 0
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    assert fa.fa_fwd(q, k, v, o, lse, *args) == 0
+    assert fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, *args) == 0
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert fa.fa_get_status() == 0
+    assert free0 - free1 < 64 << 20, (free0 - free1)
+
+
 def test_bounded_wait_reports_timeout(fa):
     """The producer withholds one tile; the consumer's bounded wait must run
     out, the kernel must exit and report FA_ERR_TIMEOUT, and the context must
