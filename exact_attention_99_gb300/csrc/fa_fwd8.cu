@@ -13,9 +13,9 @@
 //   fp8_rows_kernel<false> : per (batch, head) max |x| of Q M, K M and V.
 //   fp8_rows_kernel<true>  : Q M, K M -> e4m3 rows (a quad of lanes per row;
 //                       the Hadamard transform is a butterfly, five index
-//                       bits inside a lane and two across the quad).
-//   fp8_quant_v_kernel  : V -> e4m3, transposed to [B, Hkv, d, keys] so that
-//                       it is the K-major B operand of P V.
+//                       bits inside a lane and two across the quad), and in
+//                       the same launch V -> e4m3, transposed to [B, Hkv, d,
+//                       keys] so that it is the K-major B operand of P V.
 //   fa_fwd8_kernel    : the attention: the warp roles, unit schedule and
 //                       TMEM layout of the bf16 forward (d = 128), with
 //                       S = Q8 K8^T and O += P8 V8 from shared memory: P of
@@ -300,6 +300,35 @@ __device__ __forceinline__ void unpack_quad_row(const uint4 (&u)[4], float (&x)[
   }
 }
 
+// V rounded to e4m3 and transposed to [B, Hkv, 128 (d), Nk_pad (keys)], one
+// 128-key tile (kt) of one (batch b, kv head) per call by a 256-thread
+// block: lane l of warp w takes keys 4l .. 4l+3 and d = 16w .. 16w+15 (one
+// 32-byte sector of each key row), so that each store of the warp writes 128
+// contiguous bytes of one d row. Keys past Nk are written as zeros.
+__device__ __forceinline__ void quant_v_tile(const __nv_bfloat16* v, int Nk, int Hkv, int Nk_pad, float inv,
+                                             uint8_t* vt8, int kt, int kvh, int b) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint4 u[4][2];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int gk = kt * 128 + 4 * lane + j;
+    const uint4* src = reinterpret_cast<const uint4*>(v + ((size_t(b) * Nk + gk) * Hkv + kvh) * 128 + warp * 16);
+    u[j][0] = gk < Nk ? src[0] : make_uint4(0, 0, 0, 0);
+    u[j][1] = gk < Nk ? src[1] : make_uint4(0, 0, 0, 0);
+  }
+  uint8_t* dst = vt8 + ((size_t(b) * Hkv + kvh) * 128 + warp * 16) * Nk_pad + kt * 128 + 4 * lane;
+#pragma unroll
+  for (int dd = 0; dd < 16; ++dd) {
+    float f[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const __nv_bfloat16* h = reinterpret_cast<const __nv_bfloat16*>(&u[j][dd >> 3]);
+      f[j] = __bfloat162float(h[dd & 7]) * inv;
+    }
+    *reinterpret_cast<uint32_t*>(dst + size_t(dd) * Nk_pad) = pack_e4m3x2(f[0], f[1]) | (pack_e4m3x2(f[2], f[3]) << 16);
+  }
+}
+
 constexpr float kInvSqrt128 = 0.08838834764831845f;
 
 // Row pass over Q, K (and V when !QUANT) of one batch (blockIdx.z), tensor
@@ -315,8 +344,19 @@ template <bool QUANT>
 __global__ void __launch_bounds__(256, 2) fp8_rows_kernel(const __nv_bfloat16* q, const __nv_bfloat16* k,
                                                        const __nv_bfloat16* v, int Nq, int Nk, int Hq, int Hkv,
                                                        int had, unsigned* amax_q, unsigned* amax_k,
-                                                       unsigned* amax_v, uint8_t* q8, uint8_t* k8) {
+                                                       unsigned* amax_v, uint8_t* q8, uint8_t* k8, int Nk_pad,
+                                                       uint8_t* vt8) {
   extern __shared__ float head_sm[];  // QUANT: 1 / (scale sqrt(128)) per head; else max bits per head
+  if (QUANT && blockIdx.y == 2) {
+    // the V transpose runs in the same launch: blockIdx.y = 2 strides over
+    // the (key tile, kv head) tiles of batch blockIdx.z
+    const int b = blockIdx.z, nkt = Nk_pad / 128;
+    for (int t = blockIdx.x; t < nkt * Hkv; t += gridDim.x) {
+      const int kvh = t / nkt, kt = t - kvh * nkt;
+      quant_v_tile(v, Nk, Hkv, Nk_pad, 1.0f / amax_scale(amax_v[b * Hkv + kvh]), vt8, kt, kvh, b);
+    }
+    return;
+  }
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   const int ql = lane & 3, quad = lane >> 2;
   const int t = blockIdx.y, b = blockIdx.z;
@@ -373,37 +413,6 @@ __global__ void __launch_bounds__(256, 2) fp8_rows_kernel(const __nv_bfloat16* q
       const unsigned bits = reinterpret_cast<const unsigned*>(head_sm)[h];
       if (bits) atomicMax(amax + h, bits);
     }
-  }
-}
-
-// V rounded to e4m3 and transposed to [B, Hkv, 128 (d), Nk_pad (keys)]: one
-// block per (batch, kv head, 128-key tile); lane l of warp w takes keys
-// 4l .. 4l+3 and d = 16w .. 16w+15 (one 32-byte sector of each key row),
-// so that each store of the warp writes 128 contiguous bytes of one d row.
-// Keys past Nk are written as zeros.
-__global__ void __launch_bounds__(256) fp8_quant_v_kernel(const __nv_bfloat16* v, int Nk, int Hkv, int Nk_pad,
-                                                          const unsigned* amax_v, uint8_t* vt8) {
-  const int kt = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const float inv = 1.0f / amax_scale(amax_v[b * Hkv + kvh]);
-  uint4 u[4][2];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int gk = kt * 128 + 4 * lane + j;
-    const uint4* src = reinterpret_cast<const uint4*>(v + ((size_t(b) * Nk + gk) * Hkv + kvh) * 128 + warp * 16);
-    u[j][0] = gk < Nk ? src[0] : make_uint4(0, 0, 0, 0);
-    u[j][1] = gk < Nk ? src[1] : make_uint4(0, 0, 0, 0);
-  }
-  uint8_t* dst = vt8 + ((size_t(b) * Hkv + kvh) * 128 + warp * 16) * Nk_pad + kt * 128 + 4 * lane;
-#pragma unroll
-  for (int dd = 0; dd < 16; ++dd) {
-    float f[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const __nv_bfloat16* h = reinterpret_cast<const __nv_bfloat16*>(&u[j][dd >> 3]);
-      f[j] = __bfloat162float(h[dd & 7]) * inv;
-    }
-    *reinterpret_cast<uint32_t*>(dst + size_t(dd) * Nk_pad) = pack_e4m3x2(f[0], f[1]) | (pack_e4m3x2(f[2], f[3]) << 16);
   }
 }
 
@@ -932,11 +941,9 @@ cudaError_t launch_t(const Problem& pb, void* o, float* lse, int incoherent, cud
     const __nv_bfloat16* k = static_cast<const __nv_bfloat16*>(pb.k);
     const __nv_bfloat16* v = static_cast<const __nv_bfloat16*>(pb.v);
     fp8_rows_kernel<false><<<dim3(bx_a, 3, pb.B), 256, hs, stream>>>(q, k, v, pb.Nq, pb.Nk, pb.Hq, pb.Hkv, incoherent,
-                                                                      amax_q, amax_k, amax_v, q8, k8);
-    fp8_rows_kernel<true><<<dim3(bx_q, 2, pb.B), 256, hs, stream>>>(q, k, v, pb.Nq, pb.Nk, pb.Hq, pb.Hkv, incoherent,
-                                                                     amax_q, amax_k, amax_v, q8, k8);
-    fp8_quant_v_kernel<<<dim3(Nk_pad / 128, pb.Hkv, pb.B), 256, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(pb.v), pb.Nk, pb.Hkv, Nk_pad, amax_v, vt8);
+                                                                      amax_q, amax_k, amax_v, q8, k8, Nk_pad, vt8);
+    fp8_rows_kernel<true><<<dim3(bx_q, 3, pb.B), 256, hs, stream>>>(q, k, v, pb.Nq, pb.Nk, pb.Hq, pb.Hkv, incoherent,
+                                                                     amax_q, amax_k, amax_v, q8, k8, Nk_pad, vt8);
     e = cudaGetLastError();
   }
   if (e == cudaSuccess) {
