@@ -402,11 +402,12 @@ extern "C" int fa_step_host(const void* q, const void* k, const void* v, const v
     cudaGetLastError();
     return FA_ERR_ALLOC;
   }
-  // events: [0] start; per element b, per copy lane "q, k, v in" and "dout
-  // in", then "forward done" and "backward done"; then one "done" per copy
-  // stream
+  // events: [0] start; one set per batch element, reused for every element
+  // (each record is waited on before it is recorded again): per copy lane
+  // "q, k, v in" and "dout in", then "forward done" and "backward done";
+  // then one "done" per copy stream
   const size_t per_b = 2 * kCopyLanes + 2;
-  std::vector<cudaEvent_t> ev(1 + per_b * size_t(B) + 2 * kCopyLanes, nullptr);
+  std::vector<cudaEvent_t> ev(1 + per_b + 2 * kCopyLanes, nullptr);
   bool ok = true;
   for (auto& e : ev) ok = ok && cudaEventCreateWithFlags(&e, cudaEventDisableTiming) == cudaSuccess;
   if (ok) {
@@ -444,7 +445,7 @@ extern "C" int fa_step_host(const void* q, const void* k, const void* v, const v
     uint8_t *wk = w + 4 * bq, *wv = wk + bk, *wdk = wk + 2 * bk, *wdv = wk + 3 * bk;
     float* wl = reinterpret_cast<float*>(wk + 4 * bk);
     const size_t b_ = size_t(b);
-    cudaEvent_t* eb = ev.data() + 1 + per_b * b_;
+    cudaEvent_t* eb = ev.data() + 1;
     // the forward needs q, k, v; dout follows while it runs
     ok = copy(wq, hq + b_ * bq, bq, h2d, 0) && copy(wk, hk + b_ * bk, bk, h2d, 0) && copy(wv, hv + b_ * bk, bk, h2d, 0);
     for (int l = 0; l < kCopyLanes && ok; ++l)
@@ -468,7 +469,7 @@ extern "C" int fa_step_host(const void* q, const void* k, const void* v, const v
   }
   // the caller's stream waits for every copy stream, then frees the workspace
   for (int i = 0; i < 2 * kCopyLanes; ++i) {
-    cudaEvent_t e = ev[1 + per_b * size_t(B) + i];
+    cudaEvent_t e = ev[1 + per_b + i];
     if (e != nullptr && cudaEventRecord(e, cs[i]) == cudaSuccess) cudaStreamWaitEvent(s, e, 0);
   }
   const bool freed = cudaFreeAsync(ws, s) == cudaSuccess;
