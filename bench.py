@@ -249,7 +249,9 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
-def time_one(fn, flush, reps=5, warm=2):
+def time_one(fn, flush, reps=20, warm=3, stats=None):
+    """Median device time (ms) of `reps` calls after `warm` untimed ones, the
+    L2 flushed before each; `stats` (a dict) also receives the minimum."""
     import torch
     for _ in range(warm):
         fn()
@@ -262,6 +264,8 @@ def time_one(fn, flush, reps=5, warm=2):
         e1.record()
         torch.cuda.synchronize()
         ts.append(e0.elapsed_time(e1))
+    if stats is not None:
+        stats["min"] = min(ts)
     return statistics.median(ts)
 
 
@@ -278,15 +282,16 @@ def per_config(fa, flush, peak):
         o = torch.empty_like(q)
         lse = torch.empty((w.B, w.Hq, w.Nq), device="cuda", dtype=torch.float32)
         fwd = lambda: fa.fa_fwd(q, k, v, o, lse, w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.d, w.scale, int(w.causal))
-        ms = time_one(fwd, flush)
-        ent = {"fwd_ms": ms, "fwd_tflops": w.fwd_flops() / ms / 1e9}
+        st = {}
+        ms = time_one(fwd, flush, stats=st)
+        ent = {"fwd_ms": ms, "fwd_min_ms": st["min"], "fwd_tflops": w.fwd_flops() / ms / 1e9}
         ent["fwd_frac_of_peak"] = ent["fwd_tflops"] / peak
         if w.direction == "bwd" or w is MAIN or w.Hkv < w.Hq:
             dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
             bwd = lambda: fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.d, w.scale,
                                     int(w.causal))
-            ms = time_one(bwd, flush)
-            ent.update({"bwd_ms": ms, "bwd_tflops": w.bwd_flops() / ms / 1e9})
+            ms = time_one(bwd, flush, stats=st)
+            ent.update({"bwd_ms": ms, "bwd_min_ms": st["min"], "bwd_tflops": w.bwd_flops() / ms / 1e9})
             ent["bwd_frac_of_peak"] = ent["bwd_tflops"] / peak
         out[w.name] = {kk: (round(vv, 4) if isinstance(vv, float) else vv) for kk, vv in ent.items()}
         del q, k, v, do, o, lse
