@@ -18,7 +18,7 @@ import math
 import os
 
 __all__ = ["FAError", "lib", "fa_fwd", "fa_bwd", "fa_bwd_noalloc", "fa_get_status", "fa_status_string", "fa_debug_set",
-           "fa_debug_exp2", "fa_profile_events", "fa_trace", "forward", "backward", "STATUS"]
+           "fa_debug_exp2", "fa_tune", "TUNE_EXP2_SPLIT", "fa_profile_events", "fa_trace", "forward", "backward", "STATUS"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libfa.so")
@@ -77,6 +77,8 @@ def lib() -> ctypes.CDLL:
         L.fa_trace.restype = i
         L.fa_debug_exp2.argtypes = [vp, vp, i, i, vp]
         L.fa_debug_exp2.restype = i
+        L.fa_tune.argtypes = [i, i]
+        L.fa_tune.restype = i
         _lib = L
     return _lib
 
@@ -188,6 +190,16 @@ TRACE_CTAS, TRACE_STEPS, TRACE_POINTS = 4, 64, 16
 def fa_trace(buf=None) -> int:
     """buf: CUDA int64 tensor of TRACE_CTAS*TRACE_STEPS*TRACE_POINTS words, or None."""
     return lib().fa_trace(_ptr(buf))
+
+
+TUNE_EXP2_SPLIT = 1
+
+
+def fa_tune(knob: int, value: int) -> int:
+    """Process-wide tuning knob (see fa.h fa_tune); TUNE_EXP2_SPLIT: 0 = every
+    forward exponential on the special-function unit, N in {1, 2, 4, 8} = one
+    column pair in every N on the FMA-pipe polynomial."""
+    return lib().fa_tune(int(knob), int(value))
 
 
 def fa_debug_exp2(x, y, n, mode, stream=None) -> int:

@@ -17,7 +17,7 @@ ROOT = os.path.dirname(PKG)
 LIB = os.path.join(PKG, "libfa.so")
 BUILD_DIR = os.path.join(PKG, "_build")
 SOURCES = ["fa_api.cu", "fa_fwd.cu", "fa_fwd8.cu", "fa_bwd.cu"]
-HEADERS = ["fa_internal.h", "sm103_ptx.cuh", "sm103_math.cuh", "exp2_poly.h"]
+HEADERS = ["fa_internal.h", "fa_fwd_pipeline.cuh", "sm103_ptx.cuh", "sm103_math.cuh", "exp2_poly.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -6,9 +6,9 @@
 // rounded to e4m3 (the FlashAttention-3 summary on news.hada.io, sections
 // on FP8 and incoherent processing). Both GEMMs run as tcgen05.mma
 // kind::f8f6f4 with fp32 accumulation; P is rounded to e4m3 for the P V
-// GEMM; the softmax, its conditional rescale and the epilogue are those of
-// the bf16 kernel (fa_fwd.cu), with the per-head scales folded into the
-// logit scale and into O.
+// GEMM; the softmax, its conditional rescale and the epilogue are the
+// shared forward pipeline (fa_fwd_pipeline.cuh), with the per-head scales
+// folded into the logit scale and into O.
 //
 //   fp8_rows_kernel<false> : per (batch, head) max |x| of Q M, K M and V.
 //   fp8_rows_kernel<true>  : Q M, K M -> e4m3 rows (a quad of lanes per row;
@@ -16,199 +16,18 @@
 //                       bits inside a lane and two across the quad), and in
 //                       the same launch V -> e4m3, transposed to [B, Hkv, d,
 //                       keys] so that it is the K-major B operand of P V.
-//   fa_fwd8_kernel    : the attention: the warp roles, unit schedule and
-//                       TMEM layout of the bf16 forward (d = 128), with
-//                       S = Q8 K8^T and O += P8 V8 from shared memory: P of
-//                       each stage is staged as an e4m3 tile [128 rows x 128
-//                       keys] with the 128-byte swizzle.
-#include <cuda_bf16.h>
-#include <cmath>
-
-#include "fa_internal.h"
-#include "sm103_math.cuh"
-#include "sm103_ptx.cuh"
+//   fa_fwd8_kernel    : the attention: the shared pipeline with the E4m3
+//                       policy below (d = 128): S = Q8 K8^T and O += P8 V8
+//                       from shared memory; P of each stage is staged as an
+//                       e4m3 tile [128 rows x 128 keys] with the 128-byte
+//                       swizzle.
+#include "fa_fwd_pipeline.cuh"
 
 namespace fa {
 namespace fwd8 {
 
-constexpr int kThreads = 512;
-constexpr int kMaxSlots = 8;
-
-// Share of exponentials done by the polynomial: one column pair in every
-// kPolyEvery goes to the FMA pipes (0 = all on the special-function unit).
-#ifndef FA_POLY_EVERY
-#define FA_POLY_EVERY 0
-#endif
-constexpr int kPolyEvery = FA_POLY_EVERY;
-
-// Rescale threshold (log2 units). A row's reference max m, to which O and l
-// are scaled, moves to the new row max only when that max exceeds m by more
-// than kTau; otherwise the block is exponentiated against the stale m, so
-// every unnormalised probability stays below 2^kTau. The result is the same
-// for any kTau (O, l and LSE all use the same m); kTau = 0 moves m on every
-// growth.
-#ifndef FA_RESCALE_TAU
-#define FA_RESCALE_TAU 8.0f
-#endif
-constexpr float kTau = FA_RESCALE_TAU;
-
-template <int D>
-struct Cfg {
-  static constexpr int kChunks = 1;           // one 128-byte swizzle atom holds a whole e4m3 row of d = 128
-  static constexpr int kTileBytes = 128 * D;  // one 128-row e4m3 tile of Q, K, V^T or P
-  static constexpr int kSlots = 8;
-  static constexpr int kStgBytes = 16384;  // O staging: 4 warps x [32 rows x 64 cols] bf16
-  static constexpr int kSmemDyn = (2 + kSlots + 2) * kTileBytes + kStgBytes + 1024;
-  static constexpr uint32_t kOCol0 = 256;
-};
-
-struct Params {
-  __nv_bfloat16* o;
-  float* lse;
-  // per (batch, head) max |x| of Q M, K M, V (float bits); the e4m3 scale
-  // of a tensor is amax / 448 (1 for an all-zero head)
-  const unsigned* amax_q;
-  const unsigned* amax_k;
-  const unsigned* amax_v;
-  int B, Hq, Hkv, Nq, Nk;
-  int group;
-  float scale_log2;  // |scale| * log2(e) (2^-100 for a zero scale)
-  uint32_t neg_s;     // 1 for a negative scale: S is computed as (-Q) K^T
-  int n_mblocks;
-  int n_units;
-  // Row-split tail (non-causal): the units [n_full, n_units) of the last,
-  // partly filled round run as two work items each, one per 128-row stage,
-  // on twice as many CTAs; the work items are the n_full whole units
-  // followed by those halves, n_items in all.
-  int n_items, n_full;
-  // Visible keys of query row i (masked kernels): i + off - wl <= j <=
-  // i + off + wr with off = Nk - Nq; a negative bound is no limit. Causal
-  // is wl = -1, wr = 0.
-  int wl, wr;
-  unsigned long long wait_limit_ns;
-  int inject;
-  unsigned* status;
-  unsigned long long* trace;  // optional pipeline trace
-};
-
-// Trace points (fa_trace); a step is the CTA's running key-tile counter
-// across its units:
-//   MMA         0 PV0 issued, 1 PV1 issued, 2 S0(next) issued, 3 S1(next) issued
-//   softmax s   4+3s S ready, 5+3s alpha published, 6+3s P stored
-//   correction  10+2s alpha seen, 11+2s O released for PV
-//   producer    14 K slot free, 15 V slot free
-// and, in the last step slot (kernel events): 0 entry, 1 set-up done,
-// 2 epilogue start (last unit), 6 teardown start, 7 exit.
-constexpr int kEv = kTraceSteps - 1;
-
-struct __align__(8) Ctl {
-  uint64_t q_full[2];
-  uint64_t q_empty;
-  uint64_t kv_full[kMaxSlots];
-  uint64_t kv_empty[kMaxSlots];
-  uint64_t s_full[2];
-  uint64_t p_full[2];
-  uint64_t alpha_full[2];
-  uint64_t o_ready[2];
-  uint64_t o_full[2];
-  uint64_t stats_full[2];
-  uint64_t stats_empty[2];
-  uint64_t drain;
-  float alpha[2][128];
-  float stat_l[2][128];
-  float stat_m[2][128];
-  uint32_t tmem_base;
-  uint32_t abort;
-};
-
-struct Unit {
-  int b, h, kvh, row0;
-  int kb0;    // first key tile of the unit
-  int a[2];   // stage s visits key tiles kb0 + a[s] .. kb0 + a[s] + n[s] - 1
-  int n[2];
-  int nb;     // key tiles the unit loads: max over stages of a[s] + n[s]
-  bool rows[2];
-  __device__ __forceinline__ bool active(int s, int j) const { return j >= a[s] && j < a[s] + n[s]; }
-};
-
-// Window bounds as a kernel sees them: the plain causal kernels (WIN false)
-// fix them at compile time (no left bound, right bound 0).
-template <bool WIN>
-__device__ __forceinline__ int win_l(const Params& p) { return WIN ? p.wl : -1; }
-template <bool WIN>
-__device__ __forceinline__ int win_r(const Params& p) { return WIN ? p.wr : 0; }
-
-template <bool CAUSAL, bool WIN>
-__device__ __forceinline__ Unit decode_unit(const Params& p, int item) {
-  Unit x;
-  int u = item, half = -1;
-  if (!CAUSAL && item >= p.n_full) {
-    const int k = item - p.n_full;
-    u = p.n_full + (k >> 1);
-    half = k & 1;
-  }
-  const int bh_count = p.B * p.Hq;
-  // causal: rounds over all heads, longest units (last query blocks) first;
-  // non-causal: all query blocks of one head in a row, so the CTAs that run
-  // together share K and V through L2
-  int r, bh;
-  if (CAUSAL) {
-    r = u / bh_count;
-    bh = u - r * bh_count;
-  } else {
-    bh = u / p.n_mblocks;
-    r = u - bh * p.n_mblocks;
-  }
-  const int mb = CAUSAL ? (p.n_mblocks - 1 - r) : r;
-  x.b = bh / p.Hq;
-  x.h = bh - x.b * p.Hq;
-  x.kvh = x.h / p.group;
-  x.row0 = mb * 256;
-  const int off = p.Nk - p.Nq;
-  const int nkb = (p.Nk + 127) >> 7;
-  int t0[2];
-#pragma unroll
-  for (int s = 0; s < 2; ++s) {
-    const int r0 = x.row0 + s * 128;
-    x.rows[s] = r0 < p.Nq;
-    t0[s] = 0;
-    if (!x.rows[s]) {
-      x.n[s] = 0;
-    } else if (!CAUSAL) {
-      x.n[s] = nkb;
-    } else {
-      // keys seen by any row of the stage: [lo, hi]
-      const int rl = min(r0 + 127, p.Nq - 1);
-      const int wl = win_l<WIN>(p), wr = win_r<WIN>(p);
-      const int lo = wl >= 0 ? max(0, r0 + off - wl) : 0;
-      const int hi = wr >= 0 ? min(p.Nk - 1, rl + off + wr) : p.Nk - 1;
-      if (hi < lo) {
-        x.n[s] = 0;
-      } else {
-        t0[s] = lo >> 7;
-        x.n[s] = (hi >> 7) - t0[s] + 1;
-      }
-    }
-  }
-  if (half >= 0) {  // one stage of a row-split unit; the other item has the other rows
-    x.n[half ^ 1] = 0;
-    x.rows[half ^ 1] = false;
-  }
-  // stage 1's rows follow stage 0's, so its key range starts and ends no
-  // earlier, and (both bounds being >= 0 or absent) leaves no gap after it
-  x.kb0 = x.n[0] > 0 ? t0[0] : t0[1];
-#pragma unroll
-  for (int s = 0; s < 2; ++s) x.a[s] = x.n[s] > 0 ? t0[s] - x.kb0 : 0;
-  x.nb = max(x.a[0] + x.n[0], x.a[1] + x.n[1]);
-  return x;
-}
-
-// Static snake order over rounds of gridDim.x units (longest first when
-// causal): CTA c takes unit c in even rounds and G-1-c in odd rounds.
-__device__ __forceinline__ int unit_at(int round, int c) {
-  const int G = gridDim.x;
-  return round * G + ((round & 1) ? (G - 1 - c) : c);
-}
+using fwdp::Params;
+using fwdp::Unit;
 
 // e4m3 scale of a tensor from its per-head max |x| (float bits)
 __device__ __forceinline__ float amax_scale(unsigned bits) {
@@ -416,452 +235,92 @@ __global__ void __launch_bounds__(256, 2) fp8_rows_kernel(const __nv_bfloat16* q
   }
 }
 
-template <int D, bool CAUSAL, bool WIN>
-__global__ void __launch_bounds__(kThreads, 1)
+
+// The e4m3 operand policy of the shared forward pipeline (d = 128). A
+// 128-row e4m3 tile of d = 128 is one 128-byte swizzle atom deep, so Q, K
+// and V^T tiles are 16 KB and the K/V ring holds 8 slots. P cannot stay in
+// TMEM (the TMEM operand of the .ts form is the A operand of 16-bit kinds
+// only in the layout used here), so the softmax warps write P as e4m3 into
+// a swizzled 16 KB shared tile per stage and the P V GEMM reads both
+// operands from shared memory.
+struct E4m3 {
+  static constexpr int D = 128;
+  static constexpr int kTileBytes = 128 * D;   // one 128-row e4m3 tile of Q, K or V^T
+  static constexpr int kSlots = 8;
+  static constexpr int kPTileBytes = 128 * 128;  // e4m3 P of one stage [rows x keys]
+  static constexpr int kSmemDyn = (2 + kSlots) * kTileBytes + 2 * kPTileBytes + fwdp::kStgBytes + 1024;
+
+  __device__ __forceinline__ static void load_q(uint8_t* dst, const CUtensorMap* m, uint64_t* bar, int h, int row,
+                                                int b) {
+    tma_load_4d(dst, m, bar, 0, h, row, b);
+  }
+  // K tile [128 keys x d]
+  __device__ __forceinline__ static void load_k(uint8_t* dst, const CUtensorMap* m, uint64_t* bar, int kvh, int key0,
+                                                int b) {
+    tma_load_4d(dst, m, bar, 0, kvh, key0, b);
+  }
+  // V^T tile [d x 128 keys]
+  __device__ __forceinline__ static void load_v(uint8_t* dst, const CUtensorMap* m, uint64_t* bar, int kvh, int key0,
+                                                int b) {
+    tma_load_4d(dst, m, bar, key0, 0, kvh, b);
+  }
+
+  struct Desc {
+    uint32_t q, k, p;  // descriptor low words of tile 0: Q, K (and V^T), P; all K-major
+  };
+  __device__ __forceinline__ static Desc make_desc(uint32_t sQa, uint32_t sKVa, uint32_t sPa) {
+    return Desc{sdesc_lo(sQa, 16), sdesc_lo(sKVa, 16), sdesc_lo(sPa, 16)};
+  }
+  __host__ __device__ static constexpr uint32_t idesc_s() { return idesc_e4m3_f32(128, 128); }
+  __host__ __device__ static constexpr uint32_t idesc_pv() { return idesc_e4m3_f32(128, D); }
+  // S[stage s] = Q8_s K8^T: 32 e4m3 values (32 bytes) of d per MMA
+  __device__ __forceinline__ static void issue_s(const Desc& dc, uint32_t d, int s, uint32_t kslot, uint32_t idS) {
+    const uint32_t a0 = sdesc_step(dc.q, s * kTileBytes);
+    const uint32_t b0 = sdesc_step(dc.k, kslot * kTileBytes);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) mma_f8_lo(d, sdesc_step(a0, kk * 32), sdesc_step(b0, kk * 32), idS, kk > 0);
+  }
+  // O[stage s] (+)= P8_s V8: 32 keys per MMA, both operands in shared memory
+  __device__ __forceinline__ static void issue_pv(const Desc& dc, uint32_t d, uint32_t, int s, uint32_t vslot,
+                                                  bool acc, uint32_t idPV) {
+    const uint32_t a0 = sdesc_step(dc.p, s * kPTileBytes);
+    const uint32_t b0 = sdesc_step(dc.k, vslot * kTileBytes);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+      mma_f8_lo(d, sdesc_step(a0, kk * 32), sdesc_step(b0, kk * 32), idPV, (acc || kk > 0) ? 1u : 0u);
+  }
+
+  struct PK {
+    uint32_t w[32];  // e4m3 P of one row, four keys per word
+    uint32_t half_lo;
+  };
+  __device__ __forceinline__ static void pack_p(PK& pk, int c, float a, float b) {
+    const uint32_t h2 = pack_e4m3x2(a, b);
+    if (c & 1) pk.w[c >> 1] = pk.half_lo | (h2 << 16);
+    else pk.half_lo = h2;
+  }
+  // row r of the stage's P tile: 8 chunks of 16 keys, 128-byte swizzle
+  __device__ __forceinline__ static void store_p(const PK& pk, uint32_t, uint8_t* sP_s, int row) {
+    uint8_t* prow = sP_s + (row >> 3) * 1024 + (row & 7) * 128;
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch)
+      *reinterpret_cast<uint4*>(prow + ((ch ^ (row & 7)) << 4)) =
+          make_uint4(pk.w[4 * ch], pk.w[4 * ch + 1], pk.w[4 * ch + 2], pk.w[4 * ch + 3]);
+  }
+  __device__ __forceinline__ static void publish_p() { fence_proxy_async_smem(); }  // read by the async proxy
+  __device__ __forceinline__ static float logit_scale(const Params& p, const Unit& un) {
+    return p.scale_log2 * amax_scale(p.amax_q[un.b * p.Hq + un.h]) * amax_scale(p.amax_k[un.b * p.Hkv + un.kvh]);
+  }
+  __device__ __forceinline__ static float out_scale(const Params& p, const Unit& un) {
+    return amax_scale(p.amax_v[un.b * p.Hkv + un.kvh]);
+  }
+};
+
+template <bool CAUSAL, int POLY>
+__global__ void __launch_bounds__(fwdp::kThreads, 1)
     fa_fwd8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
-                  const Params p) {
-  using C = Cfg<D>;
-  extern __shared__ uint8_t smem_raw[];
-  __shared__ Ctl ctl;
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = smem;                               // 2 tiles
-  uint8_t* sKV = smem + 2 * C::kTileBytes;          // kSlots tiles: K [keys x d] and V^T [d x keys]
-  uint8_t* sP = sKV + C::kSlots * C::kTileBytes;    // 2 tiles: e4m3 P of each stage [rows x keys]
-  uint8_t* sStg = sP + 2 * C::kTileBytes;           // O staging
-
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const int wg = warp >> 2;
-  volatile uint32_t* abort_flag = &ctl.abort;
-  const uint64_t LIM = p.wait_limit_ns;
-  if (threadIdx.x == 0) trace_stamp(p.trace, kEv, 0);
-
-  if (threadIdx.x == 0) {
-    ctl.abort = 0;
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&ctl.q_full[s], 1);
-      mbar_init(&ctl.s_full[s], 1);
-      mbar_init(&ctl.p_full[s], 4);
-      mbar_init(&ctl.alpha_full[s], 4);
-      mbar_init(&ctl.o_ready[s], 4);
-      mbar_init(&ctl.o_full[s], 1);
-      mbar_init(&ctl.stats_full[s], 4);
-      mbar_init(&ctl.stats_empty[s], 4);
-    }
-    mbar_init(&ctl.q_empty, 1);
-    mbar_init(&ctl.drain, 1);
-    for (int i = 0; i < C::kSlots; ++i) {
-      mbar_init(&ctl.kv_full[i], 1);
-      mbar_init(&ctl.kv_empty[i], 1);
-    }
-    fence_mbar_init();
-  }
-  if (warp == 13) {
-    tmem_alloc(&ctl.tmem_base, 512);
-    tmem_relinquish();
-  }
-  if (warp == 12 && lane == 0) {
-    prefetch_tmap(&tmQ);
-    prefetch_tmap(&tmK);
-    prefetch_tmap(&tmV);
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = ctl.tmem_base;
-  if (threadIdx.x == 0) trace_stamp(p.trace, kEv, 1);
-
-  if (wg <= 1) {
-    // ------------------------------------------------------------ softmax
-    setmaxnreg_inc<176>();
-    const int s = wg;
-    const int row = ((warp & 3) << 5) + lane;
-    const uint32_t t_s = tmem + (uint32_t(warp & 3) << 21) + uint32_t(s * 128);  // lane quarter + S columns
-    uint32_t ph_s = 0, ph_se = 0;
-    int blk = 0;  // running key-tile counter (trace only)
-    float sl = p.scale_log2;
-    bool ok = true;
-    for (int rnd = 0; ok; ++rnd) {
-      const int u = unit_at(rnd, blockIdx.x);
-      if (u >= p.n_items) break;
-      const Unit un = decode_unit<CAUSAL, WIN>(p, u);
-      const int n = un.n[s];
-      const int blk0 = blk;
-      blk += un.nb;
-      if (n == 0) continue;
-      const int rg = un.row0 + s * 128 + row;  // global query row
-      sl = p.scale_log2 * amax_scale(p.amax_q[un.b * p.Hq + un.h]) * amax_scale(p.amax_k[un.b * p.Hkv + un.kvh]);
-      const int off = p.Nk - p.Nq;
-      const int r0 = un.row0 + s * 128, rl = min(r0 + 127, p.Nq - 1);  // the stage's rows
-      const int wl = win_l<WIN>(p), wr = win_r<WIN>(p);
-      float m_run = -INFINITY, l_run = 0.0f;
-      for (int j = 0; j < n; ++j) {
-        if (!mbar_wait_bounded(&ctl.s_full[s], ph_s, abort_flag, LIM)) { ok = false; break; }
-        ph_s ^= 1;
-        if (row == 0) trace_stamp(p.trace, blk0 + j, 4 + 3 * s);
-        tc_fence_after();
-        uint32_t x[128];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(t_s + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&x[c * 32]));
-        tmem_wait_ld();
-        const int kb = (un.kb0 + un.a[s] + j) * 128;
-        // a tile needs masking when it reaches past the keys or crosses a
-        // window edge of some row of the stage
-        const bool need_mask = (kb + 127 >= p.Nk) ||
-                               (CAUSAL && ((wr >= 0 && kb + 127 > r0 + off + wr) || (wl >= 0 && kb < rl + off - wl)));
-        if (need_mask) {
-          int lim = p.Nk - kb;  // columns [lo_c, lim) of this row are visible
-          int lo_c = 0;
-          if (CAUSAL && wr >= 0) lim = min(lim, rg + off + wr + 1 - kb);
-          if (CAUSAL && wl >= 0) lo_c = rg + off - wl - kb;
-#pragma unroll
-          for (int c = 0; c < 128; ++c)
-            if (c >= lim || c < lo_c) x[c] = f2u(-INFINITY);
-        }
-        float mA = -INFINITY, mB = -INFINITY, mC = -INFINITY, mD = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < 128; c += 8) {
-          mA = fmax3(mA, u2f(x[c]), u2f(x[c + 1]));
-          mB = fmax3(mB, u2f(x[c + 2]), u2f(x[c + 3]));
-          mC = fmax3(mC, u2f(x[c + 4]), u2f(x[c + 5]));
-          mD = fmax3(mD, u2f(x[c + 6]), u2f(x[c + 7]));
-        }
-        const float mx = fmaxf(fmaxf(mA, mB), fmaxf(mC, mD));
-        const float m_cand = fmaxf(m_run, mx * sl);
-        const float m_new = (m_cand > m_run + kTau) ? m_cand : m_run;
-        const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
-        const float alpha = ex2_mufu(m_run - m_use);
-        ctl.alpha[s][row] = alpha;
-        __syncwarp();
-        if (row == 0) trace_stamp(p.trace, blk0 + j, 5 + 3 * s);
-        if (lane == 0) mbar_arrive(&ctl.alpha_full[s]);
-
-        const uint64_t sl2 = pack2(sl, sl);
-        const uint64_t nm2 = pack2(-m_use, -m_use);
-        uint64_t acc0 = 0, acc1 = 0, acc2 = 0, acc3 = 0;
-        uint32_t pk[32];  // e4m3 P, four keys per word
-        uint32_t half_lo = 0;
-#pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          uint64_t y = ffma2(pack2(u2f(x[2 * c]), u2f(x[2 * c + 1])), sl2, nm2);
-          float a, b;
-          unpack2(y, a, b);
-          if (kPolyEvery > 0 && (c % (kPolyEvery > 0 ? kPolyEvery : 1)) == (kPolyEvery - 1)) {
-            exp2_poly_pair(a, b);
-          } else {
-            a = ex2_mufu(a);
-            b = ex2_mufu(b);
-          }
-          const uint64_t pr = pack2(a, b);
-          if ((c & 3) == 0) acc0 = c == 0 ? pr : fadd2(acc0, pr);
-          if ((c & 3) == 1) acc1 = c == 1 ? pr : fadd2(acc1, pr);
-          if ((c & 3) == 2) acc2 = c == 2 ? pr : fadd2(acc2, pr);
-          if ((c & 3) == 3) acc3 = c == 3 ? pr : fadd2(acc3, pr);
-          const uint32_t h2 = pack_e4m3x2(a, b);
-          if (c & 1) pk[c >> 1] = half_lo | (h2 << 16);
-          else half_lo = h2;
-        }
-        {
-          // row r of the stage's P tile: 8 chunks of 16 keys, 128-byte swizzle
-          uint8_t* prow = sP + s * C::kTileBytes + (row >> 3) * 1024 + (row & 7) * 128;
-#pragma unroll
-          for (int ch = 0; ch < 8; ++ch)
-            *reinterpret_cast<uint4*>(prow + ((ch ^ (row & 7)) << 4)) =
-                make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-        }
-        const uint64_t acc = fadd2(fadd2(acc0, acc1), fadd2(acc2, acc3));
-        float la, lb;
-        unpack2(acc, la, lb);
-        l_run = fmaf(l_run, alpha, la + lb);
-        m_run = m_new;
-        fence_proxy_async_smem();  // P is read by the tensor core (async proxy)
-        __syncwarp();
-        if (row == 0) trace_stamp(p.trace, blk0 + j, 6 + 3 * s);
-        if (lane == 0) mbar_arrive(&ctl.p_full[s]);
-      }
-      if (!ok) break;
-      // final row statistics for the epilogue
-      if (!mbar_wait_bounded(&ctl.stats_empty[s], ph_se ^ 1, abort_flag, LIM)) { ok = false; break; }
-      ph_se ^= 1;
-      ctl.stat_l[s][row] = l_run;
-      ctl.stat_m[s][row] = m_run;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl.stats_full[s]);
-    }
-  } else if (wg == 2) {
-    // ------------------------------------------------ correction + epilogue
-    setmaxnreg_dec<80>();
-    const int wq = warp & 3;
-    const int row = (wq << 5) + lane;
-    const uint32_t t_lane = tmem + (uint32_t(wq) << 21);
-    uint32_t ph_a[2] = {0, 0}, ph_st[2] = {0, 0}, ph_of[2] = {0, 0};
-    int blk = 0;
-    bool ok = true;
-    for (int rnd = 0; ok; ++rnd) {
-      const int u = unit_at(rnd, blockIdx.x);
-      if (u >= p.n_items) break;
-      const Unit un = decode_unit<CAUSAL, WIN>(p, u);
-      const int blk0 = blk;
-      blk += un.nb;
-      for (int j = 0; j < un.nb && ok; ++j) {
-#pragma unroll
-        for (int s = 0; s < 2; ++s) {
-          if (!un.active(s, j)) continue;
-          if (!mbar_wait_bounded(&ctl.alpha_full[s], ph_a[s], abort_flag, LIM)) { ok = false; break; }
-          ph_a[s] ^= 1;
-          if (row == 0) trace_stamp(p.trace, blk0 + j, 10 + 2 * s);
-          const float a = ctl.alpha[s][row];
-          if (j > un.a[s] && __any_sync(0xffffffffu, a < 1.0f)) {
-            tc_fence_after();
-            const uint32_t t_o = t_lane + C::kOCol0 + uint32_t(s * D);
-            const uint64_t a2 = pack2(a, a);
-#pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-              uint32_t v[32];
-              tmem_ld32(t_o + c * 32, v);
-              tmem_wait_ld();
-#pragma unroll
-              for (int i = 0; i < 32; i += 2) {
-                float lo, hi;
-                unpack2(fmul2(pack2(u2f(v[i]), u2f(v[i + 1])), a2), lo, hi);
-                v[i] = f2u(lo);
-                v[i + 1] = f2u(hi);
-              }
-              tmem_st32(t_o + c * 32, v);
-            }
-            tmem_wait_st();
-          }
-          tc_fence_before();
-          __syncwarp();
-          if (row == 0) trace_stamp(p.trace, blk0 + j, 11 + 2 * s);
-          if (lane == 0) mbar_arrive(&ctl.o_ready[s]);
-        }
-      }
-      if (!ok) break;
-      // epilogue: O / l -> bf16, LSE
-      if (row == 0) trace_stamp(p.trace, kEv, 2);
-#pragma unroll 1
-      for (int s = 0; s < 2; ++s) {
-        if (!un.rows[s]) continue;
-        const int rg = un.row0 + s * 128 + row;
-        const bool valid = rg < p.Nq;
-        __nv_bfloat16* dst = p.o + ((size_t(un.b) * p.Nq + rg) * p.Hq + un.h) * D;
-        float* lse_dst = p.lse + (size_t(un.b) * p.Hq + un.h) * p.Nq + rg;
-        if (un.n[s] == 0) {
-          if (valid) {
-            const uint4 z = make_uint4(0, 0, 0, 0);
-            for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4*>(dst)[c] = z;
-            *lse_dst = -INFINITY;
-          }
-          continue;
-        }
-        if (!mbar_wait_bounded(&ctl.stats_full[s], ph_st[s], abort_flag, LIM)) { ok = false; break; }
-        ph_st[s] ^= 1;
-        const float l = ctl.stat_l[s][row];
-        const float m = ctl.stat_m[s][row];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl.stats_empty[s]);
-        if (!mbar_wait_bounded(&ctl.o_full[s], ph_of[s], abort_flag, LIM)) { ok = false; break; }
-        ph_of[s] ^= 1;
-        tc_fence_after();
-        const float inv = l > 0.0f ? amax_scale(p.amax_v[un.b * p.Hkv + un.kvh]) / l : 0.0f;
-        const uint32_t t_o = t_lane + C::kOCol0 + uint32_t(s * D);
-        // each warp stages its 32 rows x 64 columns (bf16, 128-byte swizzle)
-        // and writes them with one TMA store; rows past Nq are clipped
-        uint8_t* stg = sStg + wq * 4096;
-        const int wrow0 = un.row0 + s * 128 + wq * 32;
-#pragma unroll 1
-        for (int hf = 0; hf < D / 64; ++hf) {
-          if (lane == 0) bulk_wait_read_all();  // the previous store has read the buffer
-          __syncwarp();
-#pragma unroll 1
-          for (int c2 = 0; c2 < 2; ++c2) {
-            uint32_t v[32];
-            tmem_ld32(t_o + hf * 64 + c2 * 32, v);
-            tmem_wait_ld();
-            uint32_t pk[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(u2f(v[2 * i]) * inv, u2f(v[2 * i + 1]) * inv);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              *reinterpret_cast<uint4*>(stg + lane * 128 + (((c2 * 4 + i) ^ (lane & 7)) << 4)) =
-                  make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0 && wrow0 < p.Nq) {
-            tma_store_4d(&tmO, stg, hf * 64, un.h, wrow0, un.b);
-            bulk_commit();
-          }
-        }
-        if (valid) *lse_dst = l > 0.0f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
-        tc_fence_before();
-      }
-    }
-    if (lane == 0) bulk_wait_all();  // stores complete (and staging reads done) before the CTA exits
-  } else {
-    setmaxnreg_dec<80>();
-  }
-  if (warp == 12) {
-    // ------------------------------------------------------- TMA producer
-    if (lane == 0) {
-      uint32_t kv_it = 0, ph_qe = 0;
-      int blk = 0;
-      bool first = true, ok = true;
-      bool injected = false;
-      for (int rnd = 0; ok; ++rnd) {
-        const int u = unit_at(rnd, blockIdx.x);
-        if (u >= p.n_items) break;
-        const Unit un = decode_unit<CAUSAL, WIN>(p, u);
-        if (un.nb == 0) continue;
-        if (!first) {
-          if (!mbar_wait_bounded(&ctl.q_empty, ph_qe, abort_flag, LIM)) { ok = false; break; }
-          ph_qe ^= 1;
-        }
-        first = false;
-        for (int s = 0; s < 2; ++s) {
-          if (un.n[s] == 0) continue;
-          mbar_arrive_expect_tx(&ctl.q_full[s], C::kTileBytes);
-#pragma unroll
-          for (int c = 0; c < C::kChunks; ++c)
-            tma_load_4d(sQ + s * C::kTileBytes, &tmQ, &ctl.q_full[s], 0, un.h, un.row0 + s * 128, un.b);
-        }
-        for (int j = 0; j < un.nb && ok; ++j) {
-#pragma unroll 1
-          for (int t = 0; t < 2; ++t) {
-            const uint32_t slot = kv_it % C::kSlots;
-            const uint32_t ph = ((kv_it / C::kSlots) & 1) ^ 1;
-            if (!mbar_wait_bounded(&ctl.kv_empty[slot], ph, abort_flag, LIM)) { ok = false; break; }
-            trace_stamp(p.trace, blk + j, 14 + t);
-            ++kv_it;
-            if (p.inject == 1 && !injected) {  // test hook: never deliver this tile
-              injected = true;
-              continue;
-            }
-            mbar_arrive_expect_tx(&ctl.kv_full[slot], C::kTileBytes);
-            if (t == 0)  // K tile [128 keys x d]
-              tma_load_4d(sKV + slot * C::kTileBytes, &tmK, &ctl.kv_full[slot], 0, un.kvh, (un.kb0 + j) * 128, un.b);
-            else  // V^T tile [d x 128 keys]
-              tma_load_4d(sKV + slot * C::kTileBytes, &tmV, &ctl.kv_full[slot], (un.kb0 + j) * 128, 0, un.kvh, un.b);
-          }
-        }
-        blk += un.nb;
-      }
-      if (*abort_flag) {
-        // let copies already in flight land before shared memory is released
-        const uint64_t t0 = globaltimer_ns();
-        while (globaltimer_ns() - t0 < 1000000ull) __nanosleep(1000);
-      }
-    }
-  } else if (warp == 13) {
-    // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      // a negative scale negates A (Q) in S = Q K^T: bit 13 of the instruction descriptor
-      const uint32_t idS = idesc_e4m3_f32(128, 128) | (p.neg_s << 13);
-      constexpr uint32_t idPV = idesc_e4m3_f32(128, D);
-      const uint32_t sQa = smem_u32(sQ), sKVa = smem_u32(sKV), sPa = smem_u32(sP);
-      uint32_t kv_it = 0, ph_q[2] = {0, 0}, ph_p[2] = {0, 0}, ph_o[2] = {0, 0};
-      int blk = 0;
-      bool ok = true;
-      // Tile descriptors are built once; a K step is one add of a constant,
-      // so MMAs issue back to back (the tensor core idles otherwise).
-      const uint32_t dQ = sdesc_lo(sQa, 16);   // Q tiles, K-major (K = d)
-      const uint32_t dK = sdesc_lo(sKVa, 16);  // K and V^T tiles, K-major (K = d, keys)
-      const uint32_t dP = sdesc_lo(sPa, 16);   // P tiles, K-major (K = keys)
-      auto issue_S = [&](int s, uint32_t kslot) {
-        const uint32_t a0 = sdesc_step(dQ, s * C::kTileBytes);
-        const uint32_t b0 = sdesc_step(dK, kslot * C::kTileBytes);
-        const uint32_t d = tmem + uint32_t(s * 128);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)  // 32 e4m3 values (32 bytes) of d per MMA
-          mma_f8_lo(d, sdesc_step(a0, kk * 32), sdesc_step(b0, kk * 32), idS, kk > 0);
-      };
-      auto issue_PV = [&](int s, uint32_t vslot, bool acc) {
-        const uint32_t a0 = sdesc_step(dP, s * C::kTileBytes);
-        const uint32_t b0 = sdesc_step(dK, vslot * C::kTileBytes);
-        const uint32_t d = tmem + C::kOCol0 + uint32_t(s * D);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)  // 32 keys per MMA
-          mma_f8_lo(d, sdesc_step(a0, kk * 32), sdesc_step(b0, kk * 32), idPV, (acc || kk > 0) ? 1u : 0u);
-      };
-      auto wait_kv = [&](uint32_t& slot) -> bool {
-        slot = kv_it % C::kSlots;
-        const bool r = mbar_wait_bounded(&ctl.kv_full[slot], (kv_it / C::kSlots) & 1, abort_flag, LIM);
-        ++kv_it;
-        return r;
-      };
-      for (int rnd = 0; ok; ++rnd) {
-        const int u = unit_at(rnd, blockIdx.x);
-        if (u >= p.n_items) break;
-        const Unit un = decode_unit<CAUSAL, WIN>(p, u);
-        if (un.nb == 0) continue;
-        for (int s = 0; s < 2 && ok; ++s) {
-          if (un.n[s] == 0) continue;
-          ok = mbar_wait_bounded(&ctl.q_full[s], ph_q[s], abort_flag, LIM);
-          ph_q[s] ^= 1;
-        }
-        uint32_t kslot = 0, vslot = 0;
-        if (!ok || !wait_kv(kslot)) { ok = false; break; }
-        tc_fence_after();
-        for (int s = 0; s < 2; ++s) {
-          if (!un.active(s, 0)) continue;
-          issue_S(s, kslot);
-          mma_commit(&ctl.s_full[s]);
-        }
-        mma_commit(&ctl.kv_empty[kslot]);
-        if (un.nb == 1) mma_commit(&ctl.q_empty);
-        for (int j = 0; j < un.nb && ok; ++j) {
-          if (!wait_kv(vslot)) { ok = false; break; }
-          const bool nxt = j + 1 < un.nb;
-          if (nxt && !wait_kv(kslot)) { ok = false; break; }
-          const int last_v = un.active(1, j) ? 1 : 0;  // the last stage that reads V_j
-          for (int s = 0; s < 2; ++s) {
-            if (un.active(s, j)) {
-              if (!mbar_wait_bounded(&ctl.p_full[s], ph_p[s], abort_flag, LIM)) { ok = false; break; }
-              ph_p[s] ^= 1;
-              if (!mbar_wait_bounded(&ctl.o_ready[s], ph_o[s], abort_flag, LIM)) { ok = false; break; }
-              ph_o[s] ^= 1;
-              tc_fence_after();
-              trace_stamp(p.trace, blk + j, s);
-              issue_PV(s, vslot, j > un.a[s]);
-              if (j == un.a[s] + un.n[s] - 1) mma_commit(&ctl.o_full[s]);
-              // V_j is free once the last PV reading it completes: release it
-              // before the next S is issued so the refill starts earlier
-              if (s == last_v) mma_commit(&ctl.kv_empty[vslot]);
-            }
-            if (nxt && un.active(s, j + 1)) {  // S of the next tile (a stage's first S when it starts there)
-              tc_fence_after();
-              trace_stamp(p.trace, blk + j, 2 + s);
-              issue_S(s, kslot);
-              mma_commit(&ctl.s_full[s]);
-            }
-          }
-          if (!ok) break;
-          if (nxt) mma_commit(&ctl.kv_empty[kslot]);
-          if (j + 2 == un.nb) mma_commit(&ctl.q_empty);
-        }
-        blk += un.nb;
-      }
-      if (*abort_flag) {
-        // drain the tensor pipe before TMEM is released
-        mma_commit(&ctl.drain);
-        const uint64_t t0 = globaltimer_ns();
-        while (!mbar_try_wait(smem_u32(&ctl.drain), 0) && globaltimer_ns() - t0 < 100000000ull) {
-        }
-      }
-    }
-  }
-
-  // ------------------------------------------------------------- teardown
-  if (warp == 8 && lane == 0) trace_stamp(p.trace, kEv, 6);
-  __syncwarp();
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (warp == 13) tmem_dealloc(tmem, 512);
-  if (threadIdx.x == 0 && ctl.abort) atomicOr(p.status, kDevTimeout);
-  if (threadIdx.x == 0) trace_stamp(p.trace, kEv, 7);
+                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO, const Params p) {
+  fwdp::fwd_body<E4m3, CAUSAL, false, POLY>(tmQ, tmK, tmV, tmO, p);
 }
 
 // 4-D e4m3 tensor map with a 128-byte swizzle: dims and box innermost first
@@ -873,10 +332,25 @@ bool make_u8_map(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uin
   return encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+using KernelFn = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, const Params);
+
+// the exp2 split (one column pair in every `poly` on the FMA polynomial; 0 =
+// every exponential on the special-function unit)
+template <bool CAUSAL>
+KernelFn kernel_for(int poly) {
+  switch (poly) {
+    case 1: return fa_fwd8_kernel<CAUSAL, 1>;
+    case 2: return fa_fwd8_kernel<CAUSAL, 2>;
+    case 4: return fa_fwd8_kernel<CAUSAL, 4>;
+    case 8: return fa_fwd8_kernel<CAUSAL, 8>;
+    default: return fa_fwd8_kernel<CAUSAL, 0>;
+  }
+}
+
 template <bool CAUSAL>
 cudaError_t launch_t(const Problem& pb, void* o, float* lse, int incoherent, cudaStream_t stream) {
   constexpr int D = 128;
-  using C = Cfg<D>;
+  using C = E4m3;
   const int Nk_pad = (pb.Nk + 127) / 128 * 128;
   const size_t q8_bytes = size_t(pb.B) * pb.Nq * pb.Hq * D, k8_bytes = size_t(pb.B) * pb.Nk * pb.Hkv * D;
   const size_t vt_bytes = size_t(pb.B) * pb.Hkv * D * Nk_pad;
@@ -897,7 +371,7 @@ cudaError_t launch_t(const Problem& pb, void* o, float* lse, int incoherent, cud
               make_u8_map(&mk, k8, D, pb.Hkv, pb.Nk, pb.B, D, 128, 1, 128) &&
               make_u8_map(&mv, vt8, pb.Nk, D, pb.Hkv, pb.B, Nk_pad, 128, 128, 1) &&
               make_bshd_map(&mo, o, pb.B, pb.Nq, pb.Hq, D, 32);
-  Params p;
+  Params p{};
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;
   p.amax_q = amax_q;
@@ -913,19 +387,14 @@ cudaError_t launch_t(const Problem& pb, void* o, float* lse, int incoherent, cud
   p.neg_s = pb.scale < 0.0f ? 1u : 0u;
   p.wl = -1;
   p.wr = CAUSAL ? 0 : -1;
-  p.n_mblocks = (pb.Nq + 255) / 256;
-  p.n_units = p.n_mblocks * pb.B * pb.Hq;
   const int G = num_sms();
-  const int T = p.n_units % G;
-  const int n_split = (!CAUSAL && T > 0 && 2 * T <= G && pb.Nq > 128) ? T : 0;
-  p.n_full = p.n_units - n_split;
-  p.n_items = p.n_full + 2 * n_split;
+  fwdp::plan_units(p, pb, CAUSAL, G);
   const DebugCfg dc = debug_cfg();
   p.wait_limit_ns = dc.wait_limit_ns;
   p.inject = dc.inject;
   p.trace = dc.trace;
   p.status = status_word();
-  auto kern = fa_fwd8_kernel<D, CAUSAL, false>;
+  const KernelFn kern = kernel_for<CAUSAL>(dc.poly_every);
   if (maps && p.status) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemDyn);
   } else {
@@ -949,7 +418,7 @@ cudaError_t launch_t(const Problem& pb, void* o, float* lse, int incoherent, cud
   if (e == cudaSuccess) {
     const int grid = p.n_items < G ? p.n_items : G;
     if (dc.ev_begin) cudaEventRecord(dc.ev_begin, stream);
-    kern<<<grid, kThreads, C::kSmemDyn, stream>>>(mq, mk, mv, mo, p);
+    kern<<<grid, fwdp::kThreads, C::kSmemDyn, stream>>>(mq, mk, mv, mo, p);
     e = cudaGetLastError();
     if (dc.ev_end) cudaEventRecord(dc.ev_end, stream);
   }

@@ -30,6 +30,7 @@ struct DebugCfg {
   cudaEvent_t ev_begin;  // recorded around the main kernel when set
   cudaEvent_t ev_end;
   unsigned long long* trace;  // optional device trace buffer
+  int poly_every;             // forward exp2 split (fa_tune FA_TUNE_EXP2_SPLIT)
 };
 DebugCfg debug_cfg();
 

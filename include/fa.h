@@ -209,6 +209,24 @@ int fa_debug_set(unsigned long long wait_limit_ns, int inject);
 int fa_debug_exp2(const float* x, float* y, int n, int mode, void* stream);
 
 /*
+ * fa_tune — process-wide tuning knob, read by every later launch (not
+ *   thread-safe). Returns FA_ERR_INVALID_ARG for an unknown knob or value.
+ *   FA_TUNE_EXP2_SPLIT: how the forward softmax evaluates its exponentials
+ *     (the FlashAttention-4 article on smntcn.com: part of the exponentials
+ *     are emulated in software on the FMA pipes because the special-function
+ *     unit does not keep up with the tensor cores). value 0 (the default):
+ *     every exponential by ex2.approx on the special-function unit; value N
+ *     in {1, 2, 4, 8}: one column pair in every N by the fitted degree-3
+ *     polynomial on the FMA pipes (relative error below 7.5e-5; N = 1: all
+ *     of them), the rest as before. Applies to fa_fwd (both head dims,
+ *     causal or not) and fa_fwd_fp8; fa_fwd_window and the backward always
+ *     use the special-function unit. Results differ from the default only
+ *     by the polynomial's rounding.
+ */
+#define FA_TUNE_EXP2_SPLIT 1
+int fa_tune(int knob, int value);
+
+/*
  * fa_profile_events — begin/end are cudaEvent_t handles (or NULL to stop).
  *   While set, fa_fwd records `begin` on its stream right before its kernel
  *   and `end` right after it; fa_bwd does the same around its main

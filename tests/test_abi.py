@@ -141,3 +141,13 @@ def test_no_device_fails_loudly(fa):
 def test_debug_set_validates(fa):
     assert fa.fa_debug_set(0, 2) == 1
     assert fa.fa_debug_set(0, 0) == 0
+
+
+def test_tune_validates(fa):
+    # the exp2 split takes 0, 1, 2, 4 or 8; anything else, or an unknown knob, is rejected on the host
+    for v in (0, 1, 2, 4, 8):
+        assert fa.fa_tune(fa.TUNE_EXP2_SPLIT, v) == 0
+    for v in (-1, 3, 16):
+        assert fa.fa_tune(fa.TUNE_EXP2_SPLIT, v) == 1
+    assert fa.fa_tune(99, 0) == 1
+    assert fa.fa_tune(fa.TUNE_EXP2_SPLIT, 0) == 0

@@ -98,29 +98,54 @@ def test_workload_small_full(fa):
     run_case(fa, w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.d, w.causal, w.seed, w.sigma_qk)
 
 
+def last_round_heads(n_sms, B, Hq, Nq, causal):
+    """(batch, head) pairs with a work item in the forward's last scheduling
+    round: non-causal units run head by head (query blocks of one head in a
+    row), the last round's units split by rows; causal rounds cover every
+    head (longest query blocks first, so the last round holds block 0s)."""
+    mblocks = (Nq + 255) // 256
+    units = B * Hq * mblocks
+    if causal:
+        return {(b, h) for b in range(B) for h in range(Hq)}
+    t = split_plan(n_sms, B, Hq, Nq, causal)
+    full = units - t
+    n_items = full + 2 * t
+    first_last = (n_items - 1) // n_sms * n_sms  # first item of the last round
+    heads = set()
+    for item in range(first_last, n_items):
+        u = item if item < full else full + (item - full) // 2
+        bh = u // mblocks
+        heads.add((bh // Hq, bh % Hq))
+    return heads
+
+
 @pytest.mark.parametrize("idx", [1, 2, 3])
-def test_workload_full_size_sampled(fa, idx):
+def test_workload_full_size_whole_heads(fa, idx):
     """Full-size run in the benchmark's launch configuration; the oracle
-    checks sampled rows of a few heads (every row of those heads would take
-    minutes in fp64)."""
+    checks every row of two whole heads, the first (batch, head) and the
+    last, which runs in the last scheduling round, and sampled rows of a
+    third head."""
     w = workloads.WORKLOADS[idx]
     x = workloads.workload_inputs(w)
     q, k, v = (x[n].cuda() for n in ("q", "k", "v"))
     o, lse = fa.forward(q, k, v, causal=w.causal, scale=w.scale)
     torch.cuda.synchronize()
     assert fa.fa_get_status() == 0
-    rng = np.random.default_rng(w.seed)
-    rows = np.unique(np.concatenate([rng.choice(w.Nq, 96, replace=False), [0, 1, 127, 128, 255, w.Nq - 1]]))
-    heads = [(0, 0), (w.B - 1, w.Hq - 1), (w.B // 2, w.Hq // 2)]
+    n_sms = torch.cuda.get_device_properties(0).multi_processor_count
+    last = (w.B - 1, w.Hq - 1)
+    assert last in last_round_heads(n_sms, w.B, w.Hq, w.Nq, w.causal)
     go, glse = to64(o), to64(lse)
-    for b, h in heads:
+    rng = np.random.default_rng(w.seed)
+    sampled = np.unique(np.concatenate([rng.choice(w.Nq, 96, replace=False), [0, 1, 127, 128, 255, w.Nq - 1]]))
+    for (b, h), rows in (((0, 0), None), (last, None), ((w.B // 2, w.Hq // 2), sampled)):
         kv = h // (w.Hq // w.Hkv)
         qn = x["q"][b:b + 1, :, h:h + 1].double().numpy()
         kn = x["k"][b:b + 1, :, kv:kv + 1].double().numpy()
         vn = x["v"][b:b + 1, :, kv:kv + 1].double().numpy()
         ro, rlse = attn_ref.forward(qn, kn, vn, w.scale, w.causal, rows=rows)
-        assert_close(f"o[b{b},h{h}]", go[b:b + 1, rows, h:h + 1], ro)
-        assert_lse(glse[b:b + 1, h:h + 1, rows], rlse)
+        sel = slice(None) if rows is None else rows
+        assert_close(f"o[b{b},h{h}]", go[b:b + 1, sel, h:h + 1], ro)
+        assert_lse(glse[b:b + 1, h:h + 1, sel], rlse)
     # properties that hold at any size
     assert torch.isfinite(o).all() and torch.isfinite(lse).all()
 

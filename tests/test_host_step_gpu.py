@@ -1,16 +1,19 @@
 """fa_step_host: forward + backward on host buffers, pipelined over the
 batch (inputs in on one copy stream, compute on the caller's stream,
-results out on another). Checked through the C ABI against fa_fwd + fa_bwd
-on device buffers for the same inputs: O and LSE bit for bit (each row is
-computed by the same kernel either way), the gradients within the
-backward's tolerance (dQ is summed in fp32 in a nondeterministic order)."""
+results out on another). Checked through the C ABI element by element
+against the fp64 oracle (O, LSE, dQ, dK, dV within the parity tolerances),
+and against fa_fwd + fa_bwd on device buffers for the same inputs: O and LSE
+bit for bit (each row is computed by the same kernel either way), the
+gradients within the backward's tolerance (dQ is summed in fp32 in a
+nondeterministic order)."""
 import math
 
 import pytest
 import torch
 
 import workloads
-from tests.gpu_util import assert_close, to64
+from oracle import attn_ref
+from tests.gpu_util import assert_close, assert_lse, to64
 
 pytestmark = pytest.mark.gpu
 
@@ -60,3 +63,10 @@ def test_step_host_matches_device_calls(fa, case, pinned):
         got = outs[name]
         assert torch.isfinite(got.float()).all(), name
         assert_close(name, to64(got), to64(ref.cpu()))
+    # the oracle, element by element, on the host results
+    xs = [x[n].double().numpy() for n in ("q", "k", "v", "do")]
+    ro, rlse = attn_ref.forward(*xs[:3], scale, causal)
+    assert_close("o vs oracle", to64(outs["o"]), ro)
+    assert_lse(to64(outs["lse"]), rlse)
+    for name, ref in zip(("dq", "dk", "dv"), attn_ref.backward(*xs, scale, causal)):
+        assert_close(f"{name} vs oracle", to64(outs[name]), ref)

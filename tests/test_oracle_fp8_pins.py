@@ -92,3 +92,80 @@ def test_pv_abs_bounds_p_rounding(causal):
     o_p8 = f8.e4m3(P * 256.0) / 256.0 @ v[0, :, 0]  # P scaled into the normal e4m3 range, as the kernel's 2^(x-m)
     bound = f8.pv_abs(q, k, v, scale, causal)[0, :, 0]
     assert np.all(np.abs(o_p8 - o_exact) <= 2.0 ** -4 * bound + 1e-12)
+
+
+@pytest.mark.parametrize("incoherent", [False, True])
+def test_forward_fp8_scale_equivariance(incoherent):
+    """forward_fp8 applies each per-head scale exactly once: multiplying Q
+    (or K) of one head by a power of two leaves its e4m3 codes unchanged and
+    multiplies that head's scale by the same power, so the result equals the
+    call with the softmax scale multiplied instead; multiplying V by a power
+    of two multiplies O by it and leaves LSE unchanged. A dropped, doubled or
+    misplaced scale factor (sq, sk or sv) breaks one of these equalities."""
+    rng = np.random.default_rng(7)
+    B, N, H, d = 1, 48, 2, 128
+    q, k, v = (rng.normal(size=(B, N, H, d)) for _ in range(3))
+    scale = 0.09
+    for causal in (False, True):
+        o, lse, _ = f8.forward_fp8(q, k, v, scale, causal, incoherent=incoherent)
+        o2, lse2, _ = f8.forward_fp8(4.0 * q, k, v, scale, causal, incoherent=incoherent)
+        o3, lse3, _ = f8.forward_fp8(q, k, v, 4.0 * scale, causal, incoherent=incoherent)
+        np.testing.assert_allclose(o2, o3, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lse2, lse3, rtol=0, atol=1e-12)
+        o4, lse4, _ = f8.forward_fp8(q, 0.5 * k, v, scale, causal, incoherent=incoherent)
+        o5, lse5, _ = f8.forward_fp8(q, k, v, 0.5 * scale, causal, incoherent=incoherent)
+        np.testing.assert_allclose(o4, o5, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lse4, lse5, rtol=0, atol=1e-12)
+        o6, lse6, _ = f8.forward_fp8(q, k, 8.0 * v, scale, causal, incoherent=incoherent)
+        np.testing.assert_allclose(o6, 8.0 * o, rtol=0, atol=1e-11)
+        np.testing.assert_allclose(lse6, lse, rtol=0, atol=0)
+        assert not np.allclose(o2, o, atol=1e-3)  # the factor does reach the logits
+
+
+@pytest.mark.parametrize("incoherent", [False, True])
+def test_forward_fp8_close_to_exact_attention(incoherent):
+    """On ordinary N(0, 1) inputs the FP8 result stays within the e4m3
+    quantisation error of the exact attention. First-order estimate: every
+    element of Q M, K M and V carries a relative rounding error of rms at
+    most 2^-4 / sqrt(3) (uniform within half an ulp of a 3-bit mantissa), so
+    a logit s = scale * q.k moves by about scale * sqrt(2 d) * 2^-4 / sqrt(3)
+    (about 0.05 here) and O by that much of the spread of V under P (below
+    1) plus V's own 2^-4 / sqrt(3) relative error averaged over the attended
+    keys: a relative rms error of O of a few percent, far below the 100 % of
+    a lost scale factor and above zero (quantisation did happen)."""
+    rng = np.random.default_rng(8)
+    B, N, H, d = 1, 256, 2, 128
+    q, k, v = (rng.normal(size=(B, N, H, d)) for _ in range(3))
+    scale = 1.0 / np.sqrt(d)
+    for causal in (False, True):
+        exact, lse_exact = attn_ref.forward(q, k, v, scale, causal)
+        o, lse, _ = f8.forward_fp8(q, k, v, scale, causal, incoherent=incoherent)
+        est = scale * np.sqrt(2 * d) * 2.0 ** -4 / np.sqrt(3)
+        rel = float(np.sqrt(np.mean((o - exact) ** 2)) / np.sqrt(np.mean(exact ** 2)))
+        assert 1e-3 < rel < 2 * (est + 2.0 ** -4 / np.sqrt(3)), (causal, rel, est)
+        assert float(np.abs(lse - lse_exact).max()) < 8 * est, (causal, float(np.abs(lse - lse_exact).max()))
+
+
+@pytest.mark.parametrize("which", [0, 1, 2])
+def test_planted_dropped_scale_fails_a_pin(monkeypatch, which):
+    """A planted mistake: forward_fp8 dequantising one of Q, K, V without its
+    per-head scale (the codes themselves are right). The equivariance or the
+    closeness pin must fail."""
+    real = f8.quantize_per_head
+    calls = {"n": 0}
+
+    def broken(x):
+        codes, s = real(x)
+        i = calls["n"] % 3
+        calls["n"] += 1
+        return (codes, np.ones_like(s)) if i == which else (codes, s)
+
+    monkeypatch.setattr(f8, "quantize_per_head", broken)
+    failed = 0
+    for pin in (test_forward_fp8_scale_equivariance, test_forward_fp8_close_to_exact_attention):
+        try:
+            calls["n"] = 0
+            pin(True)
+        except AssertionError:
+            failed += 1
+    assert failed >= 1

@@ -3,20 +3,27 @@ device memory during the call (serving loops with a fixed memory plan, code
 that runs where the CUDA allocator must not be entered). Its workspace is a
 fixed device array inside the library instead of a per-call allocation.
 
-Checked through the C ABI against fa_bwd on two calls in a row with
-different problems, so a result that depended on what an earlier call left
-in the shared array would show. Kept in a file that pytest collects last."""
+Checked through the C ABI on two calls in a row with different problems, so
+a result that depended on what an earlier call left in the shared array
+would show: element by element against the fp64 oracle's gradients, and
+against fa_bwd on the same inputs. A fresh process checks that the call
+takes no device memory. Kept in a file that pytest collects last."""
 import math
+import os
+import subprocess
+import sys
 
 import pytest
 import torch
 
 import workloads
+from oracle import attn_ref
 from tests.gpu_util import assert_close, to64
 
 pytestmark = pytest.mark.gpu
 
 FA_ERR_UNSUPPORTED = 2
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 @pytest.fixture(scope="module")
@@ -41,19 +48,21 @@ def both_paths(fa, B, Hq, Hkv, Nq, Nk, d, causal, seed):
     assert fa.fa_bwd_noalloc(q, k, v, o, lse, do, *got, *args) == 0
     torch.cuda.synchronize()
     assert fa.fa_get_status() == 0
-    return got, ref
+    oracle = attn_ref.backward(*(x[n].double().numpy() for n in ("q", "k", "v", "do")), scale, causal)
+    return got, ref, oracle
 
 
-def test_noalloc_matches_fa_bwd_twice(fa):
+def test_noalloc_matches_oracle_and_fa_bwd_twice(fa):
     cases = [
         (1, 4, 2, 300, 300, 128, True, 31),   # GQA, causal, ragged length
         (2, 2, 2, 200, 520, 64, False, 32),   # another shape: must not depend on the previous contents
     ]
     for B, Hq, Hkv, Nq, Nk, d, causal, seed in cases:
-        got, ref = both_paths(fa, B, Hq, Hkv, Nq, Nk, d, causal, seed)
-        for name, g, r in zip(("dq", "dk", "dv"), got, ref):
+        got, ref, oracle = both_paths(fa, B, Hq, Hkv, Nq, Nk, d, causal, seed)
+        for name, g, r, o in zip(("dq", "dk", "dv"), got, ref, oracle):
             assert torch.isfinite(g).all(), name
-            assert_close(name, to64(g), to64(r))
+            assert_close(f"{name} vs oracle", to64(g), o)
+            assert_close(f"{name} vs fa_bwd", to64(g), to64(r))
 
 
 def test_noalloc_rejects_workspace_beyond_the_array(fa):
@@ -62,3 +71,43 @@ def test_noalloc_rejects_workspace_beyond_the_array(fa):
     p = 1 << 20  # aligned, non-null: the size check fails before anything is launched
     assert fa.fa_bwd_noalloc(*([p] * 9), B, Hq, Hkv, N, N, d, d ** -0.5, 1) == FA_ERR_UNSUPPORTED
     assert fa.fa_get_status() == 0
+
+
+# Run in a fresh interpreter: the library's memory pool is still empty there,
+# so any allocation the call made (from the pool or elsewhere) would take new
+# device memory. A first call on a small problem loads the kernels and looks
+# up the array's address; the measured call uses the same kernels on a
+# problem whose workspace (about 40 MiB) is larger than the first one's.
+_CHILD = r"""
+import math, sys, torch
+sys.path.insert(0, ROOT)
+import __graft_entry__
+__graft_entry__.build()
+import exact_attention_99_gb300 as fa
+import workloads
+torch.cuda.init()
+def run(B, Hq, Hkv, N, d, seed):
+    x = workloads.make_inputs(B, Hq, Hkv, N, N, d, seed, with_dout=True)
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
+    o, lse = fa.forward(q, k, v, causal=True)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    st = fa.fa_bwd_noalloc(q, k, v, o, lse, do, dq, dk, dv, B, Hq, Hkv, N, N, d, d ** -0.5, 1)
+    torch.cuda.synchronize()
+    free1 = torch.cuda.mem_get_info()[0]
+    assert st == 0 and fa.fa_get_status() == 0, st
+    assert torch.isfinite(dq.float()).all()
+    return free0 - free1
+run(1, 2, 2, 256, 128, 1)
+taken = run(1, 8, 4, 9000, 128, 2)
+print("TAKEN", taken)
+"""
+
+
+def test_noalloc_takes_no_device_memory():
+    code = "ROOT = " + repr(ROOT) + "\n" + _CHILD
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    taken = int(r.stdout.strip().splitlines()[-1].split()[1])
+    assert taken == 0, f"the call took {taken} bytes of device memory"
