@@ -1,17 +1,19 @@
 #!/usr/bin/env python
 """Benchmark of exact attention on GB300: one step = the whole hot path
-(forward: O and LSE; backward: dQ, dK, dV) over one batch of the headline
-workload B=4, H=16, Nq=Nk=2048, d=128, non-causal, bf16, seeded synthetic
-inputs resident in HBM.
+(forward: O and LSE; backward: dQ, dK, dV) over one batch of the largest
+single-GPU workload, causal grouped-query attention B=1, Hq=32, Hkv=8,
+Nq=Nk=16384, d=128, bf16, Q and K ~ N(0, 2^2), V and dO ~ N(0, 1), seeded
+synthetic inputs resident in HBM.
 
 Prints ONE JSON line on rank 0. `value` is TFLOP/s over all ranks (forward
-4*B*H*N*N*d plus backward 2.5x that, per step), timed on the device with
+4*B*Hq*N*N*d/2 plus backward 2.5x that, per step), timed on the device with
 CUDA events over K steps with the L2 flushed (a 256 MB write) before every
 step. Extra keys: `roofline` for the dominant kernel, `cpu_baseline` (the
-fp64 oracle on a bounded sample on the host cores), `e2e` (the same metric
-through the public API with pinned host buffers, copies included), `clocks`
-sampled during the timed region, `gpu_launches`, and `configs` with
-forward/backward TFLOP/s of every headline workload.
+fp64 oracle on bounded samples on the host cores, for this workload and for
+every published one), `e2e` (the same metric through the public API with
+pinned host buffers, copies included, beside the measured copy bandwidth),
+`clocks` sampled during the timed region, `gpu_launches`, and `configs`
+with kernel TFLOP/s of every published workload.
 
 --impl reference times the fp64 CPU oracle on the same workload (a bounded
 sample per step) and prints the same kind of line with "impl": "reference".
@@ -21,6 +23,7 @@ scaling, no collective in the data path); the timing is the max over ranks.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import glob
 import hashlib
 import json
@@ -37,10 +40,12 @@ sys.path.insert(0, ROOT)
 
 import workloads  # noqa: E402
 
-MAIN = workloads.WORKLOADS[1]
+MAIN = workloads.BY_NAME["fwd_causal_gqa_b1_hq32_hkv8_n16384_d128"]
 METRIC = "attention fwd/bwd TFLOP/s at 1 GB300 and fraction of dense BF16 tensor peak"
 FLUSH_BYTES = 256 << 20
-KERNEL_SOURCES = {"fa_fwd_kernel": "fa_fwd.cu", "bwd_main_kernel": "fa_bwd.cu"}
+KERNEL_SOURCES = {"fa_fwd_kernel": ("fa_fwd.cu", "fa_fwd_pipeline.cuh"), "bwd_main_kernel": ("fa_bwd.cu",),
+                  "fa_fwd8_kernel": ("fa_fwd8.cu", "fa_fwd_pipeline.cuh")}
+PANEL = 1024  # query rows of one oracle sample
 
 
 def step_flops(w) -> float:
@@ -74,18 +79,22 @@ def dist_env():
 
 
 def load_peaks():
+    """(burst, sustained, source) dense bf16 peaks in TFLOP/s."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         with open(path) as f:
             p = json.load(f)
-        return float(p["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops, burst cuBLAS)"
-    return 1900.0, "fallback (1.9 PFLOP/s bf16 burst from an earlier GB300 measurement)"
+        return (float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "measured (MEASURED_PEAKS.json: bf16_tflops burst, bf16_tflops_sustained)")
+    return 1900.0, 1700.0, "fallback (1.9 PFLOP/s burst, 1.7 sustained, an earlier GB300 measurement)"
 
 
 def source_sha(kernel: str) -> str:
-    path = os.path.join(ROOT, "exact_attention_99_gb300", "csrc", KERNEL_SOURCES[kernel])
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "exact_attention_99_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def profiled_traffic(kernel: str, workload: str):
@@ -105,18 +114,88 @@ def profiled_traffic(kernel: str, workload: str):
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons, every 50 ms; only
-    the samples whose timestamps fall inside the timed window (mark_begin /
-    mark_end) are summarised."""
-    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """SM clock, power and clock-event reasons of one GPU, sampled every 5 ms
+    through NVML (read-only queries) in a background thread; only the samples
+    taken inside the timed window (mark_begin / mark_end) are summarised.
+    Falls back to `nvidia-smi -lms 50` when NVML cannot be loaded."""
+    REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown", 0x4: "sw_power_cap",
+               0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, device_index: int):
-        self.dev = device_index
-        self.lines = []
-        self.proc = None
+    def __init__(self, torch_device: int):
+        self.torch_device = torch_device
+        self.samples = []  # (time, sm_mhz, max_mhz, power_w, reasons bitmask)
         self.t_begin = self.t_end = None
+        self.stop_flag = threading.Event()
+        self.thread = None
+        self.kind = None
+        self.proc = None
+
+    def _nvml_handle(self):
+        import torch
+        nv = ctypes.CDLL("libnvidia-ml.so.1")
+        if nv.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        h = ctypes.c_void_p()
+        props = torch.cuda.get_device_properties(self.torch_device)
+        bus = getattr(props, "pci_bus_id", None)
+        if bus is not None:
+            busid = f"{getattr(props, 'pci_domain_id', 0):08X}:{bus:02X}:{getattr(props, 'pci_device_id', 0):02X}.0"
+            if nv.nvmlDeviceGetHandleByPciBusId_v2(busid.encode(), ctypes.byref(h)) == 0:
+                return nv, h
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        idx = int(vis.split(",")[self.torch_device]) if vis and vis.split(",")[0].isdigit() else self.torch_device
+        if nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(idx), ctypes.byref(h)) != 0:
+            raise OSError("no NVML handle")
+        return nv, h
+
+    def start(self):
+        try:
+            nv, h = self._nvml_handle()
+            reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+            self.kind = "nvml, 5 ms"
+            self.thread = threading.Thread(target=self._nvml_loop, args=(nv, h, reasons_fn), daemon=True)
+            self.thread.start()
+            return
+        except (OSError, AttributeError):
+            pass
+        try:
+            fields = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+                      "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                      "clocks_event_reasons.sw_power_cap")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={fields}", "--format=csv,noheader,nounits",
+                                          "-lms", "50", "-i", str(self.torch_device)], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            self.kind = "nvidia-smi, 50 ms"
+            self.thread = threading.Thread(target=self._smi_loop, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.kind = None
+
+    def _nvml_loop(self, nv, h, reasons_fn):
+        clk, mx, pw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self.stop_flag.is_set():
+            t = time.time()
+            if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0 and \
+                    nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                p = pw.value / 1000.0 if nv.nvmlDeviceGetPowerUsage(h, ctypes.byref(pw)) == 0 else float("nan")
+                r = rs.value if reasons_fn(h, ctypes.byref(rs)) == 0 else 0
+                self.samples.append((t, float(clk.value), float(mx.value), p, r))
+            time.sleep(0.005)
+
+    def _smi_loop(self):
+        import datetime
+        bits = [0x8, 0x40, 0x20, 0x4]
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                r = sum(b for b, flag in zip(bits, parts[4:8]) if flag.lower().startswith("active"))
+                self.samples.append((ts, float(parts[1]), float(parts[2]), float(parts[3]), r))
+            except ValueError:
+                continue
 
     def mark_begin(self):
         self.t_begin = time.time()
@@ -124,93 +203,91 @@ class ClockSampler:
     def mark_end(self):
         self.t_end = time.time()
 
-    def start(self):
-        try:
-            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                                          "-lms", "50", "-i", str(self.dev)], stdout=subprocess.PIPE,
-                                         stderr=subprocess.DEVNULL, text=True)
-            threading.Thread(target=self._read, daemon=True).start()
-        except (OSError, FileNotFoundError):
-            self.proc = None
-
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
-
     def stop(self):
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
-        time.sleep(0.3)
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        import datetime
-        sm, mx, reasons, power = [], [], set(), []
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
-            parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 9:
-                continue
+        if self.kind is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no clock source"], "samples": 0}
+        time.sleep(0.1 if self.proc is None else 0.3)
+        self.stop_flag.set()
+        if self.proc is not None:
+            self.proc.terminate()
             try:
-                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
-            except ValueError:
-                continue
-            if self.t_begin is not None and not (self.t_begin <= ts <= self.t_end):
-                continue
-            try:
-                sm.append(float(parts[1]))
-                mx.append(float(parts[2]))
-                power.append(float(parts[3]))
-            except ValueError:
-                continue
-            for n, flag in zip(names, parts[5:9]):
-                if flag.lower().startswith("active"):
-                    reasons.add(n)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples in the timed window"], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "power_w_median": statistics.median(power), "power_w_max": max(power), "samples": len(sm),
-                "window_s": round(self.t_end - self.t_begin, 3)}
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+        inside = [s for s in list(self.samples) if self.t_begin <= s[0] <= self.t_end]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples in the timed window"], "samples": 0,
+                    "source": self.kind}
+        reasons = sorted({name for s in inside for bit, name in self.REASONS.items() if s[4] & bit})
+        power = [s[3] for s in inside if s[3] == s[3]]
+        return {"sm_mhz": statistics.median(s[1] for s in inside), "sm_max_mhz": max(s[2] for s in inside),
+                "sm_mhz_min": min(s[1] for s in inside), "reasons": reasons,
+                "power_w_median": statistics.median(power) if power else None,
+                "power_w_max": max(power) if power else None, "samples": len(inside),
+                "window_s": round(self.t_end - self.t_begin, 3), "source": self.kind}
 
 
-def oracle_sample(w, x, seconds: float, max_heads: int | None = None, first: int = 0):
-    """Time the fp64 oracle (forward + backward) head by head on the main
-    workload, starting at (batch, head) slice `first`, until `seconds` have
-    passed or `max_heads` slices are done. Returns (flops, elapsed, heads)."""
+# ---------------------------------------------------------------- oracle legs
+def visible_pairs(nq: int, nk: int, causal: bool, rows) -> int:
+    """(query, key) pairs visible to the given query rows (bottom-right
+    causal alignment: key j visible to row i iff j <= i + nk - nq)."""
+    if not causal:
+        return len(rows) * nk
+    return int(sum(max(0, min(nk, i + nk - nq + 1)) for i in rows))
+
+
+def oracle_panel(w, x, b: int, h: int, direction: str):
+    """One bounded oracle sample of workload w: the last min(PANEL, Nq) query
+    rows of (batch b, query head h) against all keys. With the bottom-right
+    causal alignment, those rows as a problem of their own (Nq' rows, the
+    same Nk keys) see exactly the keys they see in the whole problem, so the
+    sample is that part of the workload. direction "fwd": the oracle's
+    forward; "fwdbwd": forward and backward. Returns (credited flops,
+    seconds): 4*d per visible pair forward, 2.5x that backward."""
     from oracle import attn_ref
-    heads = [(b, h) for b in range(w.B) for h in range(w.Hq)]
-    heads = heads[first % len(heads):] + heads[:first % len(heads)]
-    flops_per_head = step_flops(w) / (w.B * w.Hq)
-    done, t0 = 0, time.perf_counter()
-    for b, h in heads:
-        kv = h // (w.Hq // w.Hkv)
-        sl = lambda t, hh: t[b:b + 1, :, hh:hh + 1].double().numpy()
-        q, k, v, do = sl(x["q"], h), sl(x["k"], kv), sl(x["v"], kv), sl(x["do"], h)
-        attn_ref.forward(q, k, v, w.scale, w.causal)
+    r = min(PANEL, w.Nq)
+    kv = h // (w.Hq // w.Hkv)
+    q = x["q"][b:b + 1, w.Nq - r:, h:h + 1].double().numpy()
+    k = x["k"][b:b + 1, :, kv:kv + 1].double().numpy()
+    v = x["v"][b:b + 1, :, kv:kv + 1].double().numpy()
+    pairs = visible_pairs(w.Nq, w.Nk, w.causal, range(w.Nq - r, w.Nq))
+    t0 = time.perf_counter()
+    attn_ref.forward(q, k, v, w.scale, w.causal)
+    flops = 4.0 * w.d * pairs
+    if direction == "fwdbwd":
+        do = x["do"][b:b + 1, w.Nq - r:, h:h + 1].double().numpy()
         attn_ref.backward(q, k, v, do, w.scale, w.causal)
-        done += 1
-        if time.perf_counter() - t0 >= seconds or (max_heads and done >= max_heads):
+        flops *= 3.5
+    return flops, time.perf_counter() - t0
+
+
+def oracle_sample(w, x, seconds: float, max_panels: int | None = None, first: int = 0, direction="fwdbwd"):
+    """Oracle panels (oracle_panel) of successive (batch, head) slices,
+    starting at slice `first`, until `seconds` have passed or `max_panels`
+    are done. Returns (credited flops, seconds, panels)."""
+    heads = [(b, h) for b in range(w.B) for h in range(w.Hq)]
+    done, flops, el = 0, 0.0, 0.0
+    i = first
+    while True:
+        b, h = heads[i % len(heads)]
+        f, t = oracle_panel(w, x, b, h, direction)
+        flops, el, done, i = flops + f, el + t, done + 1, i + 1
+        if el >= seconds or (max_panels and done >= max_panels):
             break
-    el = time.perf_counter() - t0
-    return done * flops_per_head, el, done
+    return flops, el, done
 
 
-def oracle_single_thread(seconds: float = 2.0):
-    """The same oracle sample on one host thread (BLAS limited to 1 thread
-    in a fresh interpreter): one (batch, head) slice of the main workload.
-    Returns (TFLOP/s, elapsed s) or None if the child fails."""
-    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
-    code = ("import bench, workloads; w = bench.MAIN; x = workloads.workload_inputs(w, with_dout=True); "
-            f"f, el, n = bench.oracle_sample(w, x, {seconds}, max_heads=1); print(f / el / 1e12, el)")
+def cpu_model() -> str:
     try:
-        out = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True, text=True,
-                             timeout=600)
-        v, el = out.stdout.strip().splitlines()[-1].split()
-        return float(v), float(el)
-    except (subprocess.SubprocessError, ValueError, IndexError):
-        return None
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return "unknown"
 
 
 def blas_threads() -> int:
@@ -220,35 +297,68 @@ def blas_threads() -> int:
     return os.cpu_count() or 1
 
 
+def oracle_per_workload(seconds_each: float = 2.0):
+    """The oracle on every published workload (bounded samples: oracle
+    panels of successive heads for about `seconds_each`): forward for the
+    forward workloads, forward + backward for the backward one."""
+    out = {}
+    for w in workloads.WORKLOADS:
+        x = workloads.workload_inputs(w, with_dout=True)
+        direction = "fwdbwd" if w.direction == "bwd" else "fwd"
+        f, el, n = oracle_sample(w, x, seconds_each, direction=direction)
+        out[w.name] = {"tflops": f / el / 1e12, "seconds": round(el, 2), "direction": direction,
+                       "sample": f"{n} panel(s) of the last {min(PANEL, w.Nq)} query rows of one (batch, head)"}
+    return out
+
+
+def oracle_single_thread():
+    """The oracle on one host thread (BLAS limited to 1 thread in a fresh
+    interpreter) on the first two published workloads: forward, one panel.
+    Returns {workload: {tflops, seconds}} or {} if the child fails."""
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = ("import json, bench, workloads\nout = {}\nfor w in workloads.WORKLOADS[:2]:\n"
+            "    x = workloads.workload_inputs(w)\n"
+            "    f, el, n = bench.oracle_sample(w, x, 0.0, max_panels=1, direction='fwd')\n"
+            "    out[w.name] = {'tflops': f / el / 1e12, 'seconds': round(el, 2)}\nprint(json.dumps(out))")
+    try:
+        r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True, text=True,
+                           timeout=600)
+        return json.loads(r.stdout.strip().splitlines()[-1])
+    except (subprocess.SubprocessError, ValueError, IndexError):
+        return {}
+
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return
     w = MAIN
     x = workloads.workload_inputs(w, with_dout=True)
-    flops_head = step_flops(w) / (w.B * w.Hq)
     for i in range(args.warmup):
-        oracle_sample(w, x, 0.0, max_heads=1, first=i)
-    times = []
+        oracle_panel(w, x, 0, i % w.Hq, "fwdbwd")
+    flops, times = 0.0, []
     for i in range(args.steps):
-        _, el, _ = oracle_sample(w, x, 0.0, max_heads=1, first=args.warmup + i)
+        f, el = oracle_panel(w, x, 0, (args.warmup + i) % w.Hq, "fwdbwd")
+        flops += f
         times.append(el)
     total = sum(times)
-    value = args.steps * flops_head / total / 1e12
-    sample = f"one (batch, head) slice of {w.name} per step: fp64 forward + backward, N={w.Nq}, d={w.d}"
+    value = flops / total / 1e12
+    sample = (f"per step: the last {min(PANEL, w.Nq)} query rows of one (batch, head) slice of {w.name} against "
+              f"all {w.Nk} keys, fp64 forward + backward (credited flops: 4*d per visible pair, x3.5)")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Nq": w.Nq, "Nk": w.Nk, "d": w.d,
-                   "causal": w.causal, "step": "fwd+bwd of one head (bounded sample)"},
+                   "causal": w.causal, "sigma_qk": w.sigma_qk, "step": "fwd+bwd of a bounded sample"},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
-                         "sample": sample},
+                         "sample": sample, "cpu_model": cpu_model()},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------ GPU legs
 def time_one(fn, flush, reps=20, warm=3, stats=None):
     """Median device time (ms) of `reps` calls after `warm` untimed ones, the
     L2 flushed before each; `stats` (a dict) also receives the minimum."""
@@ -271,9 +381,9 @@ def time_one(fn, flush, reps=20, warm=3, stats=None):
 
 def per_config(fa, flush, peak):
     """Forward TFLOP/s of every workload; backward TFLOP/s (preprocess, main
-    kernel and dQ convert) of the backward workload, the headline workload
-    and, at scale for grouped-query heads, the causal GQA workload
-    (kernel-only, inputs resident, L2 flushed)."""
+    kernel and dQ convert) of the backward workload, the non-causal d = 128
+    workload and the causal GQA workload (kernel-only, inputs resident, L2
+    flushed)."""
     import torch
     out = {}
     for w in workloads.WORKLOADS:
@@ -286,7 +396,7 @@ def per_config(fa, flush, peak):
         ms = time_one(fwd, flush, stats=st)
         ent = {"fwd_ms": ms, "fwd_min_ms": st["min"], "fwd_tflops": w.fwd_flops() / ms / 1e9}
         ent["fwd_frac_of_peak"] = ent["fwd_tflops"] / peak
-        if w.direction == "bwd" or w is MAIN or w.Hkv < w.Hq:
+        if w.direction == "bwd" or w.name == "fwd_b4_h16_n2048_d128" or w.Hkv < w.Hq:
             dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
             bwd = lambda: fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.d, w.scale,
                                     int(w.causal))
@@ -369,6 +479,40 @@ def fp8_config(fa, flush, peak):
     return out
 
 
+def link_bandwidth(nbytes: int = 256 << 20, reps: int = 5):
+    """Pinned host <-> device copy bandwidth (GB/s, best of `reps`), one
+    cudaMemcpyAsync per copy (torch's copy_ between a pinned host tensor and
+    a device tensor), each direction alone and both at once on two streams."""
+    import torch
+    h_in = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    h_out = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    d_a = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    d_b = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def best(fn):
+        ts = []
+        for _ in range(reps):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            fn()
+            torch.cuda.synchronize()
+            ts.append(time.perf_counter() - t0)
+        return min(ts)
+
+    h2d = nbytes / best(lambda: d_a.copy_(h_in, non_blocking=True)) / 1e9
+    d2h = nbytes / best(lambda: h_out.copy_(d_b, non_blocking=True)) / 1e9
+
+    def both():
+        with torch.cuda.stream(s1):
+            d_a.copy_(h_in, non_blocking=True)
+        with torch.cuda.stream(s2):
+            h_out.copy_(d_b, non_blocking=True)
+    duplex = 2 * nbytes / best(both) / 1e9
+    return {"h2d_gbps": round(h2d, 1), "d2h_gbps": round(d2h, 1), "duplex_gbps": round(duplex, 1),
+            "how": f"pinned {nbytes >> 20} MiB, one cudaMemcpyAsync per copy, best of {reps}"}
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -383,7 +527,7 @@ def run_ours(args):
     fa.fa_debug_set(0, 0)
 
     w = MAIN
-    peak, peak_src = load_peaks()
+    peak, peak_sus, peak_src = load_peaks()
     x = workloads.workload_inputs(w, with_dout=True)
     q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
     o, dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
@@ -416,10 +560,9 @@ def run_ours(args):
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    sampler = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else
-                           int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]))
+    sampler = ClockSampler(local)
     sampler.start()
-    time.sleep(0.2)
+    time.sleep(0.05)
     torch.cuda.synchronize()
     sampler.mark_begin()
     for i in range(K):
@@ -457,13 +600,21 @@ def run_ours(args):
     for i in range(ke):
         flush.zero_()
         ee0[i].record()
-        # one call: per batch element, inputs in, forward + backward, results out, pipelined
+        # one call: inputs in, forward + backward, results out, pipelined over chunks of heads
         if fa.fa_step_host(*host_args, *args_f):
             raise RuntimeError("fa_step_host failed")
         ee1[i].record()
     torch.cuda.synchronize()
+    if fa.fa_get_status() != 0:
+        raise RuntimeError("device status not OK after fa_step_host")
     e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(ee0, ee1))
     e2e_value = world * step_flops(w) / (e2e_ms * 1e-3) / 1e12
+    link = link_bandwidth()
+    # the step cannot take less than its device time nor than its copies at
+    # the measured link rate (each direction alone); e2e_frac compares it
+    # with that bound
+    copy_ms = max(h2d / link["h2d_gbps"], d2h / link["d2h_gbps"]) * 1e-6
+    bound_ms = max(total_ms / K, copy_ms)
 
     if rank != 0:
         if world > 1:
@@ -478,7 +629,9 @@ def run_ours(args):
         kname, kflops, kms = "fa_fwd_kernel", w.fwd_flops(), fwd_ms
     achieved = kflops / (kms * 1e-3) / 1e12
     roofline = {"bound": "tensor", "kernel": kname, "achieved": round(achieved, 2), "peak": peak,
-                "peak_source": peak_src, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                "peak_source": peak_src + "; burst used: each launch is timed alone with CUDA events",
+                "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                "frac_of_sustained": round(achieved / peak_sus, 4), "peak_sustained": peak_sus,
                 "traffic": profiled_traffic(kname, w.name), "avg_launch_ms": round(kms, 4),
                 "flops_per_launch": kflops}
 
@@ -490,29 +643,31 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": round(total_ms / K, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Nq": w.Nq, "Nk": w.Nk, "d": w.d,
-                   "causal": w.causal, "step": "fwd (O, LSE) + bwd (dQ, dK, dV)", "l2": "flushed before every step",
+                   "causal": w.causal, "sigma_qk": w.sigma_qk, "sigma_v": w.sigma_v, "sigma_do": 1.0,
+                   "step": "fwd (O, LSE) + bwd (dQ, dK, dV)", "l2": "flushed before every step (256 MB write)",
                    "parallelism": f"replicas x{world}"},
         "fwd_kernel_ms": round(fwd_ms, 4), "bwd_main_kernel_ms": round(bwd_ms, 4),
-        "fwd_tflops": round(w.fwd_flops() / fwd_ms / 1e9, 2),
+        "fwd_tflops": round(w.fwd_flops() / fwd_ms / 1e9, 2), "fwd_frac_of_peak": round(w.fwd_flops() / fwd_ms / 1e9 / peak, 4),
         "bwd_main_tflops": round(w.bwd_flops() / bwd_ms / 1e9, 2),
         "roofline": roofline,
         "clocks": clocks,
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4), "link": link,
+                "link_gbps": link["duplex_gbps"], "copy_ms_at_link": round(copy_ms, 4),
+                "bound_ms": round(bound_ms, 4), "frac_of_bound": round(bound_ms / e2e_ms, 4),
+                "copy_fraction_of_link": round((h2d + d2h) / (e2e_ms * 1e-3) / 1e9 / link["duplex_gbps"], 4)},
         "gpu_launches": 4 * K,
         "configs": per_workload,
     }
     if world == 1:
-        flops_done, el, heads = oracle_sample(w, x, args.cpu_seconds)
-        line["cpu_baseline"] = {"value": flops_done / el / 1e12, "unit": "TFLOP/s", "cores": blas_threads(),
-                                "kind": "oracle",
-                                "sample": f"{heads} of {w.B * w.Hq} (batch, head) slices of {w.name}, fp64 "
-                                          f"forward + backward, {el:.1f} s"}
-        one = oracle_single_thread()
-        if one is not None:
-            line["cpu_baseline"]["single_thread"] = {
-                "value": one[0], "unit": "TFLOP/s", "cores": 1,
-                "sample": f"1 (batch, head) slice of {w.name}, fp64 forward + backward, {one[1]:.1f} s"}
+        flops_done, el, panels = oracle_sample(w, x, args.cpu_seconds)
+        line["cpu_baseline"] = {
+            "value": flops_done / el / 1e12, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+            "cpu_model": cpu_model(), "host_cpus": os.cpu_count(),
+            "sample": f"{panels} panel(s), each the last {min(PANEL, w.Nq)} query rows of one (batch, head) of "
+                      f"{w.name} against all keys, fp64 forward + backward, {el:.1f} s",
+            "per_workload": oracle_per_workload(args.cpu_seconds / 6),
+            "single_thread": oracle_single_thread()}
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()
@@ -530,6 +685,8 @@ def run_profile_target(args):
     __graft_entry__.build()
     import exact_attention_99_gb300 as fa
     fa.fa_debug_set(0, 0)
+    if fa.fa_tune(fa.TUNE_EXP2_SPLIT, args.exp2_split):
+        raise ValueError("bad --exp2-split")
     if args.profile_workload == WINDOW_CASE["name"]:
         c = WINDOW_CASE
         x = workloads.make_inputs(c["B"], c["H"], c["H"], c["N"], c["N"], c["d"], c["seed"], with_dout=True)
@@ -537,8 +694,7 @@ def run_profile_target(args):
         fwd_call, bwd_call = fa.fa_fwd_window, fa.fa_bwd_window
         B, H, N = c["B"], c["H"], c["N"]
     else:
-        byname = {w.name: w for w in workloads.WORKLOADS}
-        w = byname[args.profile_workload]
+        w = workloads.BY_NAME[args.profile_workload]
         x = workloads.workload_inputs(w, with_dout=True)
         a = (w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.d, w.scale, int(w.causal))
         fwd_call, bwd_call = fa.fa_fwd, fa.fa_bwd
@@ -565,12 +721,13 @@ def run_profile_target(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=400)  # about 0.4 s timed: long enough to sample clocks
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=50)  # about 0.4 s timed
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--profile-workload", default=None, help="profiling target: run one workload's pass only")
     ap.add_argument("--profile-pass", choices=["fwd", "fwd8", "bwd"], default="fwd")
+    ap.add_argument("--exp2-split", type=int, default=0, help="profiling target: forward exp2 split (fa_tune)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     if args.profile_workload:
