@@ -2,8 +2,8 @@
 // processing: Q and K are multiplied by one random orthogonal matrix
 // diag(signs) H_128 / sqrt(128) (H the Sylvester-Hadamard matrix), which
 // leaves Q K^T unchanged but spreads outlier channels, then Q, K and V are
-// scaled per (batch, head) so that their largest magnitude maps to 448 and
-// rounded to e4m3 (the FlashAttention-3 summary on news.hada.io, sections
+// scaled per (batch, head) by the power of two that maps their largest
+// magnitude into (224, 448] and rounded to e4m3 (the FlashAttention-3 summary on news.hada.io, sections
 // on FP8 and incoherent processing). Both GEMMs run as tcgen05.mma
 // kind::f8f6f4 with fp32 accumulation; P is rounded to e4m3 for the P V
 // GEMM; the softmax, its conditional rescale and the epilogue are the
@@ -29,10 +29,18 @@ namespace fwd8 {
 using fwdp::Params;
 using fwdp::Unit;
 
-// e4m3 scale of a tensor from its per-head max |x| (float bits)
+// e4m3 scale of a tensor from its per-head max |x| (float bits): the
+// smallest power of two s with amax / s <= 448, so the largest magnitude maps
+// into (224, 448]; 1 for an all-zero head. With amax = m 2^E (m in [1/2, 1))
+// and 448 = 0.875 2^9 that is s = 2^(E - 9) when m <= 0.875, else 2^(E - 8).
+// Dividing by a power of two is exact, so the e4m3 code of x is the
+// round-to-nearest-even of x / s itself, whatever precision computes it.
 __device__ __forceinline__ float amax_scale(unsigned bits) {
   const float a = __uint_as_float(bits);
-  return a > 0.0f ? a * (1.0f / 448.0f) : 1.0f;
+  if (!(a > 0.0f)) return 1.0f;
+  int E;
+  const float m = frexpf(a, &E);
+  return ldexpf(1.0f, m <= 0.875f ? E - 9 : E - 8);
 }
 
 // two floats to e4m3 (round to nearest even, saturating at +-448); lo in

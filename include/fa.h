@@ -68,7 +68,10 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
            int d, float scale, int causal, void* stream);
 
 /*
- * fa_fwd_window — the forward pass with a sliding-window (local) mask.
+ * fa_fwd_window — the forward pass with a sliding-window (local) mask (the
+ *   FlashAttention-4 article on smntcn.com names variable and local masks;
+ *   the pages do not define them, so this is the causal mask's bottom-right
+ *   alignment with two bounds).
  *   Key j is visible to query row i iff
  *       i + off - window_left <= j <= i + off + window_right,  off = Nk - Nq
  *   (the bottom-right alignment of the causal mask); a negative bound, or one
@@ -88,11 +91,16 @@ int fa_fwd_window(const void* q, const void* k, const void* v, void* o, float* l
  *   d by diag(signs) H_128 / sqrt(128) (H the Sylvester-Hadamard matrix;
  *   sign_i = -1 where bit 31 of 2654435769 * (i + 1) mod 2^32 is set), which
  *   leaves Q K^T unchanged and spreads outlier channels; incoherent = 0
- *   skips it. Q (transformed), K (transformed) and V are then scaled per
- *   (batch, head) so their largest magnitude maps to 448 and rounded to e4m3
- *   (nearest, ties to even); P is rounded to e4m3 for the P V GEMM. The
- *   result approximates fa_fwd's: O is the attention of the dequantised
- *   tensors up to the rounding of P.
+ *   skips it. Q (transformed), K (transformed) and V are then divided per
+ *   (batch, head) by the smallest power of two that brings their largest
+ *   magnitude to at most 448 (into (224, 448]) and rounded to e4m3 (nearest,
+ *   ties to even; a division by a power of two is exact, so each code is the
+ *   rounding of the exact quotient); P is rounded to e4m3 for the P V GEMM.
+ *   The result approximates fa_fwd's: O is the attention of the dequantised
+ *   tensors up to the rounding of P. (The FlashAttention-3 summary on
+ *   news.hada.io, sections on FP8 and incoherent processing: e4m3 GEMMs,
+ *   and a random orthogonal transform that spreads outliers before
+ *   quantisation.)
  *   Workspace: the e4m3 copies (B*(Nq*Hq + Nk*Hkv)*128 bytes plus
  *   B*Hkv*128*ceil(Nk/128)*128 for V transposed) and per-head maxima, from
  *   the per-device pool fa_bwd uses, on `stream`.

@@ -10,15 +10,19 @@ same low-precision path): Q and K are multiplied by one random orthogonal
 matrix M = diag(signs) H_d / sqrt(d) (H_d the Sylvester-Hadamard matrix) so
 that outlier channels are spread before quantisation; since M M^T = I,
 (Q M)(K M)^T = Q K^T and the attention is unchanged in exact arithmetic.
-Q M, K M and V are then scaled per (batch, head) so that their largest
-magnitude maps to 448 (the largest finite e4m3 value) and rounded to e4m3
-(round to nearest, ties to even, saturating). The attention of the
+Q M, K M and V are then scaled per (batch, head) by the smallest power of
+two that brings their largest magnitude to at most 448 (the largest finite
+e4m3 value), i.e. into (224, 448], and rounded to e4m3 (round to nearest,
+ties to even, saturating). The attention of the
 dequantised tensors (values times their scales) is the reference this
 module returns; the GPU path additionally rounds P to e4m3 for the P V
 GEMM, an error the tests bound separately (``pv_abs``).
 
 Readings where the pages are silent:
-  * one scale per (batch, head) and tensor;
+  * one scale per (batch, head) and tensor, a power of two: dividing by it
+    is exact, so a code is the round-to-nearest-even of x / s whatever
+    precision the division is done in (a scale of amax / 448 would let the
+    rounding of the division decide ties, which bf16 inputs hit often);
   * the signs: sign_i = -1 where bit 31 of (2654435769 * (i + 1)) mod 2^32
     is set, else +1 (a fixed counter-based sequence, the same on both
     sides);
@@ -31,7 +35,8 @@ import scipy.linalg
 
 from oracle import attn_ref
 
-__all__ = ["E4M3_MAX", "hadamard_signs", "hadamard", "e4m3", "quantize_per_head", "forward_fp8", "pv_abs"]
+__all__ = ["E4M3_MAX", "hadamard_signs", "hadamard", "e4m3", "pow2_scale", "quantize_per_head", "forward_fp8",
+           "pv_abs"]
 
 E4M3_MAX = 448.0
 
@@ -66,12 +71,23 @@ def e4m3(x: np.ndarray) -> np.ndarray:
     return np.where(x < 0, -q, q)
 
 
+def pow2_scale(amax: np.ndarray) -> np.ndarray:
+    """The smallest power of two s with amax / s <= 448 (1 where amax = 0):
+    s = 2^ceil(log2(amax / 448)), computed exactly from amax = m 2^E with m
+    in [1/2, 1) and 448 = (7/8) 2^9: s = 2^(E - 9) if m <= 7/8 else 2^(E - 8)."""
+    amax = np.asarray(amax, dtype=np.float64)
+    m, E = np.frexp(amax)
+    e = np.where(m <= 0.875, E - 9, E - 8)
+    return np.where(amax > 0, np.ldexp(1.0, e), 1.0)
+
+
 def quantize_per_head(x: np.ndarray):
-    """x [B, N, H, d] -> (e4m3 values as fp64, scales [B, H]) with
-    amax(|x[b, :, h, :]|) mapped to 448 (scale 1 for an all-zero head)."""
+    """x [B, N, H, d] -> (e4m3 values as fp64, scales [B, H]): each head's
+    scale is pow2_scale(amax(|x[b, :, h, :]|)), so its largest magnitude maps
+    into (224, 448] (scale 1 for an all-zero head)."""
     x = np.asarray(x, dtype=np.float64)
     amax = np.abs(x).max(axis=(1, 3))                      # [B, H]
-    s = np.where(amax > 0, amax / E4M3_MAX, 1.0)
+    s = pow2_scale(amax)
     q = e4m3(x / s[:, None, :, None])
     return q, s
 

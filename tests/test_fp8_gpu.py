@@ -49,13 +49,24 @@ def rounding_sd(qd, kd, vd, scale, causal):
 
 
 def check_against_oracle(go, glse, x, causal, incoherent, scale, mean_check=True):
-    """Elementwise: |err| <= 2^-4 sum_j P_ij |V_jc| (P rounding, worst case)
-    + 2^-8 |O| (bf16 output) + 4e-3 (e4m3 codes that the fp32 transform and
-    scale put on the other side of a rounding tie than fp64 does). Mean:
-    at most twice the expected |error| of independent P rounding."""
+    """Bounds, with the GPU and the oracle rounding Q M, K M, V to the same
+    e4m3 codes (power-of-two scales make each code the exact round-to-even
+    of x / s; the fp32 transform of the incoherent path can still put a
+    value within its rounding error of a tie, with probability about 2^-18
+    per element, and flip that one code by one e4m3 ulp):
+      O elementwise: |err| <= 2^-4 sum_j P_ij |V_jc| (rounding P to e4m3,
+        worst case) + 2^-8 |O| (bf16 output) + 1e-4 (fp32 accumulation),
+        + 4e-3 with the transform (a flipped code);
+      O mean: at most twice the expected |error| of independent P rounding;
+      LSE: the same -inf rows; |err| <= max_j |dS_ij| (LSE is 1-Lipschitz in
+        the logits) with dS from fp32 accumulation and ex2.approx only, so
+        max 1e-5 and mean 1e-5 without the transform; with it, max 1e-3
+        (the benchmark spec's LSE tolerance, room for a flipped code in a row it
+        does not dominate) and mean 1e-5."""
     qn, kn, vn = (x[n].double().numpy() for n in ("q", "k", "v"))
     ro, rlse, (qd, kd, vd) = f8.forward_fp8(qn, kn, vn, scale, causal, incoherent=incoherent)
-    bound = 2.0 ** -4 * f8.pv_abs(qd, kd, vd, scale, causal) + 2.0 ** -8 * np.abs(ro) + 4e-3
+    flip = 4e-3 if incoherent else 0.0
+    bound = 2.0 ** -4 * f8.pv_abs(qd, kd, vd, scale, causal) + 2.0 ** -8 * np.abs(ro) + 1e-4 + flip
     err = np.abs(go - ro)
     worst = np.unravel_index(np.argmax(err - bound), err.shape)
     assert np.all(err <= bound), (f"worst |err| {err[worst]:.3e} > bound {bound[worst]:.3e} at {worst}; "
@@ -66,7 +77,8 @@ def check_against_oracle(go, glse, x, causal, incoherent, scale, mean_check=True
     fin = np.isfinite(rlse)  # rows that see no key: -inf on both sides
     assert np.array_equal(np.isfinite(glse), fin) and np.all(glse[~fin] == rlse[~fin])
     lerr = np.abs(glse[fin] - rlse[fin])
-    assert float(lerr.max()) <= 2e-2 and float(lerr.mean()) <= 2e-3, (lerr.max(), lerr.mean())
+    lmax = 1e-3 if incoherent else 1e-5
+    assert float(lerr.max()) <= lmax and float(lerr.mean()) <= 1e-5, (lerr.max(), lerr.mean())
 
 
 SHAPES = [

@@ -51,17 +51,47 @@ def test_incoherent_transform_leaves_attention_unchanged():
         np.testing.assert_allclose(l2, l1, atol=1e-12)
 
 
+def test_pow2_scale_is_the_smallest_power_of_two():
+    """Checked with exact rational arithmetic: s is a power of two, amax / s
+    <= 448, and amax / (s / 2) > 448."""
+    from fractions import Fraction
+    rng = np.random.default_rng(9)
+    vals = np.concatenate([rng.uniform(1e-3, 1e3, 500), [448.0, 224.0, 224.00000000001, 5.25, 4.53125, 1.0, 2.0 ** -20,
+                                                         448.0 * 2 ** 7, 447.9999, 392.0, 392.5]])
+    for a, s in zip(vals, f8.pow2_scale(vals)):
+        fs = Fraction(float(s))
+        assert fs.numerator == 1 or fs.denominator == 1, s
+        assert (fs.numerator & (fs.numerator - 1)) == 0 and (fs.denominator & (fs.denominator - 1)) == 0, s
+        assert Fraction(float(a)) / fs <= 448 < Fraction(float(a)) / (fs / 2), (a, s)
+    assert f8.pow2_scale(np.array([0.0]))[0] == 1.0
+
+
 def test_quantize_per_head():
     rng = np.random.default_rng(4)
     x = rng.normal(size=(2, 50, 3, 128)) * np.array([1.0, 10.0, 0.01])[None, None, :, None]
     q, s = f8.quantize_per_head(x)
-    np.testing.assert_array_equal(np.abs(q).max(axis=(1, 3)), 448.0)  # each head's amax maps to 448
+    top = np.abs(q).max(axis=(1, 3))
+    assert np.all((top > 224.0) & (top <= 448.0))                     # each head's amax maps into (224, 448]
     np.testing.assert_array_equal(f8.e4m3(q), q)                       # already e4m3 values
+    np.testing.assert_array_equal(q, f8.e4m3(x / s[:, None, :, None]))  # exact division by a power of two
     deq = q * s[:, None, :, None]
     big = np.abs(x) > 2.0 ** -6 * s[:, None, :, None]                  # normal range: half an ulp relative
     assert np.all(np.abs(deq - x)[big] <= 2.0 ** -4 * np.abs(x)[big] + 1e-15)
     z, sz = f8.quantize_per_head(np.zeros((1, 4, 1, 8)))
     assert np.all(z == 0) and np.all(sz == 1.0)
+
+
+def test_codes_of_bf16_inputs_do_not_depend_on_the_division_precision():
+    """With a power-of-two scale, x / s in fp32 (as a GPU computes it) and in
+    fp64 give the same e4m3 code for every bf16 x, including the exact ties
+    that bf16 values hit (e.g. amax = 5.25, where amax / 448 is 3/256)."""
+    rng = np.random.default_rng(10)
+    x = torch.from_numpy(rng.normal(size=(1, 700, 1, 128))).to(torch.bfloat16).double().numpy()
+    x[0, 0, 0, 0] = 5.25
+    q64, s = f8.quantize_per_head(x)
+    x32 = torch.from_numpy(x).float() / torch.from_numpy(s).float()[:, None, :, None]
+    q32 = x32.to(torch.float8_e4m3fn).double().numpy()
+    np.testing.assert_array_equal(q32, q64)
 
 
 def test_incoherent_processing_lowers_fp8_error_with_outliers():
