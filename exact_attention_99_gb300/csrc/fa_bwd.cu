@@ -38,6 +38,7 @@
 //   The accumulator is [B*Hq, d, Nq_pad] fp32 (query index innermost).
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <cmath>
 #include <mutex>
 
@@ -100,6 +101,10 @@ struct Params {
   const float* lse2;    // [B*Hq, Nq_pad]: LSE*log2(e), +inf for padded / empty rows
   const float* delta;   // [B*Hq, Nq_pad]
   int B, Hq, Hkv, Nq, Nk, Nq_pad, group, n_ktiles, n_qtiles;
+  // causal pairs (see decode): of the n_ktiles / 2 pairs (j, n-1-j) of each
+  // head, the last n_split (those nearest the middle, both tiles about half
+  // a pair's work) run as two single-tile CTAs each, after every whole pair
+  int n_split;
   // masked kernels: key j visible to query row i iff i + off - wl <= j <=
   // i + off + wr (off = Nk - Nq); a negative bound is no limit; causal is
   // wl = -1, wr = 0
@@ -129,14 +134,29 @@ __device__ __forceinline__ Work decode(const Params& p) {
   int r;
   if (CAUSAL && win_l<WIN>(p) < 0) {
     // key tiles j and n-1-j share a CTA: the pair always has n+1 query-tile
-    // steps (for Nq = Nk), so all CTAs carry the same work; heads in a row
-    const int n_pairs = (p.n_ktiles + 1) / 2;
-    r = blockIdx.x / n_pairs;
-    const int pr = blockIdx.x - r * n_pairs;
-    const int j2 = p.n_ktiles - 1 - pr;
-    w.it[0].j = pr;
-    w.it[1].j = j2;
-    w.n_items = j2 > pr ? 2 : 1;
+    // steps (for Nq = Nk), so all these CTAs carry the same work; heads in a
+    // row. After them come single tiles: both tiles of the n_split pairs of
+    // each head nearest the middle (pair index n/2 - n_split .. n/2 - 1),
+    // then the middle tile when n is odd; each has about half a pair's work
+    // and fills what would otherwise be a partly idle last wave of pairs.
+    const int half = p.n_ktiles / 2, kept = half - p.n_split;
+    const int whole = p.B * p.Hkv * kept;
+    if (int(blockIdx.x) < whole) {
+      r = blockIdx.x / kept;
+      const int pr = blockIdx.x - r * kept;
+      w.it[0].j = pr;
+      w.it[1].j = p.n_ktiles - 1 - pr;
+      w.n_items = 2;
+    } else {
+      const int per_head = 2 * p.n_split + (p.n_ktiles & 1);
+      const int s = blockIdx.x - whole;
+      r = s / per_head;
+      const int t = s - r * per_head;
+      const int pr = kept + (t >> 1);
+      w.it[0].j = t < 2 * p.n_split ? ((t & 1) ? p.n_ktiles - 1 - pr : pr) : half;
+      w.it[1].j = 0;
+      w.n_items = 1;
+    }
   } else {
     // all key tiles of one head in a row, so concurrent CTAs share Q, dO and
     // the dQ accumulator in L2 (also for windows with a left bound, where
@@ -762,6 +782,39 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(const float* dq_acc, __nv
   }
 }
 
+// How many key-tile pairs per head (those nearest the middle) to run as two
+// single-tile CTAs, for `heads` (batch, kv head) slices of n key tiles on G
+// SMs (one CTA each). Model, in units of half a pair's work: a whole pair
+// takes 2, a single 1; CTAs start in launch order as SMs free up (pairs
+// first). With P whole pairs in W = P / G full waves and T = P mod G more,
+// S singles finish at the smallest t with (G - T) (t - 2W) + T max(0, t - 2W
+// - 2) >= S. The smallest split count reaching the least finish time wins.
+int split_pairs(int heads, int n, int G) {
+  const int half = n / 2;
+  int best_m = 0;
+  long long best_t = -1;
+  for (int m = 0; m <= half; ++m) {
+    const long long P = 1LL * heads * (half - m), S = 1LL * heads * (2 * m + (n & 1));
+    const long long W = P / G, T = P % G;
+    long long t = 2 * W + (T > 0 ? 2 : 0);
+    if (S > 0) {
+      // singles start at 2W on the G - T free SMs, at 2W + 2 on the others
+      long long lo = 1, hi = S;
+      while (lo < hi) {
+        const long long mid = (lo + hi) / 2;
+        const long long cap = (G - T) * mid + T * (mid > 2 ? mid - 2 : 0);
+        if (cap >= S) hi = mid; else lo = mid + 1;
+      }
+      t = std::max(t, 2 * W + lo);
+    }
+    if (best_t < 0 || t < best_t) {
+      best_t = t;
+      best_m = m;
+    }
+  }
+  return best_m;
+}
+
 template <int D, bool CAUSAL, bool WIN>
 cudaError_t launch_t(const Problem& pb, const void* o, const float* lse, const void* dout, void* dq, void* dk, void* dv,
                      float* ws, cudaStream_t stream) {
@@ -827,7 +880,9 @@ cudaError_t launch_t(const Problem& pb, const void* o, const float* lse, const v
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const bool paired = CAUSAL && (WIN ? p.wl : -1) < 0;  // decode: pairs of key tiles only without a left bound
-  const unsigned grid = unsigned(pb.B) * pb.Hkv * (paired ? (p.n_ktiles + 1) / 2 : p.n_ktiles);
+  p.n_split = paired ? split_pairs(pb.B * pb.Hkv, p.n_ktiles, num_sms()) : 0;
+  const unsigned grid =
+      paired ? unsigned(pb.B) * pb.Hkv * (p.n_ktiles / 2 + p.n_split + (p.n_ktiles & 1)) : unsigned(pb.B) * pb.Hkv * p.n_ktiles;
   if (dc.ev_begin) cudaEventRecord(dc.ev_begin, stream);
   kern<<<grid, kThreads, smem, stream>>>(mq, mk, mv, mdo, macc, p);
   e = cudaGetLastError();

@@ -54,7 +54,7 @@ from __future__ import annotations
 
 import numpy as np
 
-__all__ = ["visible_mask", "probabilities", "forward", "backward", "blockwise_forward"]
+__all__ = ["visible_mask", "probabilities", "forward", "backward", "backward_abs_terms", "blockwise_forward"]
 
 PANEL_ROWS = 1024  # rows of S formed at a time (memory bound only; every entry is formed)
 
@@ -186,6 +186,50 @@ def backward(q, k, v, do, scale: float, causal: bool, window=None):
                 dq[b, rr, h, :] = scale * (dS @ K)
                 dk[b, :, kv, :] += scale * (dS.T @ Q)
     return dq, dk, dv
+
+
+def backward_abs_terms(q, k, v, do, scale: float, causal: bool, window=None):
+    """Magnitudes that bound how much rounding the intermediates P and dS
+    (relative error at most e per element) can move the gradients, per
+    output element, formed from the same quantities as ``backward``:
+
+        a_dq[b, i, h, c] = scale * sum_j |dS_ij| |K_jc|
+        a_dk[b, j, g, c] = scale * sum_{h in g} sum_i |dS_ij| |Q_ic|
+        a_dv[b, j, g, c] = sum_{h in g} sum_i P_ij |dO_ic|
+
+    (triangle inequality on dQ = scale dS K, dK = scale dS^T Q, dV = P^T dO:
+    rounding every dS_ij to dS_ij (1 + e_ij) with |e_ij| <= e moves dQ_ic by
+    at most e a_dq[i, c]; likewise dK, and dV for P). Test infrastructure
+    for the error bounds of the GPU comparisons."""
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    do = np.asarray(do, dtype=np.float64)
+    B, Nq, Hq, d = q.shape
+    _, Nk, Hkv, _ = k.shape
+    g = _group(Hq, Hkv)
+    a_dq = np.zeros_like(q)
+    a_dk = np.zeros_like(k)
+    a_dv = np.zeros_like(v)
+    rows_all = np.arange(Nq)
+    for b in range(B):
+        for h in range(Hq):
+            kv = h // g
+            K = k[b, :, kv, :]
+            V = v[b, :, kv, :]
+            for r0 in range(0, Nq, PANEL_ROWS):
+                rr = rows_all[r0:r0 + PANEL_ROWS]
+                Q = q[b, rr, h, :]
+                dO = do[b, rr, h, :]
+                S = _scores(Q, K, scale, rr, Nq, causal, window)
+                P, _ = _softmax_stats(S)
+                O = P @ V
+                D = np.sum(dO * O, axis=1)
+                dS = np.abs(_softmax_grad(P, dO @ V.T, D))
+                a_dv[b, :, kv, :] += P.T @ np.abs(dO)
+                a_dq[b, rr, h, :] = scale * (dS @ np.abs(K))
+                a_dk[b, :, kv, :] += scale * (dS.T @ np.abs(Q))
+    return a_dq, a_dk, a_dv
 
 
 def blockwise_forward(q, k, v, scale: float, causal: bool, key_blocks):

@@ -73,10 +73,12 @@ def test_split_differs_only_by_polynomial_rounding(fa, split):
     """Against the all-special-function-unit kernel on the same inputs (Q, K
     with σ = 2, so many probabilities are far from 1). Each exponential moves
     by at most the polynomial's relative error (7.5e-5) plus ex2.approx's
-    (2^-22); the bf16 rounding of P before the P V GEMM can then flip by one
-    bf16 ulp (2^-8 relative). So, with S_ic = sum_j P_ij |V_jc| (the oracle's
-    attention of |V|): |dO_ic| <= (7.5e-5 + 2^-8) S_ic + one bf16 ulp of O,
-    and LSE moves by at most about 1e-4 (l sums the fp32 probabilities)."""
+    (2^-22), in the numerator P V and in the row sum l alike (2 x 7.5e-5);
+    the bf16 rounding of P before the P V GEMM can then flip by one bf16 ulp
+    (at most 2^-7 of the value). So, with S_ic = sum_j P_ij |V_jc| (the
+    oracle's attention of |V|): |dO_ic| <= (1.5e-4 + 2^-7) S_ic + one bf16
+    ulp of O, and LSE moves by at most about 1e-4 (l sums the fp32
+    probabilities)."""
     B, H, N, d = 1, 4, 640, 128
     x = workloads.make_inputs(B, H, H, N, N, d, seed=91 + split, sigma_qk=2.0)
     scale = 1.0 / math.sqrt(d)
@@ -89,7 +91,7 @@ def test_split_differs_only_by_polynomial_rounding(fa, split):
         s_abs, _ = attn_ref.forward(qn, kn, np.abs(vn), scale, causal)
         a0, a1 = to64(o0), to64(o1)
         ulp = np.maximum(np.abs(a0), np.abs(a1)) * 2.0 ** -7
-        bound = (7.5e-5 + 2.0 ** -8) * s_abs + ulp + 1e-6
+        bound = (1.5e-4 + 2.0 ** -7) * s_abs + ulp + 1e-6
         diff = np.abs(a1 - a0)
         assert (diff <= bound).all(), (causal, float((diff - bound).max()))
         assert float(diff.mean()) <= 1e-3, (causal, float(diff.mean()))

@@ -1,7 +1,9 @@
 """fa_step_host: forward + backward on host buffers, pipelined over the
 batch (inputs in on one copy stream, compute on the caller's stream,
 results out on another). Checked through the C ABI element by element
-against the fp64 oracle (O, LSE, dQ, dK, dV within the parity tolerances),
+against the fp64 oracle (O, LSE within the parity tolerances; dQ, dK, dV
+within them plus half a bf16 ulp of the value, as these GQA gradients
+exceed |x| = 4),
 and against fa_fwd + fa_bwd on device buffers for the same inputs: O and LSE
 bit for bit (each row is computed by the same kernel either way), the
 gradients within the backward's tolerance (dQ is summed in fp32 in a
@@ -13,7 +15,7 @@ import torch
 
 import workloads
 from oracle import attn_ref
-from tests.gpu_util import assert_close, assert_lse, to64
+from tests.gpu_util import assert_close, assert_close_scaled, assert_lse, to64
 
 pytestmark = pytest.mark.gpu
 
@@ -68,5 +70,8 @@ def test_step_host_matches_device_calls(fa, case, pinned):
     ro, rlse = attn_ref.forward(*xs[:3], scale, causal)
     assert_close("o vs oracle", to64(outs["o"]), ro)
     assert_lse(to64(outs["lse"]), rlse)
+    # gradients of these GQA cases reach |x| > 4 (dV of the first keys sums
+    # over every query of the group), where output rounding alone can pass
+    # 2e-2: the bound grows with the value (assert_close_scaled)
     for name, ref in zip(("dq", "dk", "dv"), attn_ref.backward(*xs, scale, causal)):
-        assert_close(f"{name} vs oracle", to64(outs[name]), ref)
+        assert_close_scaled(f"{name} vs oracle", to64(outs[name]), ref)

@@ -443,3 +443,65 @@ def test_negative_scale_is_positive_scale_with_negated_keys():
             w = [math.exp(t - m) for t in s]
             ref = sum(wj * v[0, j, 1] for j, wj in enumerate(w)) / sum(w)
             np.testing.assert_allclose(o1[0, i, 1], ref, atol=1e-12)
+
+
+def brute_abs_terms(q, k, v, do, scale, causal):
+    """backward_abs_terms by scalar loops (math.fsum), with D_i formed as
+    sum_j P_ij dP_ij (equal to sum_c dO_ic O_ic in exact arithmetic)."""
+    B, Nq, Hq, d = q.shape
+    _, Nk, Hkv, _ = k.shape
+    g = Hq // Hkv
+    a_dq, a_dk, a_dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    for b in range(B):
+        for h in range(Hq):
+            kv = h // g
+            for i in range(Nq):
+                keys = [j for j in range(Nk) if seen(i, j, Nq, Nk, causal, None)]
+                if not keys:
+                    continue
+                logits = [scale * math.fsum(q[b, i, h, c] * k[b, j, kv, c] for c in range(d)) for j in keys]
+                top = max(logits)
+                w = [math.exp(s - top) for s in logits]
+                tot = math.fsum(w)
+                P = [x / tot for x in w]
+                dP = [math.fsum(do[b, i, h, c] * v[b, j, kv, c] for c in range(d)) for j in keys]
+                D = math.fsum(p * dp for p, dp in zip(P, dP))
+                dS = [abs(p * (dp - D)) for p, dp in zip(P, dP)]
+                for c in range(d):
+                    a_dq[b, i, h, c] = scale * math.fsum(s * abs(k[b, j, kv, c]) for s, j in zip(dS, keys))
+                for t, j in enumerate(keys):
+                    for c in range(d):
+                        a_dk[b, j, kv, c] += scale * dS[t] * abs(q[b, i, h, c])
+                        a_dv[b, j, kv, c] += P[t] * abs(do[b, i, h, c])
+    return a_dq, a_dk, a_dv
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_abs_terms_brute_force(causal):
+    rng = np.random.default_rng(12)
+    B, Hq, Hkv, N, d = 1, 4, 2, 9, 5
+    q, k, v, do = (rng.normal(size=(B, N, h, d)) * 1.5 for h in (Hq, Hkv, Hkv, Hq))
+    got = attn_ref.backward_abs_terms(q, k, v, do, 0.7, causal)
+    want = brute_abs_terms(q, k, v, do, 0.7, causal)
+    for g_, w_ in zip(got, want):
+        np.testing.assert_allclose(g_, w_, rtol=1e-10, atol=1e-12)
+
+
+def test_backward_abs_terms_bound_a_perturbed_ds():
+    """Rounding each dS_ij (P_ij) with relative error up to e moves dQ, dK
+    (dV) by at most e times the terms: checked on a direct fp64 computation
+    with random perturbations of the largest allowed size."""
+    rng = np.random.default_rng(13)
+    N, d, scale, e = 12, 6, 0.5, 2.0 ** -8
+    q, k, v, do = (rng.normal(size=(1, N, 1, d)) * 2.0 for _ in range(4))
+    a_dq, a_dk, a_dv = attn_ref.backward_abs_terms(q, k, v, do, scale, True)
+    Q, K, V, dO = q[0, :, 0], k[0, :, 0], v[0, :, 0], do[0, :, 0]
+    P = attn_ref.probabilities(Q, K, scale, True)
+    dP = dO @ V.T
+    dS = P * (dP - np.sum(P * dP, axis=1, keepdims=True))
+    for _ in range(20):
+        eps = e * rng.choice([-1.0, 1.0], size=dS.shape)
+        dS2, P2 = dS * (1 + eps), P * (1 + eps)
+        assert np.all(np.abs(scale * (dS2 - dS) @ K) <= e * a_dq[0, :, 0] + 1e-12)
+        assert np.all(np.abs(scale * (dS2 - dS).T @ Q) <= e * a_dk[0, :, 0] + 1e-12)
+        assert np.all(np.abs((P2 - P).T @ dO) <= e * a_dv[0, :, 0] + 1e-12)

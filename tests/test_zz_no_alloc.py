@@ -18,7 +18,7 @@ import torch
 
 import workloads
 from oracle import attn_ref
-from tests.gpu_util import assert_close, to64
+from tests.gpu_util import assert_close, assert_close_scaled, to64
 
 pytestmark = pytest.mark.gpu
 
@@ -61,7 +61,7 @@ def test_noalloc_matches_oracle_and_fa_bwd_twice(fa):
         got, ref, oracle = both_paths(fa, B, Hq, Hkv, Nq, Nk, d, causal, seed)
         for name, g, r, o in zip(("dq", "dk", "dv"), got, ref, oracle):
             assert torch.isfinite(g).all(), name
-            assert_close(f"{name} vs oracle", to64(g), o)
+            assert_close_scaled(f"{name} vs oracle", to64(g), o)  # GQA dV passes |x| = 4
             assert_close(f"{name} vs fa_bwd", to64(g), to64(r))
 
 
