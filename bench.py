@@ -718,6 +718,38 @@ def run_profile_target(args):
         raise RuntimeError("device status not OK")
 
 
+def run_exp2_split_sweep(args):
+    """The d = 128 forward workloads timed with each exp2 split (fa_tune
+    FA_TUNE_EXP2_SPLIT = 0, 8, 4, 2, 1): median of 10 calls after 3 warm-ups,
+    L2 flushed before each, inputs resident. Prints one JSON object; no
+    bench line."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import exact_attention_99_gb300 as fa
+    fa.fa_debug_set(0, 0)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    out = {}
+    for w in workloads.WORKLOADS[1:4]:
+        x = workloads.workload_inputs(w)
+        q, k, v = (x[n].cuda() for n in ("q", "k", "v"))
+        o = torch.empty_like(q)
+        lse = torch.empty((w.B, w.Hq, w.Nq), device="cuda", dtype=torch.float32)
+        a = (w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.d, w.scale, int(w.causal))
+        r = {}
+        for sp in (0, 8, 4, 2, 1):
+            if fa.fa_tune(fa.TUNE_EXP2_SPLIT, sp):
+                raise RuntimeError("fa_tune failed")
+            ms = time_one(lambda: fa.fa_fwd(q, k, v, o, lse, *a), flush, reps=10)
+            r[str(sp)] = {"ms": round(ms, 4), "tflops": round(w.fwd_flops() / ms / 1e9, 1)}
+        fa.fa_tune(fa.TUNE_EXP2_SPLIT, 0)
+        out[w.name] = r
+        del q, k, v, o, lse
+    if fa.fa_get_status() != 0:
+        raise RuntimeError("device status not OK")
+    print(json.dumps(out), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -728,9 +760,12 @@ def main():
     ap.add_argument("--profile-workload", default=None, help="profiling target: run one workload's pass only")
     ap.add_argument("--profile-pass", choices=["fwd", "fwd8", "bwd"], default="fwd")
     ap.add_argument("--exp2-split", type=int, default=0, help="profiling target: forward exp2 split (fa_tune)")
+    ap.add_argument("--exp2-split-sweep", action="store_true", help="time the d = 128 forwards for each exp2 split")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
-    if args.profile_workload:
+    if args.exp2_split_sweep:
+        run_exp2_split_sweep(args)
+    elif args.profile_workload:
         run_profile_target(args)
     elif args.impl == "reference":
         run_reference(args)

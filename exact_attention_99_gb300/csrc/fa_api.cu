@@ -399,32 +399,38 @@ extern "C" int fa_step_host(const void* q, const void* k, const void* v, const v
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaStream_t cs[2 * kCopyLanes];
   if (!copy_streams(cs)) return FA_ERR_LAUNCH;
-  // device copy of one batch element: q, dout, o, dq [Nq, Hq, d]; k, v, dk,
-  // dv [Nk, Hkv, d]; lse [Hq, Nq] padded to 16 bytes
-  const size_t bq = size_t(Nq) * Hq * d * 2, bk = size_t(Nk) * Hkv * d * 2, nl = size_t(Hq) * Nq;
+  // Chunks: one batch element each; a batch of one element is cut into two
+  // halves of its kv heads (each with its query heads) when Hkv is even, so
+  // that copies and compute still overlap. A chunk is a problem of its own
+  // (B = 1, hq query heads, hk kv heads) in contiguous device buffers.
+  const int C = (B == 1 && Hkv % 2 == 0) ? 2 : 1;  // kv-head slices per batch element
+  const int hk = Hkv / C, hq = Hq / C;
+  const size_t e2 = 2;  // bf16
+  const size_t bq = size_t(Nq) * hq * d * e2, bk = size_t(Nk) * hk * d * e2, nl = size_t(hq) * Nq;
   const size_t bl = (nl * 4 + 15) & ~size_t(15);
   const size_t per = 4 * bq + 4 * bk + bl;
+  const int n_chunks = B * C;
   cudaMemPool_t pool = workspace_pool();
   void* ws = nullptr;
-  if (pool == nullptr || cudaMallocFromPoolAsync(&ws, per * size_t(B), pool, s) != cudaSuccess) {
+  if (pool == nullptr || cudaMallocFromPoolAsync(&ws, per * size_t(n_chunks), pool, s) != cudaSuccess) {
     cudaGetLastError();
     return FA_ERR_ALLOC;
   }
-  // events: [0] start; one set per batch element, reused for every element
-  // (each record is waited on before it is recorded again): per copy lane
-  // "q, k, v in" and "dout in", then "forward done" and "backward done";
-  // then one "done" per copy stream
-  const size_t per_b = 2 * kCopyLanes + 2;
-  std::vector<cudaEvent_t> ev(1 + per_b + 2 * kCopyLanes, nullptr);
+  // events: [0] start; one set per chunk, reused for every chunk (each
+  // record is waited on before it is recorded again): per copy lane "q, k, v
+  // in" and "dout in", then "forward done" and "backward done"; then one
+  // "done" per copy stream
+  const size_t per_c = 2 * kCopyLanes + 2;
+  std::vector<cudaEvent_t> ev(1 + per_c + 2 * kCopyLanes, nullptr);
   bool ok = true;
   for (auto& e : ev) ok = ok && cudaEventCreateWithFlags(&e, cudaEventDisableTiming) == cudaSuccess;
   if (ok) {
     ok = cudaEventRecord(ev[0], s) == cudaSuccess;
     for (int i = 0; i < 2 * kCopyLanes && ok; ++i) ok = cudaStreamWaitEvent(cs[i], ev[0], 0) == cudaSuccess;
   }
-  const auto* hq = static_cast<const uint8_t*>(q);
-  const auto* hk = static_cast<const uint8_t*>(k);
-  const auto* hv = static_cast<const uint8_t*>(v);
+  const auto* hq_ = static_cast<const uint8_t*>(q);
+  const auto* hk_ = static_cast<const uint8_t*>(k);
+  const auto* hv_ = static_cast<const uint8_t*>(v);
   const auto* hdo = static_cast<const uint8_t*>(dout);
   auto* ho = static_cast<uint8_t*>(o);
   auto* hl = reinterpret_cast<uint8_t*>(lse);
@@ -432,52 +438,71 @@ extern "C" int fa_step_host(const void* q, const void* k, const void* v, const v
   auto* hdk = static_cast<uint8_t*>(dk);
   auto* hdv = static_cast<uint8_t*>(dv);
   const cudaMemcpyKind h2d = cudaMemcpyHostToDevice, d2h = cudaMemcpyDeviceToHost;
-  // one copy, split in kCopyLanes contiguous pieces over the copy streams of one direction
-  auto copy = [&](void* dst, const void* src, size_t bytes, cudaMemcpyKind kind, int dir) -> bool {
-    const size_t piece = ((bytes + kCopyLanes - 1) / kCopyLanes + 15) & ~size_t(15);
+  // rows x (h heads of d) bf16 between a [rows, H, d] host tensor (starting
+  // at head h0) and a contiguous [rows, h, d] device buffer: one 2-D copy
+  // (plain 1-D when the slice is the whole row), split in kCopyLanes
+  // contiguous pieces of rows over the copy streams of one direction
+  auto copy_heads = [&](uint8_t* dev, uint8_t* host, int rows, int H, int h0, int h, cudaMemcpyKind kind,
+                        int dir) -> bool {
+    const size_t w = size_t(h) * d * e2, pitch = size_t(H) * d * e2;
+    const int piece = (rows + kCopyLanes - 1) / kCopyLanes;
     for (int l = 0; l < kCopyLanes; ++l) {
-      const size_t off = piece * size_t(l);
-      if (off >= bytes) break;
-      const size_t n = bytes - off < piece ? bytes - off : piece;
-      if (cudaMemcpyAsync(static_cast<uint8_t*>(dst) + off, static_cast<const uint8_t*>(src) + off, n, kind,
-                          cs[2 * l + dir]) != cudaSuccess)
-        return false;
+      const int r0 = piece * l;
+      if (r0 >= rows) break;
+      const int nr = rows - r0 < piece ? rows - r0 : piece;
+      uint8_t* hp = host + size_t(r0) * pitch + size_t(h0) * d * e2;
+      uint8_t* dp = dev + size_t(r0) * w;
+      const cudaError_t e =
+          w == pitch ? cudaMemcpyAsync(kind == h2d ? dp : hp, kind == h2d ? hp : dp, w * nr, kind, cs[2 * l + dir])
+                     : (kind == h2d ? cudaMemcpy2DAsync(dp, w, hp, pitch, w, nr, kind, cs[2 * l + dir])
+                                    : cudaMemcpy2DAsync(hp, pitch, dp, w, w, nr, kind, cs[2 * l + dir]));
+      if (e != cudaSuccess) return false;
     }
     return true;
   };
-  // batch element b: its inputs go in while b-1 computes on the caller's
-  // stream and the results of b-2 come back
-  for (int b = 0; b < B && ok; ++b) {
-    uint8_t* w = static_cast<uint8_t*>(ws) + per * size_t(b);
+  auto in = [&](uint8_t* dev, const uint8_t* host, int rows, int H, int h0, int h) {
+    return copy_heads(dev, const_cast<uint8_t*>(host), rows, H, h0, h, h2d, 0);
+  };
+  auto out = [&](uint8_t* host, uint8_t* dev, int rows, int H, int h0, int h) {
+    return copy_heads(dev, host, rows, H, h0, h, d2h, 1);
+  };
+  // chunk c: its inputs go in while chunk c-1 computes on the caller's
+  // stream and the results of chunk c-2 come back
+  for (int c = 0; c < n_chunks && ok; ++c) {
+    const int b = c / C, g = c - b * C;
+    const int q0 = g * hq, k0 = g * hk;  // first query / kv head of the chunk
+    uint8_t* w = static_cast<uint8_t*>(ws) + per * size_t(c);
     uint8_t *wq = w, *wdo = w + bq, *wo = w + 2 * bq, *wdq = w + 3 * bq;
     uint8_t *wk = w + 4 * bq, *wv = wk + bk, *wdk = wk + 2 * bk, *wdv = wk + 3 * bk;
     float* wl = reinterpret_cast<float*>(wk + 4 * bk);
-    const size_t b_ = size_t(b);
-    cudaEvent_t* eb = ev.data() + 1;
+    const size_t qoff = size_t(b) * Nq * Hq * d * e2, koff = size_t(b) * Nk * Hkv * d * e2;
+    cudaEvent_t* ec = ev.data() + 1;
     // the forward needs q, k, v; dout follows while it runs
-    ok = copy(wq, hq + b_ * bq, bq, h2d, 0) && copy(wk, hk + b_ * bk, bk, h2d, 0) && copy(wv, hv + b_ * bk, bk, h2d, 0);
+    ok = in(wq, hq_ + qoff, Nq, Hq, q0, hq) && in(wk, hk_ + koff, Nk, Hkv, k0, hk) &&
+         in(wv, hv_ + koff, Nk, Hkv, k0, hk);
     for (int l = 0; l < kCopyLanes && ok; ++l)
-      ok = cudaEventRecord(eb[l], cs[2 * l]) == cudaSuccess && cudaStreamWaitEvent(s, eb[l], 0) == cudaSuccess;
-    ok = ok && copy(wdo, hdo + b_ * bq, bq, h2d, 0);
-    for (int l = 0; l < kCopyLanes && ok; ++l) ok = cudaEventRecord(eb[kCopyLanes + l], cs[2 * l]) == cudaSuccess;
+      ok = cudaEventRecord(ec[l], cs[2 * l]) == cudaSuccess && cudaStreamWaitEvent(s, ec[l], 0) == cudaSuccess;
+    ok = ok && in(wdo, hdo + qoff, Nq, Hq, q0, hq);
+    for (int l = 0; l < kCopyLanes && ok; ++l) ok = cudaEventRecord(ec[kCopyLanes + l], cs[2 * l]) == cudaSuccess;
     if (!ok) break;
-    const Problem p{wq, wk, wv, 1, Hq, Hkv, Nq, Nk, d, scale, causal};
-    ok = launch_fwd(p, wo, wl, s) == cudaSuccess && cudaEventRecord(eb[2 * kCopyLanes], s) == cudaSuccess;
+    const Problem p{wq, wk, wv, 1, hq, hk, Nq, Nk, d, scale, causal};
+    ok = launch_fwd(p, wo, wl, s) == cudaSuccess && cudaEventRecord(ec[2 * kCopyLanes], s) == cudaSuccess;
     // o and lse go out while the backward runs
     for (int l = 0; l < kCopyLanes && ok; ++l)
-      ok = cudaStreamWaitEvent(cs[2 * l + 1], eb[2 * kCopyLanes], 0) == cudaSuccess;
-    ok = ok && copy(ho + b_ * bq, wo, bq, d2h, 1) && copy(hl + b_ * nl * 4, wl, nl * 4, d2h, 1);
-    for (int l = 0; l < kCopyLanes && ok; ++l) ok = cudaStreamWaitEvent(s, eb[kCopyLanes + l], 0) == cudaSuccess;
+      ok = cudaStreamWaitEvent(cs[2 * l + 1], ec[2 * kCopyLanes], 0) == cudaSuccess;
+    ok = ok && out(ho + qoff, wo, Nq, Hq, q0, hq) &&
+         cudaMemcpyAsync(hl + (size_t(b) * Hq + q0) * Nq * 4, wl, nl * 4, d2h, cs[1]) == cudaSuccess;
+    for (int l = 0; l < kCopyLanes && ok; ++l) ok = cudaStreamWaitEvent(s, ec[kCopyLanes + l], 0) == cudaSuccess;
     ok = ok && bwd_pooled(p, wo, wl, wdo, wdq, wdk, wdv, stream) == FA_OK &&
-         cudaEventRecord(eb[2 * kCopyLanes + 1], s) == cudaSuccess;
+         cudaEventRecord(ec[2 * kCopyLanes + 1], s) == cudaSuccess;
     for (int l = 0; l < kCopyLanes && ok; ++l)
-      ok = cudaStreamWaitEvent(cs[2 * l + 1], eb[2 * kCopyLanes + 1], 0) == cudaSuccess;
-    ok = ok && copy(hdq + b_ * bq, wdq, bq, d2h, 1) && copy(hdk + b_ * bk, wdk, bk, d2h, 1) &&
-         copy(hdv + b_ * bk, wdv, bk, d2h, 1);
+      ok = cudaStreamWaitEvent(cs[2 * l + 1], ec[2 * kCopyLanes + 1], 0) == cudaSuccess;
+    ok = ok && out(hdq + qoff, wdq, Nq, Hq, q0, hq) && out(hdk + koff, wdk, Nk, Hkv, k0, hk) &&
+         out(hdv + koff, wdv, Nk, Hkv, k0, hk);
   }
   // the caller's stream waits for every copy stream, then frees the workspace
   for (int i = 0; i < 2 * kCopyLanes; ++i) {
-    cudaEvent_t e = ev[1 + per_b + i];
+    cudaEvent_t e = ev[1 + per_c + i];
     if (e != nullptr && cudaEventRecord(e, cs[i]) == cudaSuccess) cudaStreamWaitEvent(s, e, 0);
   }
   const bool freed = cudaFreeAsync(ws, s) == cudaSuccess;

@@ -100,7 +100,7 @@ def flip_terms(qn, kn, vd, qd, kd, scale, causal, incoherent):
     for b in range(B):
         for h in range(Hq):
             kv = h // g
-            f = scale * sq[b, h] * sk[b, kv]
+            f = abs(scale) * sq[b, h] * sk[b, kv]
             kmax = np.abs(k8[b, :, kv, :]).max(axis=0)
             dq = (tq[b, :, h, :] * stq[b, :, h, :] * kmax).sum(axis=1)     # [Nq]
             qmax = np.abs(q8[b, :, h, :]).max(axis=1)                     # [Nq]

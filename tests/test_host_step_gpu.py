@@ -1,6 +1,7 @@
 """fa_step_host: forward + backward on host buffers, pipelined over the
 batch (inputs in on one copy stream, compute on the caller's stream,
-results out on another). Checked through the C ABI element by element
+results out on another; a one-element batch is cut into two halves of its
+kv heads). Checked through the C ABI element by element
 against the fp64 oracle (O, LSE within the parity tolerances; dQ, dK, dV
 within them plus half a bf16 ulp of the value, as these GQA gradients
 exceed |x| = 4),
@@ -34,7 +35,9 @@ CASES = [
     # B, Hq, Hkv, Nq, Nk, d, causal
     (3, 4, 2, 300, 300, 128, True),
     (2, 2, 2, 200, 520, 64, False),
-    (1, 4, 4, 256, 256, 128, False),
+    (1, 4, 4, 256, 256, 128, False),  # one batch element: two chunks of two kv heads (2-D copies)
+    (1, 8, 2, 300, 420, 128, True),   # one batch element, GQA: two chunks of one kv head and four query heads
+    (1, 3, 3, 129, 129, 64, True),    # odd Hkv: one chunk
 ]
 
 
