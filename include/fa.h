@@ -143,10 +143,12 @@ int fa_bwd_window(const void* q, const void* k, const void* v, const void* o, co
  * and results), with every pointer a host address:
  *   in : q [B,Nq,Hq,d], k, v [B,Nk,Hkv,d], dout [B,Nq,Hq,d] (bf16)
  *   out: o [B,Nq,Hq,d] (bf16), lse [B,Hq,Nq] (fp32), dq, dk, dv (bf16).
- * The batch is processed one element at a time and pipelined: the inputs of
- * element b are copied in on a library-owned copy stream while element b-1
- * computes on `stream` and the results of element b-2 are copied out on a
- * second copy stream. The call only enqueues; `stream` is ordered after all
+ * The batch is processed in chunks and pipelined: the inputs of chunk c are
+ * copied in on a library-owned copy stream while chunk c-1 computes on
+ * `stream` and the results of chunk c-2 are copied out on a second copy
+ * stream. A chunk is one batch element; a batch of one element with an even
+ * Hkv is cut into two halves of its kv heads (each with its query heads),
+ * copied as 2-D slices of the head dimension. The call only enqueues; `stream` is ordered after all
  * of it, so synchronise `stream` before reading the outputs, and keep every
  * host buffer alive (and the inputs unchanged) until then. Page-locked host
  * memory gives asynchronous, full-speed copies; pageable memory works but
