@@ -83,11 +83,3 @@ def workload_inputs(w: Workload, with_dout: bool | None = None) -> dict:
     if with_dout is None:
         with_dout = w.direction == "bwd"
     return make_inputs(w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.d, w.seed, w.sigma_qk, w.sigma_v, with_dout)
-
-
-def shard(n_units: int, rank: int, world: int) -> range:
-    """Contiguous block of ``n_units`` owned by ``rank`` (sizes differ by at most one)."""
-    base, extra = divmod(n_units, world)
-    lo = rank * base + min(rank, extra)
-    hi = lo + base + (1 if rank < extra else 0)
-    return range(lo, hi)
