@@ -19,16 +19,17 @@
 //              tiles (j, n-1-j) when causal, so every CTA has the same work --
 //              looping over the query heads of the GQA group x 128-row query
 //              tiles that see the tile.
-//     warps 0-3  compute: one thread per key row; P^T = 2^(S^T*scale*log2e -
-//                LSE*log2e), dS^T = P^T o (dP^T - D)
-//     warps 4-7  dQ drain and the dK/dV epilogue. d = 128: dQ^T leaves TMEM
+//     warps 0-7  compute: two warps per lane quarter, each thread one key
+//                row and 64 of the tile's 128 query columns; P^T =
+//                2^(S^T*scale*log2e - LSE*log2e), dS^T = P^T o (dP^T - D)
+//     warps 8-11 dQ drain and the dK/dV epilogue. d = 128: dQ^T leaves TMEM
 //                into a shared-memory staging buffer and is added to the fp32
 //                accumulator by TMA bulk reductions; d = 64: coalesced fp32
 //                reductions.
 //     Shared memory: K and V tiles (resident), a 2-slot Q ring, a 1-slot dO
 //     ring (its last reader, dV, runs early in each step), the dS^T tile,
 //     the dQ staging buffer, LSE/D vectors.
-//     warp 8     TMA producer, warp 9 MMA issuer, warps 10-11 idle
+//     warp 12    TMA producer, warp 13 MMA issuer, warps 14-15 idle
 //     TMEM: S^T [0,128) with P^T (bf16) over its first 64 columns;
 //           dP^T [128,256), reused for dQ^T once read; dV [256,256+d);
 //           dK [256+d, 256+2d).
@@ -50,7 +51,7 @@
 namespace fa {
 namespace bwd {
 
-constexpr int kThreads = 384;
+constexpr int kThreads = 512;
 
 template <int D>
 struct Cfg {
@@ -243,12 +244,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&ctl.do_empty, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ctl.vec_full[i], 1);
-      mbar_init(&ctl.vec_empty[i], 4);
+      mbar_init(&ctl.vec_empty[i], 8);
     }
     mbar_init(&ctl.s_full, 1);
-    mbar_init(&ctl.p_full, 4);
+    mbar_init(&ctl.p_full, 8);
     mbar_init(&ctl.dp_full, 1);
-    mbar_init(&ctl.ds_full, 4);
+    mbar_init(&ctl.ds_full, 8);
     mbar_init(&ctl.dq_full, 1);
     mbar_init(&ctl.dq_empty, 4);
     mbar_init(&ctl.acc_full, 1);
@@ -257,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&ctl.drain, 1);
     fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == 13) {
     tmem_alloc(&ctl.tmem_base, 512);
     tmem_relinquish();
   }
@@ -272,10 +273,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sDs = smem + C::kOffDs;
   float* sVec = reinterpret_cast<float*>(smem + C::kOffVec);
 
-  if (wg == 0) {
+  if (wg <= 1) {
     // ------------------------------------------------------------ compute
-    setmaxnreg_inc<232>();
+    // Two warps per lane quarter: warp w (0-7) takes key rows of lane
+    // quarter w % 4 and query columns [64 h, 64 h + 64) with h = w / 4. P and
+    // dS are elementwise given the row's LSE and D, so the halves need no
+    // exchange; two warps per SMSP hide each other's latencies.
+    // Registers (launch: 512 threads x 128): compute 8 warps x 136, dQ drain
+    // 4 x 144, producer / MMA / idle 4 x 96 = 2048 x 32 = the 65536 of the SM.
+    setmaxnreg_inc<136>();
     const int row = ((warp & 3) << 5) + lane;  // key row within the tile
+    const int c0 = (warp >> 2) * 64;          // first query column of this warp
     const uint32_t t_lane = tmem + (uint32_t(warp & 3) << 21);
     const int off = p.Nk - p.Nq;
     const float sl = p.scale_log2;
@@ -289,62 +297,64 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int st = 0; st < I.steps && ok; ++st, ++g) {
         const int it = I.i0 + st % I.nq;  // query tile
         const int vs = g & 1;
-        const float* lse2 = sVec + vs * 256;
-        const float* dlt = lse2 + 128;
+        const float* lse2 = sVec + vs * 256 + c0;
+        const float* dlt = sVec + vs * 256 + 128 + c0;
         if (!mbar_wait_bounded(&ctl.vec_full[vs], (g >> 1) & 1, abort_flag, LIM)) { ok = false; break; }
         if (threadIdx.x == 0) trace_stamp(p.trace, g, 5);
         if (!mbar_wait_bounded(&ctl.s_full, ph_s, abort_flag, LIM)) { ok = false; break; }
         ph_s ^= 1;
         if (threadIdx.x == 0) trace_stamp(p.trace, g, 6);
         tc_fence_after();
-        uint32_t x[128];
+        float pv[64];
+        {
+          uint32_t x[64];
+          tmem_ld32(t_lane + C::kColS + c0, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
+          tmem_ld32(t_lane + C::kColS + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
+          tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-          tmem_ld32(t_lane + C::kColS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&x[c * 32]));
-        tmem_wait_ld();
+          for (int c = 0; c < 64; c += 4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(lse2 + c);
+            const uint64_t y0 = ffma2(pack2(u2f(x[c]), u2f(x[c + 1])), pack2(sl, sl), pack2(-l4.x, -l4.y));
+            const uint64_t y1 = ffma2(pack2(u2f(x[c + 2]), u2f(x[c + 3])), pack2(sl, sl), pack2(-l4.z, -l4.w));
+            float a0, a1, a2, a3;
+            unpack2(y0, a0, a1);
+            unpack2(y1, a2, a3);
+            pv[c] = ex2_mufu(a0);
+            pv[c + 1] = ex2_mufu(a1);
+            pv[c + 2] = ex2_mufu(a2);
+            pv[c + 3] = ex2_mufu(a3);
+          }
+        }
         // query row q (column c = q - it*128) sees this key iff
         // key - off - wr <= q <= key - off + wl: mask tiles that cross an edge
         const int wl = win_l<WIN>(p), wr = win_r<WIN>(p);
         const bool need_mask = CAUSAL && ((wr >= 0 && it * 128 < I.j * 128 + 127 - off - wr) ||
                                           (wl >= 0 && it * 128 + 127 > I.j * 128 - off + wl));
-        const int qlim = wr >= 0 ? key - off - wr - it * 128 : -(1 << 30);  // columns c < qlim are hidden
-        const int qmax = wl >= 0 ? key - off + wl - it * 128 : (1 << 30);   // and columns c > qmax
-        float pv[128];
-#pragma unroll
-        for (int c = 0; c < 128; c += 4) {
-          const float4 l4 = *reinterpret_cast<const float4*>(lse2 + c);
-          const uint64_t y0 = ffma2(pack2(u2f(x[c]), u2f(x[c + 1])), pack2(sl, sl), pack2(-l4.x, -l4.y));
-          const uint64_t y1 = ffma2(pack2(u2f(x[c + 2]), u2f(x[c + 3])), pack2(sl, sl), pack2(-l4.z, -l4.w));
-          float a0, a1, a2, a3;
-          unpack2(y0, a0, a1);
-          unpack2(y1, a2, a3);
-          pv[c] = ex2_mufu(a0);
-          pv[c + 1] = ex2_mufu(a1);
-          pv[c + 2] = ex2_mufu(a2);
-          pv[c + 3] = ex2_mufu(a3);
-        }
         // masking only on diagonal tiles and past-the-end keys, in its own
-        // pass so the common case carries no per-element selects
+        // pass so the common case carries no per-element selects; column
+        // bounds relative to this warp's first column
         if (need_mask || !kvalid) {
-          const int lim = kvalid ? qlim : 128;
+          const int qlim = wr >= 0 ? key - off - wr - it * 128 - c0 : -(1 << 30);  // columns c < qlim are hidden
+          const int lim = kvalid ? qlim : 64;
           if (WIN) {
+            const int qmax = wl >= 0 ? key - off + wl - it * 128 - c0 : (1 << 30);  // and columns c > qmax
             const int top = kvalid ? qmax : -1;
 #pragma unroll
-            for (int c = 0; c < 128; ++c)
+            for (int c = 0; c < 64; ++c)
               if (c < lim || c > top) pv[c] = 0.0f;
           } else {
 #pragma unroll
-            for (int c = 0; c < 128; ++c)
+            for (int c = 0; c < 64; ++c)
               if (c < lim) pv[c] = 0.0f;
           }
         }
         {
-          uint32_t pk[64];
+          uint32_t pk[32];
 #pragma unroll
-          for (int c = 0; c < 64; ++c) pk[c] = pack_bf16x2(pv[2 * c], pv[2 * c + 1]);
+          for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(pv[2 * c], pv[2 * c + 1]);
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
-            tmem_st16(t_lane + C::kColS + c * 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[c * 16]));
+          for (int c = 0; c < 2; ++c)
+            tmem_st16(t_lane + C::kColS + c0 / 2 + c * 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[c * 16]));
         }
         tmem_wait_st();
         tc_fence_before();
@@ -352,31 +362,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (threadIdx.x == 0) trace_stamp(p.trace, g, 7);
         if (lane == 0) mbar_arrive(&ctl.p_full);
 
-        // dS^T = P^T o (dP^T - D)
+        // dS^T = P^T o (dP^T - D), 32 columns per TMEM load
         if (!mbar_wait_bounded(&ctl.dp_full, ph_dp, abort_flag, LIM)) { ok = false; break; }
         ph_dp ^= 1;
         if (threadIdx.x == 0) trace_stamp(p.trace, g, 8);
         tc_fence_after();
 #pragma unroll
-        for (int c0 = 0; c0 < 128; c0 += 64) {
-          uint32_t gg[64];  // two loads in flight per wait
-          tmem_ld32(t_lane + C::kColDP + c0, *reinterpret_cast<uint32_t(*)[32]>(&gg[0]));
-          tmem_ld32(t_lane + C::kColDP + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(&gg[32]));
+        for (int h = 0; h < 64; h += 32) {
+          uint32_t gg[32];
+          tmem_ld32(t_lane + C::kColDP + c0 + h, gg);
           tmem_wait_ld();
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {  // 8 columns = one 16-byte unit
-            const int c = c0 + u * 8;
+          for (int u = 0; u < 4; ++u) {  // 8 columns = one 16-byte unit
+            const int c = h + u * 8;
             const float4 d0 = *reinterpret_cast<const float4*>(dlt + c);
             const float4 d1 = *reinterpret_cast<const float4*>(dlt + c + 4);
             const float dd[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
             uint32_t pk[4];
 #pragma unroll
             for (int e = 0; e < 8; e += 2) {
-              const float s0 = pv[c + e] * (u2f(gg[u * 8 + e]) - dd[e]);
-              const float s1 = pv[c + e + 1] * (u2f(gg[u * 8 + e + 1]) - dd[e + 1]);
+              float s0, s1;
+              unpack2(fmul2(pack2(pv[c + e], pv[c + e + 1]),
+                            fadd2(pack2(u2f(gg[u * 8 + e]), u2f(gg[u * 8 + e + 1])), pack2(-dd[e], -dd[e + 1]))),
+                      s0, s1);
               pk[e >> 1] = pack_bf16x2(s0, s1);
             }
-            *reinterpret_cast<uint4*>(sDs + sw128_off(row, c)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            *reinterpret_cast<uint4*>(sDs + sw128_off(row, c0 + c)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
           }
         }
         fence_proxy_async_smem();
@@ -389,8 +400,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (wg == 1) {
+  } else if (wg == 2) {
     // ------------------------------------------------ dQ drain + epilogue
+    setmaxnreg_inc<144>();
     const int wq = warp & 3;
     const uint32_t t_lane = tmem + (uint32_t(wq) << 21);
     const int lr = (wq << 5) + lane;  // TMEM lane: d index (D=128) or query row (D=64)
@@ -404,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int h = w.kvh * p.group + st / I.nq;
         if (!mbar_wait_bounded(&ctl.dq_full, ph_dq, abort_flag, LIM)) { ok = false; break; }
         ph_dq ^= 1;
-        if (threadIdx.x == 128) trace_stamp(p.trace, g, 10);
+        if (threadIdx.x == 256) trace_stamp(p.trace, g, 10);
         tc_fence_after();
         if (D == 128) {
           uint32_t v[128];
@@ -415,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&ctl.dq_empty);
-          if (threadIdx.x == 128) trace_stamp(p.trace, g, 11);
+          if (threadIdx.x == 256) trace_stamp(p.trace, g, 11);
           // dQ^T: lane = d index, column = query row of the tile. Stage it as
           // 128-byte-swizzled boxes of [32 d rows][32 q] fp32, two boxes per
           // warp and half-tile, and add each box into the accumulator with a
@@ -445,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               bulk_commit();
             }
           }
-          if (threadIdx.x == 128) trace_stamp(p.trace, g, 12);
+          if (threadIdx.x == 256) trace_stamp(p.trace, g, 12);
         } else {
           uint32_t v[64];
 #pragma unroll
@@ -508,12 +520,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (D == 128 && lane == 0) bulk_wait_all();  // the accumulator is complete when the kernel ends
   } else {
-    setmaxnreg_dec<104>();
+    setmaxnreg_dec<96>();
   }
   int total_steps = 0;
 #pragma unroll
   for (int k = 0; k < 2; ++k) total_steps += w.it[k].steps;
-  if (warp == 8) {
+  if (warp == 12) {
     // ------------------------------------------------------- TMA producer
     if (lane == 0 && total_steps > 0) {
       bool ok = true;
@@ -560,7 +572,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         while (globaltimer_ns() - t0 < 1000000ull) __nanosleep(1000);
       }
     }
-  } else if (warp == 9) {
+  } else if (warp == 13) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0 && total_steps > 0) {
       constexpr uint32_t idSS = idesc_bf16_f32(128, 128, 0, 0);     // S^T, dP^T
@@ -666,7 +678,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 9) tmem_dealloc(tmem, 512);
+  if (warp == 13) tmem_dealloc(tmem, 512);
   if (threadIdx.x == 0 && ctl.abort) atomicOr(p.status, kDevTimeout);
 }
 
