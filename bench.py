@@ -397,6 +397,12 @@ def per_config(fa, flush, peak):
         ms = time_one(fwd, flush, stats=st)
         ent = {"fwd_ms": ms, "fwd_min_ms": st["min"], "fwd_tflops": w.fwd_flops() / ms / 1e9}
         ent["fwd_frac_of_peak"] = ent["fwd_tflops"] / peak
+        if w.d == 128:  # the same forward on CTA pairs (cta_group::2)
+            fa.fa_tune(fa.TUNE_CTA_PAIRS, 1)
+            pms = time_one(fwd, flush, stats=st)
+            fa.fa_tune(fa.TUNE_CTA_PAIRS, 0)
+            ent.update({"fwd_pairs_ms": pms, "fwd_pairs_min_ms": st["min"],
+                        "fwd_pairs_tflops": w.fwd_flops() / pms / 1e9})
         if w.direction == "bwd" or w.name == "fwd_b4_h16_n2048_d128" or w.Hkv < w.Hq:
             dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
             bwd = lambda: fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.d, w.scale,
@@ -714,7 +720,7 @@ def run_profile_target(args):
     __graft_entry__.build()
     import exact_attention_99_gb300 as fa
     fa.fa_debug_set(0, 0)
-    if fa.fa_tune(fa.TUNE_EXP2_SPLIT, args.exp2_split):
+    if fa.fa_tune(fa.TUNE_EXP2_SPLIT, args.exp2_split) or fa.fa_tune(fa.TUNE_CTA_PAIRS, int(args.cta_pairs)):
         raise ValueError("bad --exp2-split")
     if args.profile_workload == WINDOW_CASE["name"]:
         c = WINDOW_CASE
@@ -790,6 +796,7 @@ def main():
     ap.add_argument("--profile-pass", choices=["fwd", "fwd8", "bwd"], default="fwd")
     ap.add_argument("--exp2-split", type=int, default=0, help="profiling target: forward exp2 split (fa_tune)")
     ap.add_argument("--exp2-split-sweep", action="store_true", help="time the d = 128 forwards for each exp2 split")
+    ap.add_argument("--cta-pairs", action="store_true", help="profiling target: the d = 128 forward on CTA pairs")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     if args.exp2_split_sweep:

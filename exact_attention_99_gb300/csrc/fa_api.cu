@@ -35,7 +35,7 @@ constexpr int kCopyLanes = 1;
 cudaStream_t g_copy[kMaxDevices][2 * kCopyLanes];
 unsigned* g_status_ptr[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-DebugCfg g_debug = {kDefaultWaitNs, 0, nullptr, nullptr, nullptr, 0};
+DebugCfg g_debug = {kDefaultWaitNs, 0, nullptr, nullptr, nullptr, 0, 0};
 
 int current_device() {
   int dev = -1;
@@ -355,11 +355,19 @@ extern "C" int fa_debug_set(unsigned long long wait_limit_ns, int inject) {
 }
 
 extern "C" int fa_tune(int knob, int value) {
-  if (knob != FA_TUNE_EXP2_SPLIT) return FA_ERR_INVALID_ARG;
-  if (value != 0 && value != 1 && value != 2 && value != 4 && value != 8) return FA_ERR_INVALID_ARG;
-  std::lock_guard<std::mutex> lk(g_mu);
-  g_debug.poly_every = value;
-  return FA_OK;
+  if (knob == FA_TUNE_EXP2_SPLIT) {
+    if (value != 0 && value != 1 && value != 2 && value != 4 && value != 8) return FA_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_debug.poly_every = value;
+    return FA_OK;
+  }
+  if (knob == FA_TUNE_CTA_PAIRS) {
+    if (value != 0 && value != 1) return FA_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_debug.cta_pairs = value;
+    return FA_OK;
+  }
+  return FA_ERR_INVALID_ARG;
 }
 
 extern "C" int fa_profile_events(void* begin, void* end) {

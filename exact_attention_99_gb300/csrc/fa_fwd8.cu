@@ -252,8 +252,10 @@ __global__ void __launch_bounds__(256, 2) fp8_rows_kernel(const __nv_bfloat16* q
 // a swizzled 16 KB shared tile per stage and the P V GEMM reads both
 // operands from shared memory.
 struct E4m3 {
+  static constexpr bool kPair = false;
   static constexpr int D = 128;
   static constexpr int kTileBytes = 128 * D;   // one 128-row e4m3 tile of Q, K or V^T
+  static constexpr int kSlotBytes = kTileBytes;  // a K/V ring slot holds one tile
   static constexpr int kSlots = 8;
   static constexpr int kPTileBytes = 128 * 128;  // e4m3 P of one stage [rows x keys]
   static constexpr int kSmemDyn = (2 + kSlots) * kTileBytes + 2 * kPTileBytes + fwdp::kStgBytes + 1024;

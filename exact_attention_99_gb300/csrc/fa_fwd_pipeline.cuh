@@ -5,7 +5,8 @@
 // loads, where P lives, the GEMM instructions, the per-head scales of the
 // e4m3 path) comes from a policy class `K`:
 //
-//   K::D, K::kTileBytes, K::kSlots, K::kPTileBytes, K::kSmemDyn
+//   K::kPair (CTA pairs, below), K::D, K::kTileBytes (a Q tile),
+//   K::kSlotBytes (a K/V ring slot), K::kSlots, K::kPTileBytes, K::kSmemDyn
 //   K::load_q / load_k / load_v (producer; TMA tile loads onto an mbarrier)
 //   K::Desc, K::make_desc, K::idesc_s, K::idesc_pv, K::issue_s, K::issue_pv
 //   K::PK, K::pack_p, K::store_p, K::publish_p (softmax -> P for the P V GEMM)
@@ -46,6 +47,17 @@
 //     ... PV0(j), S0(j+1), PV1(j), S1(j+1), PV0(j+1), ...
 //   Every mbarrier wait is bounded; on timeout the CTA stops cleanly and
 //   the per-device status word records it.
+//
+// CTA pairs (K::kPair): a cluster of two CTAs runs one unit of 512 query
+// rows. Stage s covers 256 consecutive rows, 128 in each CTA (each CTA keeps
+// its own softmax, correction and epilogue for its rows), and the even CTA
+// alone issues tcgen05.mma with cta_group::2: M = 256 over both CTAs' tensor
+// memory, each CTA holding half of each K tile (64 keys) and half of each V
+// tile (64 of the d columns) at the same shared-memory offset, so one MMA
+// instruction does the work of two and each CTA loads half the K/V bytes.
+// The barriers the issuing CTA waits on (Q and K/V loaded, P stored, O
+// corrected) count the other CTA's arrivals too; its commits arrive on the
+// barriers of both CTAs. Each CTA loads its own tiles (no multicast).
 //
 // exp2 split: the template argument POLY sends one column pair in every
 // POLY of the softmax's exponentials to the fitted polynomial on the FMA
@@ -155,8 +167,12 @@ __device__ __forceinline__ int win_l(const Params& p) { return WIN ? p.wl : -1; 
 template <bool WIN>
 __device__ __forceinline__ int win_r(const Params& p) { return WIN ? p.wr : 0; }
 
-template <bool CAUSAL, bool WIN>
+// A unit is a block of query rows of one (batch, head): two stages of 128
+// rows (256 rows), or with CTA pairs two stages of 256 rows (512 rows, 128 of
+// each stage per CTA). Key ranges are those of a whole stage.
+template <bool CAUSAL, bool WIN, bool PAIR = false>
 __device__ __forceinline__ Unit decode_unit(const Params& p, int item) {
+  constexpr int kStage = PAIR ? 256 : 128;  // query rows per stage
   Unit x;
   int u = item, half = -1;
   if (!CAUSAL && item >= p.n_full) {
@@ -180,13 +196,13 @@ __device__ __forceinline__ Unit decode_unit(const Params& p, int item) {
   x.b = bh / p.Hq;
   x.h = bh - x.b * p.Hq;
   x.kvh = x.h / p.group;
-  x.row0 = mb * 256;
+  x.row0 = mb * 2 * kStage;
   const int off = p.Nk - p.Nq;
   const int nkb = (p.Nk + 127) >> 7;
   int t0[2];
 #pragma unroll
   for (int s = 0; s < 2; ++s) {
-    const int r0 = x.row0 + s * 128;
+    const int r0 = x.row0 + s * kStage;
     x.rows[s] = r0 < p.Nq;
     t0[s] = 0;
     if (!x.rows[s]) {
@@ -195,7 +211,7 @@ __device__ __forceinline__ Unit decode_unit(const Params& p, int item) {
       x.n[s] = nkb;
     } else {
       // keys seen by any row of the stage: [lo, hi]
-      const int rl = min(r0 + 127, p.Nq - 1);
+      const int rl = min(r0 + kStage - 1, p.Nq - 1);
       const int wl = win_l<WIN>(p), wr = win_r<WIN>(p);
       const int lo = wl >= 0 ? max(0, r0 + off - wl) : 0;
       const int hi = wr >= 0 ? min(p.Nk - 1, rl + off + wr) : p.Nk - 1;
@@ -220,10 +236,10 @@ __device__ __forceinline__ Unit decode_unit(const Params& p, int item) {
   return x;
 }
 
-// Static snake order over rounds of gridDim.x units (longest first when
-// causal): CTA c takes unit c in even rounds and G-1-c in odd rounds.
-__device__ __forceinline__ int unit_at(int round, int c) {
-  const int G = gridDim.x;
+// Static snake order over rounds of G units (longest first when causal):
+// worker c (a CTA, or a CTA pair) takes unit c in even rounds and G-1-c in
+// odd rounds.
+__device__ __forceinline__ int unit_at(int round, int c, int G) {
   return round * G + ((round & 1) ? (G - 1 - c) : c);
 }
 
@@ -235,12 +251,14 @@ template <class K, bool CAUSAL, bool WIN, int POLY>
 __device__ __forceinline__ void fwd_body(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                                          const CUtensorMap& tmO, const Params& p) {
   constexpr int D = K::D;
+  constexpr bool PAIR = K::kPair;
+  constexpr int kStage = PAIR ? 256 : 128;  // query rows per stage of a unit
   extern __shared__ uint8_t smem_raw[];
   __shared__ Ctl ctl;  // one per CTA
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;                                 // 2 tiles
-  uint8_t* sKV = smem + 2 * K::kTileBytes;            // kSlots tiles
-  uint8_t* sP = sKV + K::kSlots * K::kTileBytes;      // 2 P tiles (none when P stays in TMEM)
+  uint8_t* sKV = smem + 2 * K::kTileBytes;            // kSlots K/V slots
+  uint8_t* sP = sKV + K::kSlots * K::kSlotBytes;      // 2 P tiles (none when P stays in TMEM)
   uint8_t* sStg = sP + 2 * K::kPTileBytes;            // O staging
 
   const int warp = threadIdx.x >> 5;
@@ -248,6 +266,11 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmQ, const CUtensorM
   const int wg = warp >> 2;
   volatile uint32_t* abort_flag = &ctl.abort;
   const uint64_t LIM = p.wait_limit_ns;
+  // CTA pairs: this CTA's rank in the pair (0 issues the MMAs), the worker
+  // index and the number of workers of the static schedule
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const int worker = PAIR ? int(blockIdx.x >> 1) : int(blockIdx.x);
+  const int n_workers = PAIR ? int(gridDim.x >> 1) : int(gridDim.x);
   if (threadIdx.x == 0) trace_stamp(p.trace, kEv, 0);
 
   if (threadIdx.x == 0) {
@@ -255,9 +278,9 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmQ, const CUtensorM
     for (int s = 0; s < 2; ++s) {
       mbar_init(&ctl.q_full[s], 1);
       mbar_init(&ctl.s_full[s], 1);
-      mbar_init(&ctl.p_full[s], 4);
+      mbar_init(&ctl.p_full[s], PAIR ? 8 : 4);   // softmax warps of both CTAs of a pair
       mbar_init(&ctl.alpha_full[s], 4);
-      mbar_init(&ctl.o_ready[s], 4);
+      mbar_init(&ctl.o_ready[s], PAIR ? 8 : 4);  // correction warps of both CTAs of a pair
       mbar_init(&ctl.o_full[s], 1);
       mbar_init(&ctl.stats_full[s], 4);
       mbar_init(&ctl.stats_empty[s], 4);
@@ -271,8 +294,13 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmQ, const CUtensorM
     fence_mbar_init();
   }
   if (warp == 13) {
-    tmem_alloc(&ctl.tmem_base, 512);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(&ctl.tmem_base, 512);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(&ctl.tmem_base, 512);
+      tmem_relinquish();
+    }
   }
   if (warp == 12 && lane == 0) {
     prefetch_tmap(&tmQ);
@@ -280,9 +308,22 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmQ, const CUtensorM
     prefetch_tmap(&tmV);
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR) {
+    cluster_sync_all();  // both CTAs' barriers are initialised before any remote arrival
+  } else {
+    __syncthreads();
+  }
   tc_fence_after();
   const uint32_t tmem = ctl.tmem_base;
+  // arrival on a barrier that the MMA-issuing CTA waits on: local, or on the
+  // even CTA of a pair
+  auto arrive_issuer = [&](uint64_t* bar) {
+    if constexpr (PAIR) {
+      mbar_arrive_cluster(mapa_shared(smem_u32(bar), 0));
+    } else {
+      mbar_arrive(bar);
+    }
+  };
   if (threadIdx.x == 0) trace_stamp(p.trace, kEv, 1);
 
   if (wg <= 1) {
@@ -296,17 +337,17 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmQ, const CUtensorM
     int blk = 0;  // running key-tile counter (trace only)
     bool ok = true;
     for (int rnd = 0; ok; ++rnd) {
-      const int u = unit_at(rnd, blockIdx.x);
+      const int u = unit_at(rnd, worker, n_workers);
       if (u >= p.n_items) break;
-      const Unit un = decode_unit<CAUSAL, WIN>(p, u);
+      const Unit un = decode_unit<CAUSAL, WIN, PAIR>(p, u);
       const int n = un.n[s];
       const int blk0 = blk;
       blk += un.nb;
       if (n == 0) continue;
       const float sl = K::logit_scale(p, un);
-      const int rg = un.row0 + s * 128 + row;  // global query row
+      const int r0 = un.row0 + s * kStage + 128 * int(rank), rl = min(r0 + 127, p.Nq - 1);  // this CTA's rows
+      const int rg = r0 + row;  // global query row
       const int off = p.Nk - p.Nq;
-      const int r0 = un.row0 + s * 128, rl = min(r0 + 127, p.Nq - 1);  // the stage's rows
       const int wl = win_l<WIN>(p), wr = win_r<WIN>(p);
       float m_run = -INFINITY, l_run = 0.0f;
       for (int j = 0; j < n; ++j) {
@@ -381,7 +422,7 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmQ, const CUtensorM
         K::publish_p();
         __syncwarp();
         if (row == 0) trace_stamp(p.trace, blk0 + j, 6 + 3 * s);
-        if (lane == 0) mbar_arrive(&ctl.p_full[s]);
+        if (lane == 0) arrive_issuer(&ctl.p_full[s]);
       }
       if (!ok) break;
       // final row statistics for the epilogue
@@ -402,9 +443,9 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmQ, const CUtensorM
     int blk = 0;
     bool ok = true;
     for (int rnd = 0; ok; ++rnd) {
-      const int u = unit_at(rnd, blockIdx.x);
+      const int u = unit_at(rnd, worker, n_workers);
       if (u >= p.n_items) break;
-      const Unit un = decode_unit<CAUSAL, WIN>(p, u);
+      const Unit un = decode_unit<CAUSAL, WIN, PAIR>(p, u);
       const int blk0 = blk;
       blk += un.nb;
       for (int j = 0; j < un.nb && ok; ++j) {
@@ -438,7 +479,7 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmQ, const CUtensorM
           tc_fence_before();
           __syncwarp();
           if (row == 0) trace_stamp(p.trace, blk0 + j, 11 + 2 * s);
-          if (lane == 0) mbar_arrive(&ctl.o_ready[s]);
+          if (lane == 0) arrive_issuer(&ctl.o_ready[s]);
         }
       }
       if (!ok) break;
@@ -447,7 +488,7 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmQ, const CUtensorM
 #pragma unroll 1
       for (int s = 0; s < 2; ++s) {
         if (!un.rows[s]) continue;
-        const int rg = un.row0 + s * 128 + row;
+        const int rg = un.row0 + s * kStage + 128 * int(rank) + row;
         const bool valid = rg < p.Nq;
         __nv_bfloat16* dst = p.o + ((size_t(un.b) * p.Nq + rg) * p.Hq + un.h) * D;
         float* lse_dst = p.lse + (size_t(un.b) * p.Hq + un.h) * p.Nq + rg;
@@ -473,7 +514,7 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmQ, const CUtensorM
         // each warp stages its 32 rows x 64 columns (bf16, 128-byte swizzle)
         // and writes them with one TMA store; rows past Nq are clipped
         uint8_t* stg = sStg + wq * 4096;
-        const int wrow0 = un.row0 + s * 128 + wq * 32;
+        const int wrow0 = un.row0 + s * kStage + 128 * int(rank) + wq * 32;
 #pragma unroll 1
         for (int hf = 0; hf < D / 64; ++hf) {
           if (lane == 0) bulk_wait_read_all();  // the previous store has read the buffer
@@ -514,9 +555,9 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmQ, const CUtensorM
       bool first = true, ok = true;
       bool injected = false;
       for (int rnd = 0; ok; ++rnd) {
-        const int u = unit_at(rnd, blockIdx.x);
+        const int u = unit_at(rnd, worker, n_workers);
         if (u >= p.n_items) break;
-        const Unit un = decode_unit<CAUSAL, WIN>(p, u);
+        const Unit un = decode_unit<CAUSAL, WIN, PAIR>(p, u);
         if (un.nb == 0) continue;
         if (!first) {
           if (!mbar_wait_bounded(&ctl.q_empty, ph_qe, abort_flag, LIM)) { ok = false; break; }
@@ -525,8 +566,15 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmQ, const CUtensorM
         first = false;
         for (int s = 0; s < 2; ++s) {
           if (un.n[s] == 0) continue;
-          mbar_arrive_expect_tx(&ctl.q_full[s], K::kTileBytes);
-          K::load_q(sQ + s * K::kTileBytes, &tmQ, &ctl.q_full[s], un.h, un.row0 + s * 128, un.b);
+          if constexpr (PAIR) {
+            // both CTAs' Q tiles complete on the even CTA's barrier
+            if (rank == 0) mbar_arrive_expect_tx(&ctl.q_full[s], 2 * K::kTileBytes);
+            K::load_q(sQ + s * K::kTileBytes, &tmQ, mapa_shared(smem_u32(&ctl.q_full[s]), 0), un.h,
+                      un.row0 + s * kStage + 128 * int(rank), un.b);
+          } else {
+            mbar_arrive_expect_tx(&ctl.q_full[s], K::kTileBytes);
+            K::load_q(sQ + s * K::kTileBytes, &tmQ, &ctl.q_full[s], un.h, un.row0 + s * kStage, un.b);
+          }
         }
         for (int j = 0; j < un.nb && ok; ++j) {
 #pragma unroll 1
@@ -536,15 +584,25 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmQ, const CUtensorM
             if (!mbar_wait_bounded(&ctl.kv_empty[slot], ph, abort_flag, LIM)) { ok = false; break; }
             trace_stamp(p.trace, blk + j, 14 + t);
             ++kv_it;
-            if (p.inject == 1 && !injected) {  // test hook: never deliver this tile
+            if (p.inject == 1 && !injected && rank == 0) {  // test hook: never deliver this tile
               injected = true;
               continue;
             }
-            mbar_arrive_expect_tx(&ctl.kv_full[slot], K::kTileBytes);
-            if (t == 0)
-              K::load_k(sKV + slot * K::kTileBytes, &tmK, &ctl.kv_full[slot], un.kvh, (un.kb0 + j) * 128, un.b);
-            else
-              K::load_v(sKV + slot * K::kTileBytes, &tmV, &ctl.kv_full[slot], un.kvh, (un.kb0 + j) * 128, un.b);
+            uint8_t* dst = sKV + slot * K::kSlotBytes;
+            if constexpr (PAIR) {
+              if (rank == 0) mbar_arrive_expect_tx(&ctl.kv_full[slot], 2 * K::kSlotBytes);
+              const uint32_t bar = mapa_shared(smem_u32(&ctl.kv_full[slot]), 0);
+              if (t == 0)
+                K::load_k(dst, &tmK, bar, un.kvh, (un.kb0 + j) * 128, un.b, rank);
+              else
+                K::load_v(dst, &tmV, bar, un.kvh, (un.kb0 + j) * 128, un.b, rank);
+            } else {
+              mbar_arrive_expect_tx(&ctl.kv_full[slot], K::kSlotBytes);
+              if (t == 0)
+                K::load_k(dst, &tmK, &ctl.kv_full[slot], un.kvh, (un.kb0 + j) * 128, un.b);
+              else
+                K::load_v(dst, &tmV, &ctl.kv_full[slot], un.kvh, (un.kb0 + j) * 128, un.b);
+            }
           }
         }
         blk += un.nb;
@@ -557,7 +615,17 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmQ, const CUtensorM
     }
   } else if (warp == 13) {
     // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    // (with CTA pairs only the even CTA issues, for both)
+    if (lane == 0 && rank == 0) {
+      // completion of the issued MMAs: on this CTA's barrier, or on the same
+      // barrier of both CTAs of a pair
+      auto commit = [&](uint64_t* bar) {
+        if constexpr (PAIR) {
+          mma_commit_pair(bar, 3);
+        } else {
+          mma_commit(bar);
+        }
+      };
       // a negative scale negates A (Q) in S = Q K^T: bit 13 of the instruction descriptor
       const uint32_t idS = K::idesc_s() | (p.neg_s << 13);
       constexpr uint32_t idPV = K::idesc_pv();
@@ -574,9 +642,9 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmQ, const CUtensorM
         return r;
       };
       for (int rnd = 0; ok; ++rnd) {
-        const int u = unit_at(rnd, blockIdx.x);
+        const int u = unit_at(rnd, worker, n_workers);
         if (u >= p.n_items) break;
-        const Unit un = decode_unit<CAUSAL, WIN>(p, u);
+        const Unit un = decode_unit<CAUSAL, WIN, PAIR>(p, u);
         if (un.nb == 0) continue;
         for (int s = 0; s < 2 && ok; ++s) {
           if (un.n[s] == 0) continue;
@@ -589,10 +657,10 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmQ, const CUtensorM
         for (int s = 0; s < 2; ++s) {
           if (!un.active(s, 0)) continue;
           K::issue_s(dsc, tmem + uint32_t(s * 128), s, kslot, idS);
-          mma_commit(&ctl.s_full[s]);
+          commit(&ctl.s_full[s]);
         }
-        mma_commit(&ctl.kv_empty[kslot]);
-        if (un.nb == 1) mma_commit(&ctl.q_empty);
+        commit(&ctl.kv_empty[kslot]);
+        if (un.nb == 1) commit(&ctl.q_empty);
         for (int j = 0; j < un.nb && ok; ++j) {
           if (!wait_kv(vslot)) { ok = false; break; }
           const bool nxt = j + 1 < un.nb;
@@ -608,27 +676,31 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmQ, const CUtensorM
               trace_stamp(p.trace, blk + j, s);
               K::issue_pv(dsc, tmem + kOCol0 + uint32_t(s * D), tmem + uint32_t(s * 128), s, vslot, j > un.a[s],
                           idPV);
-              if (j == un.a[s] + un.n[s] - 1) mma_commit(&ctl.o_full[s]);
+              if (j == un.a[s] + un.n[s] - 1) commit(&ctl.o_full[s]);
               // V_j is free once the last PV reading it completes: release it
               // before the next S is issued so the refill starts earlier
-              if (s == last_v) mma_commit(&ctl.kv_empty[vslot]);
+              if (s == last_v) commit(&ctl.kv_empty[vslot]);
             }
             if (nxt && un.active(s, j + 1)) {  // S of the next tile (a stage's first S when it starts there)
               tc_fence_after();
               trace_stamp(p.trace, blk + j, 2 + s);
               K::issue_s(dsc, tmem + uint32_t(s * 128), s, kslot, idS);
-              mma_commit(&ctl.s_full[s]);
+              commit(&ctl.s_full[s]);
             }
           }
           if (!ok) break;
-          if (nxt) mma_commit(&ctl.kv_empty[kslot]);
-          if (j + 2 == un.nb) mma_commit(&ctl.q_empty);
+          if (nxt) commit(&ctl.kv_empty[kslot]);
+          if (j + 2 == un.nb) commit(&ctl.q_empty);
         }
         blk += un.nb;
       }
       if (*abort_flag) {
         // drain the tensor pipe before TMEM is released
-        mma_commit(&ctl.drain);
+        if constexpr (PAIR) {
+          mma_commit_pair(&ctl.drain, 1);
+        } else {
+          mma_commit(&ctl.drain);
+        }
         const uint64_t t0 = globaltimer_ns();
         while (!mbar_try_wait(smem_u32(&ctl.drain), 0) && globaltimer_ns() - t0 < 100000000ull) {
         }
@@ -640,17 +712,28 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmQ, const CUtensorM
   if (warp == 8 && lane == 0) trace_stamp(p.trace, kEv, 6);
   __syncwarp();
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR) {
+    cluster_sync_all();  // no CTA of a pair leaves while the other may still reach its memory
+  } else {
+    __syncthreads();
+  }
   tc_fence_after();
-  if (warp == 13) tmem_dealloc(tmem, 512);
+  if (warp == 13) {
+    if constexpr (PAIR) {
+      tmem_dealloc_pair(tmem, 512);
+    } else {
+      tmem_dealloc(tmem, 512);
+    }
+  }
   if (threadIdx.x == 0 && ctl.abort) atomicOr(p.status, kDevTimeout);
   if (threadIdx.x == 0) trace_stamp(p.trace, kEv, 7);
 }
 
 // Work items of one launch: the unit count and the row-split tail
-// (non-causal only; see Params).
-inline void plan_units(Params& p, const Problem& pb, bool causal, int G) {
-  p.n_mblocks = (pb.Nq + 255) / 256;
+// (non-causal only; see Params). G is the number of workers (CTAs, or CTA
+// pairs with 512-row units).
+inline void plan_units(Params& p, const Problem& pb, bool causal, int G, int rows_per_unit = 256) {
+  p.n_mblocks = (pb.Nq + rows_per_unit - 1) / rows_per_unit;
   p.n_units = p.n_mblocks * pb.B * pb.Hq;
   // Row-split tail: when the T = n_units mod G units of the last round fit
   // on G CTAs twice over, each runs as two single-stage items (its two
@@ -659,7 +742,7 @@ inline void plan_units(Params& p, const Problem& pb, bool causal, int G) {
   // round ends sooner. Causal units stay whole: their longest-first order
   // already fills the last round with short units.
   const int T = p.n_units % G;
-  const int n_split = (!causal && T > 0 && 2 * T <= G && pb.Nq > 128) ? T : 0;
+  const int n_split = (!causal && T > 0 && 2 * T <= G && pb.Nq > rows_per_unit / 2) ? T : 0;
   p.n_full = p.n_units - n_split;
   p.n_items = p.n_full + 2 * n_split;
 }

@@ -31,6 +31,7 @@ struct DebugCfg {
   cudaEvent_t ev_end;
   unsigned long long* trace;  // optional device trace buffer
   int poly_every;             // forward exp2 split (fa_tune FA_TUNE_EXP2_SPLIT)
+  int cta_pairs;              // forward on CTA pairs (fa_tune FA_TUNE_CTA_PAIRS)
 };
 DebugCfg debug_cfg();
 

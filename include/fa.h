@@ -234,6 +234,19 @@ int fa_debug_exp2(const float* x, float* y, int n, int mode, void* stream);
  *     by the polynomial's rounding.
  */
 #define FA_TUNE_EXP2_SPLIT 1
+/*
+ *   FA_TUNE_CTA_PAIRS: value 1 runs fa_fwd (d = 128, causal or not; not
+ *     fa_fwd_window) on pairs of CTAs: a cluster of two CTAs takes 512
+ *     query rows at a time and the even one issues tcgen05.mma with
+ *     cta_group::2 (M = 256 over both CTAs' tensor memory), each CTA loading
+ *     half of every K and V tile (the FlashAttention-4 article on smntcn.com:
+ *     fifth-generation tensor cores and 256 KB of tensor memory per SM; the
+ *     pair form halves the MMA instructions and the K/V shared-memory
+ *     traffic per flop). value 0 (the default): one CTA per SM. The exp2
+ *     split does not apply to the paired kernel. Results are the same up to
+ *     the order of floating-point additions.
+ */
+#define FA_TUNE_CTA_PAIRS 2
 int fa_tune(int knob, int value);
 
 /*

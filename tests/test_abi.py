@@ -151,3 +151,8 @@ def test_tune_validates(fa):
         assert fa.fa_tune(fa.TUNE_EXP2_SPLIT, v) == 1
     assert fa.fa_tune(99, 0) == 1
     assert fa.fa_tune(fa.TUNE_EXP2_SPLIT, 0) == 0
+    # CTA pairs: 0 or 1
+    for v in (-1, 2):
+        assert fa.fa_tune(fa.TUNE_CTA_PAIRS, v) == 1
+    assert fa.fa_tune(fa.TUNE_CTA_PAIRS, 1) == 0
+    assert fa.fa_tune(fa.TUNE_CTA_PAIRS, 0) == 0
