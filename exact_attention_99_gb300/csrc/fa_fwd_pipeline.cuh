@@ -315,10 +315,12 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmQ, const CUtensorM
   }
   tc_fence_after();
   const uint32_t tmem = ctl.tmem_base;
-  // arrival on a barrier that the MMA-issuing CTA waits on: local, or on the
-  // even CTA of a pair
+  // arrival on a barrier that the MMA-issuing CTA waits on: local, or from
+  // the odd CTA of a pair on the even CTA's barrier (release at cluster
+  // scope, so that this CTA's tensor-memory writes are ordered before the
+  // MMA that reads them)
   auto arrive_issuer = [&](uint64_t* bar) {
-    if constexpr (PAIR) {
+    if (PAIR && rank != 0) {
       mbar_arrive_cluster(mapa_shared(smem_u32(bar), 0));
     } else {
       mbar_arrive(bar);
