@@ -34,15 +34,20 @@ struct Bf16 {
   static constexpr int kPTileBytes = 0;  // P stays in TMEM
   static constexpr int kSmemDyn = (2 + kSlots) * kTileBytes + fwdp::kStgBytes + 1024;
 
+  // L2 policy: Q is read once per unit (evict first); K and V tiles are read
+  // by every unit of their head (evict last), which keeps more of them in L2
+  // for the causal order's concurrent heads
   __device__ __forceinline__ static void load_q(uint8_t* dst, const CUtensorMap* m, uint64_t* bar, int h, int row,
                                                 int b) {
+    const uint64_t pol = l2_policy_evict_first();
 #pragma unroll
-    for (int c = 0; c < kChunks; ++c) tma_load_4d(dst + c * 16384, m, bar, c * 64, h, row, b);
+    for (int c = 0; c < kChunks; ++c) tma_load_4d_hint(dst + c * 16384, m, bar, c * 64, h, row, b, pol);
   }
   __device__ __forceinline__ static void load_k(uint8_t* dst, const CUtensorMap* m, uint64_t* bar, int kvh, int key0,
                                                 int b) {
+    const uint64_t pol = l2_policy_evict_last();
 #pragma unroll
-    for (int c = 0; c < kChunks; ++c) tma_load_4d(dst + c * 16384, m, bar, c * 64, kvh, key0, b);
+    for (int c = 0; c < kChunks; ++c) tma_load_4d_hint(dst + c * 16384, m, bar, c * 64, kvh, key0, b, pol);
   }
   __device__ __forceinline__ static void load_v(uint8_t* dst, const CUtensorMap* m, uint64_t* bar, int kvh, int key0,
                                                 int b) {
