@@ -673,6 +673,23 @@ def run_ours(args):
     per_workload = per_config(fa, flush, peak)
     per_workload.update({WINDOW_CASE["name"]: window_config(fa, flush, peak)})
     per_workload.update(fp8_config(fa, flush, peak))
+    # a roofline entry per published d = 128 workload and pass: kernel-call
+    # time (median of 20, L2 flushed) against the measured burst peak, and
+    # the DRAM bytes per launch of the pass's main kernel from a committed ncu
+    # summary taken on the current source (else null)
+    rooflines = {}
+    for wl in workloads.WORKLOADS:
+        if wl.d != 128:
+            continue
+        ent = per_workload[wl.name]
+        for pas, kern, fl in (("fwd", "fa_fwd_kernel", wl.fwd_flops()), ("bwd", "bwd_main_kernel", wl.bwd_flops())):
+            if f"{pas}_ms" not in ent:
+                continue
+            ach = fl / ent[f"{pas}_ms"] / 1e9
+            rooflines[f"{wl.name}:{pas}"] = {
+                "bound": "tensor", "achieved": round(ach, 1), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(ach / peak, 4), "time": "whole call" + (" (preprocess, main, dQ convert)" if pas == "bwd" else ""),
+                "traffic": profiled_traffic(kern, wl.name), "traffic_kernel": kern}
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(total_ms / K, 4), "higher_is_better": True, "scaling": "weak",
@@ -685,6 +702,7 @@ def run_ours(args):
         "fwd_tflops": round(w.fwd_flops() / fwd_ms / 1e9, 2), "fwd_frac_of_peak": round(w.fwd_flops() / fwd_ms / 1e9 / peak, 4),
         "bwd_main_tflops": round(w.bwd_flops() / bwd_ms / 1e9, 2),
         "roofline": roofline,
+        "rooflines": rooflines,
         "clocks": clocks,
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4), "link": link,
