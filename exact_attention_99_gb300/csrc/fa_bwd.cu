@@ -15,10 +15,12 @@
 // Kernels:
 //   bwd_pre  : D_i and LSE * log2(e) per query row (padded to whole tiles),
 //              zero the fp32 dQ accumulator.
-//   bwd_main : one CTA per (batch, kv head, 128-key tile) -- per pair of key
-//              tiles (j, n-1-j) when causal, so every CTA has the same work --
-//              looping over the query heads of the GQA group x 128-row query
-//              tiles that see the tile.
+//   bwd_main : persistent, one CTA per SM, running work units round robin:
+//              a unit is one (batch, kv head, 128-key tile) -- a pair of key
+//              tiles (j, n-1-j) when causal, so the units have the same work
+//              -- and each tile ("item") loops over the query heads of the GQA
+//              group x 128-row query tiles that see it. Near an item's end
+//              the next item's K and V are prefetched into L2.
 //     warps 0-7  compute: two warps per lane quarter, each thread one key
 //                row and 64 of the tile's 128 query columns; P^T =
 //                2^(S^T*scale*log2e - LSE*log2e), dS^T = P^T o (dP^T - D)
@@ -52,6 +54,7 @@ namespace fa {
 namespace bwd {
 
 constexpr int kThreads = 512;
+constexpr int kPrefetchSteps = 4;  // the next item's K/V go to L2 this many steps before an item ends
 
 template <int D>
 struct Cfg {
@@ -83,6 +86,18 @@ struct Work {
   Item it[2];
 };
 
+// The maps the dQ drain writes through, in one kernel parameter so that one
+// base address serves all three: the fp32 dQ accumulator (reductions), dK
+// and dV (stores).
+struct OutMaps {
+  CUtensorMap acc, dk, dv;
+};
+
+struct Cur {  // a warp's current item, kept in shared memory (see below)
+  Item I;
+  int b, kvh;
+};
+
 struct __align__(8) Ctl {
   uint64_t kv_full;
   uint64_t q_full[2], q_empty[2], do_full, do_empty;
@@ -92,7 +107,7 @@ struct __align__(8) Ctl {
   uint64_t s_full, p_full, dp_full, ds_full, dq_full, dq_empty, acc_full, drain;
   uint32_t tmem_base;
   uint32_t abort;
-  Work work;  // this CTA's items, decoded once
+  Cur cur[kThreads / 32];
 };
 
 struct Params {
@@ -106,6 +121,9 @@ struct Params {
   // head, the last n_split (those nearest the middle, both tiles about half
   // a pair's work) run as two single-tile CTAs each, after every whole pair
   int n_split;
+  // work units (a pair or a single key tile of one (batch, kv head)); the
+  // CTAs are persistent: CTA c runs units c, c + gridDim.x, ...
+  int n_units;
   // masked kernels: key j visible to query row i iff i + off - wl <= j <=
   // i + off + wr (off = Nk - Nq); a negative bound is no limit; causal is
   // wl = -1, wr = 0
@@ -130,7 +148,7 @@ template <bool WIN>
 __device__ __forceinline__ int win_r(const Params& p) { return WIN ? p.wr : 0; }
 
 template <bool CAUSAL, bool WIN>
-__device__ __forceinline__ Work decode(const Params& p) {
+__device__ __forceinline__ Work decode(const Params& p, int unit) {
   Work w;
   int r;
   if (CAUSAL && win_l<WIN>(p) < 0) {
@@ -142,15 +160,15 @@ __device__ __forceinline__ Work decode(const Params& p) {
     // and fills what would otherwise be a partly idle last wave of pairs.
     const int half = p.n_ktiles / 2, kept = half - p.n_split;
     const int whole = p.B * p.Hkv * kept;
-    if (int(blockIdx.x) < whole) {
-      r = blockIdx.x / kept;
-      const int pr = blockIdx.x - r * kept;
+    if (unit < whole) {
+      r = unit / kept;
+      const int pr = unit - r * kept;
       w.it[0].j = pr;
       w.it[1].j = p.n_ktiles - 1 - pr;
       w.n_items = 2;
     } else {
       const int per_head = 2 * p.n_split + (p.n_ktiles & 1);
-      const int s = blockIdx.x - whole;
+      const int s = unit - whole;
       r = s / per_head;
       const int t = s - r * per_head;
       const int pr = kept + (t >> 1);
@@ -162,8 +180,8 @@ __device__ __forceinline__ Work decode(const Params& p) {
     // all key tiles of one head in a row, so concurrent CTAs share Q, dO and
     // the dQ accumulator in L2 (also for windows with a left bound, where
     // every key tile has about the same number of query tiles)
-    r = blockIdx.x / p.n_ktiles;
-    w.it[0].j = blockIdx.x - r * p.n_ktiles;
+    r = unit / p.n_ktiles;
+    w.it[0].j = unit - r * p.n_ktiles;
     w.it[1].j = 0;
     w.n_items = 1;
   }
@@ -189,7 +207,23 @@ __device__ __forceinline__ Work decode(const Params& p) {
   return w;
 }
 
-__device__ __forceinline__ Item pick(const Work& w, int k) { return w.it[k]; }
+// (a select, not an indexed load: keeps a Work in registers)
+__device__ __forceinline__ Item pick(const Work& w, int k) { return k == 0 ? w.it[0] : w.it[1]; }
+
+// The k-th item of this (persistent) CTA: item k & 1 of unit blockIdx.x +
+// (k >> 1) * gridDim.x. Returns 0 past the last unit, 1 when the unit has no
+// such item (a single), 2 with I, b, kvh set.
+template <bool CAUSAL, bool WIN>
+__device__ __forceinline__ int item_at(const Params& p, int k, Item& I, int& b, int& kvh) {
+  const int u = int(blockIdx.x) + (k >> 1) * int(gridDim.x);
+  if (u >= p.n_units) return 0;
+  const Work w = decode<CAUSAL, WIN>(p, u);
+  if ((k & 1) >= w.n_items) return 1;
+  I = pick(w, k & 1);
+  b = w.b;
+  kvh = w.kvh;
+  return 2;
+}
 
 // swizzled (128-byte) byte offset of element (row, col) in a [128 rows x 128
 // cols] bf16 tile stored as two 64-column atoms
@@ -217,14 +251,13 @@ template <int D, bool CAUSAL, bool WIN>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-                    const __grid_constant__ CUtensorMap tmAcc, const Params p) {
+                    const __grid_constant__ OutMaps out, const Params p) {
   using C = Cfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   Ctl& ctl = *reinterpret_cast<Ctl*>(smem + C::kOffCtl);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int wg = warp >> 2;
-  const Work& w = ctl.work;  // read from shared memory to keep it out of every role's registers
   const uint64_t LIM = p.wait_limit_ns;
   volatile uint32_t* abort_flag = &ctl.abort;
 
@@ -234,7 +267,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (threadIdx.x == 0) {
     ctl.abort = 0;
-    ctl.work = decode<CAUSAL, WIN>(p);
     mbar_init(&ctl.kv_full, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ctl.q_full[i], 1);
@@ -290,8 +322,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t ph_s = 0, ph_dp = 0;
     bool ok = true;
     int g = 0;  // step counter across items
-    for (int ii = 0; ii < w.n_items && ok; ++ii) {
-      const Item I = pick(w, ii);
+    for (int k = 0; ok; ++k) {
+      {
+        // the item goes to this warp's shared slot: the compute and drain
+        // warps have no registers to spare for it
+        Item t;
+        int tb, tk;
+        const int have = item_at<CAUSAL, WIN>(p, k, t, tb, tk);
+        if (have == 0) break;
+        if (have == 1) continue;
+        __syncwarp();
+        if (lane == 0) ctl.cur[warp] = Cur{t, tb, tk};
+        __syncwarp();
+      }
+      const Item& I = ctl.cur[warp].I;
+      const int& ib = ctl.cur[warp].b;
+      const int& ikvh = ctl.cur[warp].kvh;
       const int key = I.j * 128 + row;
       const bool kvalid = key < p.Nk;  // keys past Nk are zero-filled: give them P = 0
       for (int st = 0; st < I.steps && ok; ++st, ++g) {
@@ -409,11 +455,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t ph_dq = 0, nacc = 0;
     bool ok = true;
     int g = 0;
-    for (int ii = 0; ii < w.n_items && ok; ++ii) {
-      const Item I = pick(w, ii);
+    for (int k = 0; ok; ++k) {
+      {
+        // the item goes to this warp's shared slot: the compute and drain
+        // warps have no registers to spare for it
+        Item t;
+        int tb, tk;
+        const int have = item_at<CAUSAL, WIN>(p, k, t, tb, tk);
+        if (have == 0) break;
+        if (have == 1) continue;
+        __syncwarp();
+        if (lane == 0) ctl.cur[warp] = Cur{t, tb, tk};
+        __syncwarp();
+      }
+      const Item& I = ctl.cur[warp].I;
+      const int& ib = ctl.cur[warp].b;
+      const int& ikvh = ctl.cur[warp].kvh;
       for (int st = 0; st < I.steps && ok; ++st, ++g) {
         const int it = I.i0 + st % I.nq;
-        const int h = w.kvh * p.group + st / I.nq;
+        const int h = ikvh * p.group + st / I.nq;
         if (!mbar_wait_bounded(&ctl.dq_full, ph_dq, abort_flag, LIM)) { ok = false; break; }
         ph_dq ^= 1;
         if (threadIdx.x == 256) trace_stamp(p.trace, g, 10);
@@ -453,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) {
 #pragma unroll
               for (int b2 = 0; b2 < 2; ++b2)
-                tma_reduce_add_4d(&tmAcc, stg + b2 * 4096, it * 128 + (half * 2 + b2) * 32, wq * 32, h, w.b);
+                tma_reduce_add_4d(&out.acc, stg + b2 * 4096, it * 128 + (half * 2 + b2) * 32, wq * 32, h, ib);
               bulk_commit();
             }
           }
@@ -470,19 +530,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           // dQ: lane = query row, 64 columns = d; for a fixed d the warp's
           // lanes hit consecutive query rows of the accumulator
           const int q = it * 128 + lr;
-          float* dst = p.dq_acc + (size_t(w.b) * p.Hq + h) * D * size_t(p.Nq_pad) + q;
+          float* dst = p.dq_acc + (size_t(ib) * p.Hq + h) * D * size_t(p.Nq_pad) + q;
 #pragma unroll
           for (int c = 0; c < 64; ++c) red_add_f32(dst + size_t(c) * p.Nq_pad, u2f(v[c]));
         }
       }
       if (!ok) break;
       // epilogue of this item: dV, dK rows of its key tile (lane = key row)
-      const int key = I.j * 128 + lr;
-      const bool valid = key < p.Nk;
-      __nv_bfloat16* dv = p.dv + ((size_t(w.b) * p.Nk + key) * p.Hkv + w.kvh) * D;
-      __nv_bfloat16* dk = p.dk + ((size_t(w.b) * p.Nk + key) * p.Hkv + w.kvh) * D;
       if (I.steps == 0) {
-        if (valid) {
+        const int key = I.j * 128 + lr;
+        __nv_bfloat16* dv = p.dv + ((size_t(ib) * p.Nk + key) * p.Hkv + ikvh) * D;
+        __nv_bfloat16* dk = p.dk + ((size_t(ib) * p.Nk + key) * p.Hkv + ikvh) * D;
+        if (key < p.Nk) {
           for (int c = 0; c < D / 8; ++c) {
             reinterpret_cast<uint4*>(dv)[c] = make_uint4(0, 0, 0, 0);
             reinterpret_cast<uint4*>(dk)[c] = make_uint4(0, 0, 0, 0);
@@ -493,70 +552,143 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait_bounded(&ctl.acc_full, nacc & 1, abort_flag, LIM)) { ok = false; break; }
       ++nacc;
       tc_fence_after();
+      if (D == 128) {
+        // Each warp stages its 32 key rows of dV, then of dK, as two
+        // 128-byte-swizzled [32 rows][64 d] bf16 boxes in its quarter of the
+        // dQ staging buffer and writes them with TMA stores (rows past Nk
+        // are clipped): whole-line writes, and the warp is free at once.
+        // The accumulators are released as soon as dK is in registers.
+        uint8_t* stg = smem + C::kOffStg + wq * 8192;
+        const int row0 = I.j * 128 + wq * 32;
 #pragma unroll 1
-      for (int t = 0; t < 2; ++t) {
-        const uint32_t col = t == 0 ? C::kColDV : C::kColDK;
-        const float mul = t == 0 ? 1.0f : p.scale;
-        __nv_bfloat16* dst = t == 0 ? dv : dk;
+        for (int t = 0; t < 2; ++t) {
+          const uint32_t col = t == 0 ? C::kColDV : C::kColDK;
+          const float mul = t == 0 ? 1.0f : p.scale;
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld32(t_lane + col + c * 32, v);
-          tmem_wait_ld();
-          uint32_t pk[16];
+          for (int b2 = 0; b2 < 2; ++b2) {  // 64 columns (one box) at a time
+            uint32_t v[64];
+            tmem_ld32(t_lane + col + b2 * 64, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+            tmem_ld32(t_lane + col + b2 * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+            tmem_wait_ld();
+            if (t == 1 && b2 == 1) {  // the next item's MMAs may overwrite the accumulators
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&ctl.acc_empty);
+            }
+            if (b2 == 0) {
+              if (lane == 0) bulk_wait_read_all();  // earlier reductions and stores have read the quarter
+              __syncwarp();
+            }
+            uint8_t* box = stg + b2 * 4096 + lane * 128;
 #pragma unroll
-          for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(u2f(v[2 * i]) * mul, u2f(v[2 * i + 1]) * mul);
-          if (valid) {
-            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+            for (int u = 0; u < 8; ++u) {
+              const int c = u * 8;
+              *reinterpret_cast<uint4*>(box + ((u ^ (lane & 7)) << 4)) =
+                  make_uint4(pack_bf16x2(u2f(v[c]) * mul, u2f(v[c + 1]) * mul),
+                             pack_bf16x2(u2f(v[c + 2]) * mul, u2f(v[c + 3]) * mul),
+                             pack_bf16x2(u2f(v[c + 4]) * mul, u2f(v[c + 5]) * mul),
+                             pack_bf16x2(u2f(v[c + 6]) * mul, u2f(v[c + 7]) * mul));
+            }
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && row0 < p.Nk) {
+            const CUtensorMap* m = t == 0 ? &out.dv : &out.dk;
+            tma_store_4d(m, stg, 0, ikvh, row0, ib);
+            tma_store_4d(m, stg + 4096, 64, ikvh, row0, ib);
+            bulk_commit();
           }
         }
+      } else {
+        const int key = I.j * 128 + lr;
+        const bool valid = key < p.Nk;
+#pragma unroll 1
+        for (int t = 0; t < 2; ++t) {
+          const uint32_t col = t == 0 ? C::kColDV : C::kColDK;
+          const float mul = t == 0 ? 1.0f : p.scale;
+          __nv_bfloat16* dst = (t == 0 ? p.dv : p.dk) + ((size_t(ib) * p.Nk + key) * p.Hkv + ikvh) * D;
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld32(t_lane + col + c * 32, v);
+            tmem_wait_ld();
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(u2f(v[2 * i]) * mul, u2f(v[2 * i + 1]) * mul);
+            if (valid) {
+              uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+            }
+          }
+        }
+        // the accumulators may now be overwritten by the next item
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl.acc_empty);
       }
-      // the accumulators may now be overwritten by the next item
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl.acc_empty);
     }
-    if (D == 128 && lane == 0) bulk_wait_all();  // the accumulator is complete when the kernel ends
+    if (D == 128 && lane == 0) bulk_wait_all();  // the accumulator and dK/dV are written when the kernel ends
   } else {
     setmaxnreg_dec<96>();
   }
-  int total_steps = 0;
-#pragma unroll
-  for (int k = 0; k < 2; ++k) total_steps += w.it[k].steps;
   if (warp == 12) {
     // ------------------------------------------------------- TMA producer
-    if (lane == 0 && total_steps > 0) {
+    if (lane == 0) {
       bool ok = true;
       int g = 0, nkv = 0;
-      for (int ii = 0; ii < w.n_items && ok; ++ii) {
-        const Item I = pick(w, ii);
+      for (int k = 0; ok; ++k) {
+        {
+          Item t;
+          int tb, tk;
+          const int have = item_at<CAUSAL, WIN>(p, k, t, tb, tk);
+          if (have == 0) break;
+          if (have == 1) continue;
+          ctl.cur[warp] = Cur{t, tb, tk};  // one thread runs this role
+        }
+        const Item& I = ctl.cur[warp].I;
+        const int& ib = ctl.cur[warp].b;
+        const int& ikvh = ctl.cur[warp].kvh;
         if (I.steps == 0) continue;
         if (nkv > 0 && !mbar_wait_bounded(&ctl.kv_empty, (nkv - 1) & 1, abort_flag, LIM)) { ok = false; break; }
         ++nkv;
         mbar_arrive_expect_tx(&ctl.kv_full, 2 * C::kTile);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c) {
-          tma_load_4d(sK + c * 16384, &tmK, &ctl.kv_full, c * 64, w.kvh, I.j * 128, w.b);
-          tma_load_4d(sV + c * 16384, &tmV, &ctl.kv_full, c * 64, w.kvh, I.j * 128, w.b);
+          tma_load_4d(sK + c * 16384, &tmK, &ctl.kv_full, c * 64, ikvh, I.j * 128, ib);
+          tma_load_4d(sV + c * 16384, &tmV, &ctl.kv_full, c * 64, ikvh, I.j * 128, ib);
         }
         for (int st = 0; st < I.steps && ok; ++st, ++g) {
           const int it = I.i0 + st % I.nq;
-          const int h = w.kvh * p.group + st / I.nq;
+          const int h = ikvh * p.group + st / I.nq;
           const int qs = g & 1;
+          if (st == max(0, I.steps - kPrefetchSteps)) {
+            // the next item's K and V into L2, so that its loads (issued
+            // once this item's last GEMM has read K and V) hit L2
+            Item N;
+            int nb, nkvh;
+            int nh = item_at<CAUSAL, WIN>(p, k + 1, N, nb, nkvh);
+            if (nh == 1) nh = item_at<CAUSAL, WIN>(p, k + 2, N, nb, nkvh);
+            if (nh == 2 && N.steps > 0) {
+#pragma unroll
+              for (int c = 0; c < D / 64; ++c) {
+                tma_prefetch_l2_4d(&tmK, c * 64, nkvh, N.j * 128, nb);
+                tma_prefetch_l2_4d(&tmV, c * 64, nkvh, N.j * 128, nb);
+              }
+            }
+          }
           if (!mbar_wait_bounded(&ctl.q_empty[qs], ((g >> 1) & 1) ^ 1, abort_flag, LIM)) { ok = false; break; }
           trace_stamp(p.trace, g, 13);
           mbar_arrive_expect_tx(&ctl.q_full[qs], C::kTile);
 #pragma unroll
           for (int c = 0; c < D / 64; ++c)
-            tma_load_4d(sQ + qs * C::kTile + c * 16384, &tmQ, &ctl.q_full[qs], c * 64, h, it * 128, w.b);
+            tma_load_4d(sQ + qs * C::kTile + c * 16384, &tmQ, &ctl.q_full[qs], c * 64, h, it * 128, ib);
           // LSE/D rows before dO: the compute warps need them as soon as
           // S is ready, while dO (one slot) waits for the previous dV
           const int vs = g & 1;
           if (!mbar_wait_bounded(&ctl.vec_empty[vs], ((g >> 1) & 1) ^ 1, abort_flag, LIM)) { ok = false; break; }
           mbar_arrive_expect_tx(&ctl.vec_full[vs], 1024);
-          const size_t roff = (size_t(w.b) * p.Hq + h) * p.Nq_pad + size_t(it) * 128;
+          const size_t roff = (size_t(ib) * p.Hq + h) * p.Nq_pad + size_t(it) * 128;
           bulk_load(sVec + vs * 256, p.lse2 + roff, 512, &ctl.vec_full[vs]);
           bulk_load(sVec + vs * 256 + 128, p.delta + roff, 512, &ctl.vec_full[vs]);
           if (!mbar_wait_bounded(&ctl.do_empty, (g & 1) ^ 1, abort_flag, LIM)) { ok = false; break; }
@@ -564,7 +696,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(&ctl.do_full, C::kTile);
 #pragma unroll
           for (int c = 0; c < D / 64; ++c)
-            tma_load_4d(sDO + c * 16384, &tmDO, &ctl.do_full, c * 64, h, it * 128, w.b);
+            tma_load_4d(sDO + c * 16384, &tmDO, &ctl.do_full, c * 64, h, it * 128, ib);
         }
       }
       if (*abort_flag) {
@@ -574,7 +706,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 13) {
     // ---------------------------------------------------------- MMA issuer
-    if (lane == 0 && total_steps > 0) {
+    if (lane == 0) {
       constexpr uint32_t idSS = idesc_bf16_f32(128, 128, 0, 0);     // S^T, dP^T
       constexpr uint32_t idAcc = idesc_bf16_f32(128, D, 0, 1);      // dV, dK
       constexpr uint32_t idDQ = D == 128 ? idesc_bf16_f32(128, 128, 1, 1) : idesc_bf16_f32(128, 64, 1, 1);
@@ -596,8 +728,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ss_lo(tmem + d_col, sdesc_step(a0, ko), sdesc_step(b0, ko), idSS, kk > 0);
         }
       };
-      for (int ii = 0; ii < w.n_items && ok; ++ii) {
-        const Item I = pick(w, ii);
+      for (int k = 0; ok; ++k) {
+        {
+          Item t;
+          int tb, tk;
+          const int have = item_at<CAUSAL, WIN>(p, k, t, tb, tk);
+          if (have == 0) break;
+          if (have == 1) continue;
+          ctl.cur[warp] = Cur{t, tb, tk};  // one thread runs this role
+        }
+        const Item& I = ctl.cur[warp].I;
+        const int& ib = ctl.cur[warp].b;
+        const int& ikvh = ctl.cur[warp].kvh;
         if (I.steps == 0) continue;
         ok = mbar_wait_bounded(&ctl.kv_full, nkv & 1, abort_flag, LIM);
         if (ok) ok = mbar_wait_bounded(&ctl.q_full[g & 1], (g >> 1) & 1, abort_flag, LIM);
@@ -797,12 +939,13 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(const float* dq_acc, __nv
 }
 
 // How many key-tile pairs per head (those nearest the middle) to run as two
-// single-tile CTAs, for `heads` (batch, kv head) slices of n key tiles on G
-// SMs (one CTA each). Model, in units of half a pair's work: a whole pair
-// takes 2, a single 1; CTAs start in launch order as SMs free up (pairs
-// first). With P whole pairs in W = P / G full waves and T = P mod G more,
-// S singles finish at the smallest t with (G - T) (t - 2W) + T max(0, t - 2W
-// - 2) >= S. The smallest split count reaching the least finish time wins.
+// single-tile units, for `heads` (batch, kv head) slices of n key tiles on G
+// persistent CTAs. Model, in units of half a pair's work: a whole pair takes
+// 2, a single 1. Units go to CTAs round robin in order (P pairs, then S
+// singles): with W = P / G and T = P mod G, CTA c runs W pairs (one more if
+// c < T) and then the singles u with (P + u) mod G = c. The finish time is
+// the largest CTA's total; the smallest split count reaching the least
+// finish time wins.
 int split_pairs(int heads, int n, int G) {
   const int half = n / 2;
   int best_m = 0;
@@ -810,17 +953,11 @@ int split_pairs(int heads, int n, int G) {
   for (int m = 0; m <= half; ++m) {
     const long long P = 1LL * heads * (half - m), S = 1LL * heads * (2 * m + (n & 1));
     const long long W = P / G, T = P % G;
-    long long t = 2 * W + (T > 0 ? 2 : 0);
-    if (S > 0) {
-      // singles start at 2W on the G - T free SMs, at 2W + 2 on the others
-      long long lo = 1, hi = S;
-      while (lo < hi) {
-        const long long mid = (lo + hi) / 2;
-        const long long cap = (G - T) * mid + T * (mid > 2 ? mid - 2 : 0);
-        if (cap >= S) hi = mid; else lo = mid + 1;
-      }
-      t = std::max(t, 2 * W + lo);
-    }
+    // CTAs c >= T take singles at positions c - T, those below T at
+    // c - T + G; each takes S / G, plus one at positions below S mod G
+    const long long q = S / G, r = S % G;
+    long long t = 2 * W + q + (r > 0 ? 1 : 0);
+    if (T > 0) t = std::max(t, 2 * (W + 1) + q + (r > G - T ? 1 : 0));
     if (best_t < 0 || t < best_t) {
       best_t = t;
       best_m = m;
@@ -851,16 +988,18 @@ cudaError_t launch_t(const Problem& pb, const void* o, const float* lse, const v
     if (e != cudaSuccess) return e;
   }
   CUtensorMap mq, mk, mv, mdo;
+  OutMaps out;  // dK/dV: stores of [32 key rows][64 d] boxes
   if (!make_bshd_map(&mq, pb.q, pb.B, pb.Nq, pb.Hq, D, 128) || !make_bshd_map(&mk, pb.k, pb.B, pb.Nk, pb.Hkv, D, 128) ||
       !make_bshd_map(&mv, pb.v, pb.B, pb.Nk, pb.Hkv, D, 128) ||
-      !make_bshd_map(&mdo, dout, pb.B, pb.Nq, pb.Hq, D, 128))
+      !make_bshd_map(&mdo, dout, pb.B, pb.Nq, pb.Hq, D, 128) || !make_bshd_map(&out.dk, dk, pb.B, pb.Nk, pb.Hkv, D, 32) ||
+      !make_bshd_map(&out.dv, dv, pb.B, pb.Nk, pb.Hkv, D, 32))
     return cudaErrorInvalidValue;
-  CUtensorMap macc;  // fp32 accumulator [B, Hq, D, Nq_pad], boxes of 32 q x 32 d
+  // out.acc: the fp32 accumulator [B, Hq, D, Nq_pad], boxes of 32 q x 32 d
   {
     const uint64_t dims[4] = {uint64_t(Nq_pad), uint64_t(D), uint64_t(pb.Hq), uint64_t(pb.B)};
     const uint64_t strides[3] = {uint64_t(Nq_pad) * 4, uint64_t(D) * Nq_pad * 4, uint64_t(pb.Hq) * D * Nq_pad * 4};
     const uint32_t box[4] = {32, 32, 1, 1};
-    if (!encode_tiled(&macc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dq_acc, dims, strides, box,
+    if (!encode_tiled(&out.acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dq_acc, dims, strides, box,
                       CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
@@ -895,10 +1034,13 @@ cudaError_t launch_t(const Problem& pb, const void* o, const float* lse, const v
   if (e != cudaSuccess) return e;
   const bool paired = CAUSAL && (WIN ? p.wl : -1) < 0;  // decode: pairs of key tiles only without a left bound
   p.n_split = paired ? split_pairs(pb.B * pb.Hkv, p.n_ktiles, num_sms()) : 0;
-  const unsigned grid =
-      paired ? unsigned(pb.B) * pb.Hkv * (p.n_ktiles / 2 + p.n_split + (p.n_ktiles & 1)) : unsigned(pb.B) * pb.Hkv * p.n_ktiles;
+  const long long units = paired ? 1LL * pb.B * pb.Hkv * (p.n_ktiles / 2 + p.n_split + (p.n_ktiles & 1))
+                                 : 1LL * pb.B * pb.Hkv * p.n_ktiles;
+  if (units > (1LL << 31) - 1) return cudaErrorInvalidValue;
+  p.n_units = int(units);
+  const unsigned grid = unsigned(std::min<long long>(units, num_sms()));  // persistent CTAs, one per SM
   if (dc.ev_begin) cudaEventRecord(dc.ev_begin, stream);
-  kern<<<grid, kThreads, smem, stream>>>(mq, mk, mv, mdo, macc, p);
+  kern<<<grid, kThreads, smem, stream>>>(mq, mk, mv, mdo, out, p);
   e = cudaGetLastError();
   if (dc.ev_end) cudaEventRecord(dc.ev_end, stream);
   if (e != cudaSuccess) return e;
