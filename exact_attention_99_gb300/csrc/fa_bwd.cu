@@ -24,21 +24,24 @@
 //     warps 0-7  compute: two warps per lane quarter, each thread one key
 //                row and 64 of the tile's 128 query columns; P^T =
 //                2^(S^T*scale*log2e - LSE*log2e), dS^T = P^T o (dP^T - D)
-//     warps 8-11 dQ drain and the dK/dV epilogue. d = 128: dQ^T leaves TMEM
+//     warps 8-11 dQ drain and the dK/dV epilogue. d = 128: dQ leaves TMEM
 //                into a shared-memory staging buffer and is added to the fp32
-//                accumulator by TMA bulk reductions; d = 64: coalesced fp32
+//                accumulator by TMA bulk reductions, and dK/dV leave through
+//                the same buffer by TMA stores; d = 64: coalesced fp32
 //                reductions.
 //     Shared memory: K and V tiles (resident), a 2-slot Q ring, a 1-slot dO
 //     ring (its last reader, dV, runs early in each step), the dS^T tile,
 //     the dQ staging buffer, LSE/D vectors.
 //     warp 12    TMA producer, warp 13 MMA issuer, warps 14-15 idle
 //     TMEM: S^T [0,128) with P^T (bf16) over its first 64 columns;
-//           dP^T [128,256), reused for dQ^T once read; dV [256,256+d);
+//           dP^T [128,256), reused for dQ once read; dV [256,256+d);
 //           dK [256+d, 256+2d).
 //     MMA order per query tile i:
-//       dP(i), dV(i) += P^T dO, S(i+1), dK(i) += dS^T Q, dQ^T(i) = K^T dS^T
-//   bwd_post : dQ = bf16(scale * accumulator), transposed back to BSHD.
-//   The accumulator is [B*Hq, d, Nq_pad] fp32 (query index innermost).
+//       dP(i), dV(i) += P^T dO, S(i+1), dK(i) += dS^T Q, dQ(i) = dS K
+//   bwd_post : dQ = bf16(scale * accumulator) in BSHD (a row-by-row pass for
+//              d = 128, a transpose through shared memory for d = 64).
+//   The accumulator is fp32, [B*Hq, Nq_pad, d] (d innermost) for d = 128
+//   and [B*Hq, d, Nq_pad] (query index innermost) for d = 64.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -60,7 +63,7 @@ template <int D>
 struct Cfg {
   static constexpr int kTile = 128 * D * 2;  // K, V, Q or dO tile of 128 rows
   static constexpr int kDsBytes = 128 * 128 * 2;
-  static constexpr int kStgBytes = D == 128 ? 32768 : 0;  // dQ^T staging: 4 warps x 2 boxes of [32 d][32 q] fp32
+  static constexpr int kStgBytes = D == 128 ? 32768 : 0;  // dQ staging: 4 warps x 2 boxes of [32 q][32 d] fp32
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kTile;
   static constexpr int kOffQ = 2 * kTile;   // 2 slots
@@ -113,7 +116,7 @@ struct __align__(8) Ctl {
 struct Params {
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
-  float* dq_acc;        // [B*Hq, D, Nq_pad] fp32
+  float* dq_acc;        // fp32: [B*Hq, Nq_pad, D] for D = 128, [B*Hq, D, Nq_pad] for D = 64
   const float* lse2;    // [B*Hq, Nq_pad]: LSE*log2(e), +inf for padded / empty rows
   const float* delta;   // [B*Hq, Nq_pad]
   int B, Hq, Hkv, Nq, Nk, Nq_pad, group, n_ktiles, n_qtiles;
@@ -135,9 +138,9 @@ struct Params {
 };
 
 // Trace points (fa_trace), per query-tile step:
-//   MMA      0 dP issued, 1 P ready (dV next), 2 next Q ready (S next), 3 dS ready (dK next), 4 dQ^T issued
+//   MMA      0 dP issued, 1 P ready (dV next), 2 next Q ready (S next), 3 dS ready (dK next), 4 dQ issued
 //   compute  5 LSE/D ready, 6 S^T ready, 7 P^T stored, 8 dP^T ready, 9 dS^T stored
-//   drain    10 dQ^T ready, 11 dQ^T columns released, 12 reductions issued
+//   drain    10 dQ ready, 11 dQ columns released, 12 reductions issued
 //   producer 13 Q slot free, 14 dO slot free
 
 // Window bounds as a kernel sees them: the plain causal kernels (WIN false)
@@ -336,8 +339,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
       }
       const Item& I = ctl.cur[warp].I;
-      const int& ib = ctl.cur[warp].b;
-      const int& ikvh = ctl.cur[warp].kvh;
       const int key = I.j * 128 + row;
       const bool kvalid = key < p.Nk;  // keys past Nk are zero-filled: give them P = 0
       for (int st = 0; st < I.steps && ok; ++st, ++g) {
@@ -488,9 +489,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&ctl.dq_empty);
           if (threadIdx.x == 256) trace_stamp(p.trace, g, 11);
-          // dQ^T: lane = d index, column = query row of the tile. Stage it as
-          // 128-byte-swizzled boxes of [32 d rows][32 q] fp32, two boxes per
-          // warp and half-tile, and add each box into the accumulator with a
+          // dQ: lane = query row of the tile, column = d. Stage it as
+          // 128-byte-swizzled boxes of [32 q rows][32 d] fp32, two boxes per
+          // warp and half of d, and add each box into the accumulator with a
           // TMA reduction; the buffer is rewritten once the previous
           // reductions have read it.
           uint8_t* stg = smem + C::kOffStg + wq * 8192;
@@ -500,20 +501,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
 #pragma unroll
             for (int b2 = 0; b2 < 2; ++b2) {
-              const int qb = half * 2 + b2;
+              const int db = half * 2 + b2;  // d block of 32
               uint8_t* box = stg + b2 * 4096 + lane * 128;
 #pragma unroll
               for (int u = 0; u < 8; ++u)
                 *reinterpret_cast<uint4*>(box + ((u ^ (lane & 7)) << 4)) =
-                    make_uint4(v[qb * 32 + 4 * u], v[qb * 32 + 4 * u + 1], v[qb * 32 + 4 * u + 2],
-                               v[qb * 32 + 4 * u + 3]);
+                    make_uint4(v[db * 32 + 4 * u], v[db * 32 + 4 * u + 1], v[db * 32 + 4 * u + 2],
+                               v[db * 32 + 4 * u + 3]);
             }
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
 #pragma unroll
               for (int b2 = 0; b2 < 2; ++b2)
-                tma_reduce_add_4d(&out.acc, stg + b2 * 4096, it * 128 + (half * 2 + b2) * 32, wq * 32, h, ib);
+                tma_reduce_add_4d(&out.acc, stg + b2 * 4096, (half * 2 + b2) * 32, it * 128 + wq * 32, h, ib);
               bulk_commit();
             }
           }
@@ -738,8 +739,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           ctl.cur[warp] = Cur{t, tb, tk};  // one thread runs this role
         }
         const Item& I = ctl.cur[warp].I;
-        const int& ib = ctl.cur[warp].b;
-        const int& ikvh = ctl.cur[warp].kvh;
         if (I.steps == 0) continue;
         ok = mbar_wait_bounded(&ctl.kv_full, nkv & 1, abort_flag, LIM);
         if (ok) ok = mbar_wait_bounded(&ctl.q_full[g & 1], (g >> 1) & 1, abort_flag, LIM);
@@ -786,7 +785,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ph_ds ^= 1;
           trace_stamp(p.trace, g, 3);
           tc_fence_after();
-          // dK first, then dQ^T (issuing dQ^T first, so that its drain overlaps
+          // dK first, then dQ (issuing dQ first, so that its drain overlaps
           // dK, measured 0.5-1 % slower)
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {  // dK += dS^T Q   (dS^T K-major, Q MN-major)
@@ -797,10 +796,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_commit(&ctl.q_empty[g & 1]);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
-            if (D == 128)  // dQ^T = K^T dS^T  (both MN-major)
-              mma_ss_lo(tmem + C::kColDP, sdesc_step(mK, kk * 2048), sdesc_step(mDs, kk * 2048), idDQ, kk > 0);
-            else  // dQ = dS K  (both MN-major)
-              mma_ss_lo(tmem + C::kColDP, sdesc_step(mDs, kk * 2048), sdesc_step(mK, kk * 2048), idDQ, kk > 0);
+            // dQ = dS K  (both MN-major): lane = query row, column = d
+            mma_ss_lo(tmem + C::kColDP, sdesc_step(mDs, kk * 2048), sdesc_step(mK, kk * 2048), idDQ, kk > 0);
           }
           mma_commit(&ctl.dq_full);
           trace_stamp(p.trace, g, 4);
@@ -830,33 +827,48 @@ __global__ void __launch_bounds__(kThreads, 1)
 // [B*Hq, Nq_pad] arrays; padded rows and rows with LSE = -inf get +inf (so
 // their probabilities recompute to 0) and D = 0. Also zeroes the fp32 dQ
 // accumulator.
+// Work is split into groups of 16 consecutive query rows of one (batch,
+// head), one group per warp at a time: the warp loads the group's O and dO
+// rows (16 bytes per lane per row piece, all loads issued before any is
+// used), zeroes an equal share of the accumulator meanwhile, then writes the
+// group's 16 LSE/D values as one contiguous run.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* o, const __nv_bfloat16* dout,
                                                       const float* lse, float* lse2, float* delta, float* dq_acc,
                                                       int B, int Hq, int Nq, int Nq_pad) {
-  constexpr int TPR = D / 8;     // threads per row, 8 elements (16 bytes) each
-  constexpr int RPW = 32 / TPR;  // rows a warp covers per pass
-  constexpr int R = 4;           // passes whose loads are issued before any is reduced
-  const long long rows = 1LL * B * Nq * Hq;
+  constexpr int TPR = D / 8;          // lanes per row, 8 elements (16 bytes) each
+  constexpr int RPP = 32 / TPR;       // rows per pass of the warp
+  constexpr int kRows = 16;           // rows per group
+  constexpr int kPass = kRows / RPP;  // passes per group
   const int lane = threadIdx.x & 31;
   const int part = lane % TPR, sub = lane / TPR;
-  const long long tid = 1LL * blockIdx.x * blockDim.x + threadIdx.x;
-  const long long nthreads = 1LL * gridDim.x * blockDim.x;
-  const long long wstep = (nthreads >> 5) * RPW * R;
-  // the loop bound is the same for all lanes of a warp (the shuffles need all 32)
-  for (long long r0 = (tid >> 5) * RPW * R; r0 < rows; r0 += wstep) {
-    uint4 a[R], g[R];
+  const long long warp_id = (1LL * blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const long long n_warps = (1LL * gridDim.x * blockDim.x) >> 5;
+  const int gq = (Nq + kRows - 1) / kRows;  // groups per (batch, head)
+  const long long n_groups = 1LL * B * Hq * gq;
+  const long long n4 = 1LL * B * Hq * D * Nq_pad / 4;  // accumulator, in float4
+  const long long zc = (n4 + n_groups - 1) / n_groups;  // float4 zeroed per group
+  float4* acc4 = reinterpret_cast<float4*>(dq_acc);
+  for (long long grp = warp_id; grp < n_groups; grp += n_warps) {
+    const long long bh = grp / gq;
+    const int q0 = int(grp - bh * gq) * kRows;
+    const int b = int(bh / Hq), h = int(bh - 1LL * b * Hq);
+    uint4 a[kPass], g[kPass];
 #pragma unroll
-    for (int i = 0; i < R; ++i) {
-      const long long r = r0 + i * RPW + sub;
+    for (int i = 0; i < kPass; ++i) {
+      const int q = q0 + i * RPP + sub;
       a[i] = g[i] = make_uint4(0, 0, 0, 0);
-      if (r < rows) {
-        a[i] = *reinterpret_cast<const uint4*>(o + r * D + part * 8);
-        g[i] = *reinterpret_cast<const uint4*>(dout + r * D + part * 8);
+      if (q < Nq) {
+        const size_t off = ((size_t(b) * Nq + q) * Hq + h) * D + part * 8;
+        a[i] = *reinterpret_cast<const uint4*>(o + off);
+        g[i] = *reinterpret_cast<const uint4*>(dout + off);
       }
     }
+    const long long z1 = (grp + 1) * zc < n4 ? (grp + 1) * zc : n4;
+    for (long long z = grp * zc + lane; z < z1; z += 32) acc4[z] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    float mine = 0.0f;  // lane t < 16: D of the group's row t
 #pragma unroll
-    for (int i = 0; i < R; ++i) {
+    for (int i = 0; i < kPass; ++i) {
       const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a[i]);
       const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&g[i]);
       float acc = 0.0f;
@@ -868,21 +880,21 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* o, co
       }
 #pragma unroll
       for (int m = TPR / 2; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
-      const long long r = r0 + i * RPW + sub;
-      if (r < rows && part == 0) {
-        // r indexes [B, Nq, Hq]
-        const int h = int(r % Hq);
-        const long long bq = r / Hq;
-        const int q = int(bq % Nq);
-        const int b = int(bq / Nq);
-        const size_t dst = (size_t(b) * Hq + h) * Nq_pad + q;
-        const float l = lse[(size_t(b) * Hq + h) * Nq + q];
-        lse2[dst] = l == -INFINITY ? INFINITY : l * 1.4426950408889634f;
-        delta[dst] = acc;
-      }
+      // row i * RPP + r sits in lanes [r * TPR, r * TPR + TPR)
+      const float v = __shfl_sync(0xffffffffu, acc, (lane % RPP) * TPR);
+      if (lane / RPP == i) mine = v;
+    }
+    const int q = q0 + lane;
+    if (lane < kRows && q < Nq) {
+      const size_t dst = size_t(bh) * Nq_pad + q;
+      const float l = lse[size_t(bh) * Nq + q];
+      lse2[dst] = l == -INFINITY ? INFINITY : l * 1.4426950408889634f;
+      delta[dst] = mine;
     }
   }
   // padded rows
+  const long long tid = 1LL * blockIdx.x * blockDim.x + threadIdx.x;
+  const long long nthreads = 1LL * gridDim.x * blockDim.x;
   const long long pad = 1LL * B * Hq * (Nq_pad - Nq);
   for (long long i = tid; i < pad; i += nthreads) {
     const long long bh = i / (Nq_pad - Nq);
@@ -890,18 +902,52 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* o, co
     lse2[bh * Nq_pad + q] = INFINITY;
     delta[bh * Nq_pad + q] = 0.0f;
   }
-  // zero the dQ accumulator, four 16-byte stores per thread per pass
-  const long long n4 = 1LL * B * Hq * D * Nq_pad / 4;
-  float4* acc4 = reinterpret_cast<float4*>(dq_acc);
-  const float4 z = make_float4(0, 0, 0, 0);
-  for (long long i = tid; i < n4; i += 4 * nthreads) {
+}
+
+// d = 128: dq[b, q, h, :] = bf16(scale * acc[b*Hq + h, q, :]) (the
+// accumulator is row-major there), a streaming pass: 16 lanes per row, each
+// reading 32 bytes and writing 16, four row pieces per thread in flight.
+__global__ void __launch_bounds__(256) bwd_post_rows_kernel(const float* dq_acc, __nv_bfloat16* dq, int B, int Hq,
+                                                            int Nq, int Nq_pad, float scale) {
+  constexpr int D = 128, TPR = D / 8, U = 4;
+  const long long n = 1LL * B * Hq * Nq * TPR;  // 8-element pieces
+  const long long tid = 1LL * blockIdx.x * blockDim.x + threadIdx.x;
+  const long long nth = 1LL * gridDim.x * blockDim.x;
+  for (long long base = tid; base < n; base += U * nth) {
+    float4 x[U][2];
 #pragma unroll
-    for (int u = 0; u < 4; ++u)
-      if (i + u * nthreads < n4) acc4[i + u * nthreads] = z;
+    for (int u = 0; u < U; ++u) {
+      const long long idx = base + u * nth;
+      if (idx < n) {
+        const long long row = idx / TPR;  // (b*Hq + h)*Nq + q
+        const int part = int(idx - row * TPR);
+        const long long bh = row / Nq;
+        const int q = int(row - bh * Nq);
+        const float4* src = reinterpret_cast<const float4*>(dq_acc + (size_t(bh) * Nq_pad + q) * D + part * 8);
+        x[u][0] = __ldcs(src);
+        x[u][1] = __ldcs(src + 1);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const long long idx = base + u * nth;
+      if (idx < n) {
+        const long long row = idx / TPR;
+        const int part = int(idx - row * TPR);
+        const long long bh = row / Nq;
+        const int q = int(row - bh * Nq);
+        const int b = int(bh / Hq), h = int(bh - 1LL * b * Hq);
+        *reinterpret_cast<uint4*>(dq + ((size_t(b) * Nq + q) * Hq + h) * D + part * 8) =
+            make_uint4(pack_bf16x2(x[u][0].x * scale, x[u][0].y * scale),
+                       pack_bf16x2(x[u][0].z * scale, x[u][0].w * scale),
+                       pack_bf16x2(x[u][1].x * scale, x[u][1].y * scale),
+                       pack_bf16x2(x[u][1].z * scale, x[u][1].w * scale));
+      }
+    }
   }
 }
 
-// dq[b, q, h, :] = bf16(scale * acc[b*Hq + h, :, q]), through a shared
+// d = 64: dq[b, q, h, :] = bf16(scale * acc[b*Hq + h, :, q]), through a shared
 // tile: a block takes 64 queries of one (batch, head); each warp reads whole
 // 256-byte runs of accumulator rows (one d, 64 q), then every thread writes
 // 16-byte pieces of dq rows (16 consecutive threads write one 256-byte row
@@ -975,11 +1021,11 @@ cudaError_t launch_t(const Problem& pb, const void* o, const float* lse, const v
   float* lse2 = ws + acc_elems;
   float* delta = lse2 + size_t(pb.B) * pb.Hq * Nq_pad;
   {
-    // 8 warps a block, 32 / (D / 8) rows a warp per pass, 4 passes per load batch
-    const long long rows_per_block = 8LL * (32 / (D / 8)) * 4;
-    long long blocks = (1LL * pb.B * pb.Nq * pb.Hq + rows_per_block - 1) / rows_per_block;
-    const long long minb = 4LL * num_sms(), maxb = 32LL * num_sms();
-    if (blocks < minb) blocks = minb;
+    // 8 warps a block, one group of 16 query rows per warp at a time; at
+    // most 8 blocks per SM, so the blocks are resident together
+    const long long groups = 1LL * pb.B * pb.Hq * ((pb.Nq + 15) / 16);
+    long long blocks = (groups + 7) / 8;
+    const long long maxb = 8LL * num_sms();
     if (blocks > maxb) blocks = maxb;
     bwd_pre_kernel<D><<<unsigned(blocks), 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(o),
                                                              static_cast<const __nv_bfloat16*>(dout), lse, lse2, delta,
@@ -994,10 +1040,10 @@ cudaError_t launch_t(const Problem& pb, const void* o, const float* lse, const v
       !make_bshd_map(&mdo, dout, pb.B, pb.Nq, pb.Hq, D, 128) || !make_bshd_map(&out.dk, dk, pb.B, pb.Nk, pb.Hkv, D, 32) ||
       !make_bshd_map(&out.dv, dv, pb.B, pb.Nk, pb.Hkv, D, 32))
     return cudaErrorInvalidValue;
-  // out.acc: the fp32 accumulator [B, Hq, D, Nq_pad], boxes of 32 q x 32 d
+  // out.acc (d = 128): the fp32 accumulator [B, Hq, Nq_pad, D], boxes of 32 q x 32 d
   {
-    const uint64_t dims[4] = {uint64_t(Nq_pad), uint64_t(D), uint64_t(pb.Hq), uint64_t(pb.B)};
-    const uint64_t strides[3] = {uint64_t(Nq_pad) * 4, uint64_t(D) * Nq_pad * 4, uint64_t(pb.Hq) * D * Nq_pad * 4};
+    const uint64_t dims[4] = {uint64_t(D), uint64_t(Nq_pad), uint64_t(pb.Hq), uint64_t(pb.B)};
+    const uint64_t strides[3] = {uint64_t(D) * 4, uint64_t(D) * Nq_pad * 4, uint64_t(pb.Hq) * D * Nq_pad * 4};
     const uint32_t box[4] = {32, 32, 1, 1};
     if (!encode_tiled(&out.acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dq_acc, dims, strides, box,
                       CU_TENSOR_MAP_SWIZZLE_128B))
@@ -1044,7 +1090,13 @@ cudaError_t launch_t(const Problem& pb, const void* o, const float* lse, const v
   e = cudaGetLastError();
   if (dc.ev_end) cudaEventRecord(dc.ev_end, stream);
   if (e != cudaSuccess) return e;
-  {
+  if (D == 128) {
+    const long long pieces = 1LL * pb.B * pb.Hq * pb.Nq * (D / 8);
+    long long blocks = (pieces + 4 * 256 - 1) / (4 * 256);
+    if (blocks > 8LL * num_sms()) blocks = 8LL * num_sms();
+    bwd_post_rows_kernel<<<unsigned(blocks), 256, 0, stream>>>(dq_acc, static_cast<__nv_bfloat16*>(dq), pb.B, pb.Hq,
+                                                              pb.Nq, Nq_pad, pb.scale);
+  } else {
     const long long blocks = 1LL * pb.B * pb.Hq * (Nq_pad / 64);
     bwd_post_kernel<D><<<unsigned(blocks), 256, 0, stream>>>(
         dq_acc, static_cast<__nv_bfloat16*>(dq), pb.B * pb.Hq, pb.Hq, pb.Nq, Nq_pad, pb.scale);
