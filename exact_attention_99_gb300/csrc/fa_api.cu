@@ -33,6 +33,19 @@ cudaMemPool_t g_pool[kMaxDevices];
 // direction made the end-to-end step slower (1.44 instead of 1.19 ms).
 constexpr int kCopyLanes = 1;
 cudaStream_t g_copy[kMaxDevices][2 * kCopyLanes];
+// fa_step_host: two device buffers per device, used by alternate calls, so
+// that a call's input copies can run while the previous call computes. A
+// buffer is released (event on the caller's stream) once its call's last
+// copy and kernel have finished; the call after next waits for that.
+struct StepSlots {
+  void* buf[2];
+  size_t cap[2];
+  cudaEvent_t released[2];
+  bool pending[2];
+  int next;
+};
+std::mutex g_step_mu;  // held for a whole fa_step_host enqueue
+StepSlots g_step[kMaxDevices];
 unsigned* g_status_ptr[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 DebugCfg g_debug = {kDefaultWaitNs, 0, nullptr, nullptr, nullptr, 0, 0};
@@ -418,23 +431,46 @@ extern "C" int fa_step_host(const void* q, const void* k, const void* v, const v
   const size_t bl = (nl * 4 + 15) & ~size_t(15);
   const size_t per = 4 * bq + 4 * bk + bl;
   const int n_chunks = B * C;
-  cudaMemPool_t pool = workspace_pool();
-  void* ws = nullptr;
-  if (pool == nullptr || cudaMallocFromPoolAsync(&ws, per * size_t(n_chunks), pool, s) != cudaSuccess) {
+  const int dev = current_device();
+  if (dev < 0) return FA_ERR_LAUNCH;
+  std::lock_guard<std::mutex> step_lock(g_step_mu);
+  StepSlots& slots = g_step[dev];
+  const int slot = slots.next;
+  slots.next ^= 1;
+  if (slots.released[slot] == nullptr &&
+      cudaEventCreateWithFlags(&slots.released[slot], cudaEventDisableTiming) != cudaSuccess) {
+    slots.released[slot] = nullptr;
     cudaGetLastError();
-    return FA_ERR_ALLOC;
+    return FA_ERR_LAUNCH;
   }
-  // events: [0] start; one set per chunk, reused for every chunk (each
-  // record is waited on before it is recorded again): per copy lane "q, k, v
-  // in" and "dout in", then "forward done" and "backward done"; then one
-  // "done" per copy stream
+  const size_t need = per * size_t(n_chunks);
+  if (slots.cap[slot] < need) {  // grow: wait for the buffer's last user, then reallocate
+    if (slots.pending[slot]) cudaEventSynchronize(slots.released[slot]);
+    if (slots.buf[slot] != nullptr) cudaFree(slots.buf[slot]);
+    slots.buf[slot] = nullptr;
+    slots.cap[slot] = 0;
+    slots.pending[slot] = false;
+    if (cudaMalloc(&slots.buf[slot], need) != cudaSuccess) {
+      slots.buf[slot] = nullptr;
+      cudaGetLastError();
+      return FA_ERR_ALLOC;
+    }
+    slots.cap[slot] = need;
+  }
+  void* ws = slots.buf[slot];
+  // events: one set per chunk, reused for every chunk (each record is
+  // waited on before it is recorded again): per copy lane "q, k, v in" and
+  // "dout in", then "forward done" and "backward done"; then one "done" per
+  // copy stream
   const size_t per_c = 2 * kCopyLanes + 2;
-  std::vector<cudaEvent_t> ev(1 + per_c + 2 * kCopyLanes, nullptr);
+  std::vector<cudaEvent_t> ev(per_c + 2 * kCopyLanes, nullptr);
   bool ok = true;
   for (auto& e : ev) ok = ok && cudaEventCreateWithFlags(&e, cudaEventDisableTiming) == cudaSuccess;
-  if (ok) {
-    ok = cudaEventRecord(ev[0], s) == cudaSuccess;
-    for (int i = 0; i < 2 * kCopyLanes && ok; ++i) ok = cudaStreamWaitEvent(cs[i], ev[0], 0) == cudaSuccess;
+  // the copies wait only for the previous user of this buffer (two calls
+  // back), not for earlier work on the caller's stream
+  if (ok && slots.pending[slot]) {
+    for (int i = 0; i < 2 * kCopyLanes && ok; ++i)
+      ok = cudaStreamWaitEvent(cs[i], slots.released[slot], 0) == cudaSuccess;
   }
   const auto* hq_ = static_cast<const uint8_t*>(q);
   const auto* hk_ = static_cast<const uint8_t*>(k);
@@ -484,7 +520,7 @@ extern "C" int fa_step_host(const void* q, const void* k, const void* v, const v
     uint8_t *wk = w + 4 * bq, *wv = wk + bk, *wdk = wk + 2 * bk, *wdv = wk + 3 * bk;
     float* wl = reinterpret_cast<float*>(wk + 4 * bk);
     const size_t qoff = size_t(b) * Nq * Hq * d * e2, koff = size_t(b) * Nk * Hkv * d * e2;
-    cudaEvent_t* ec = ev.data() + 1;
+    cudaEvent_t* ec = ev.data();
     // the forward needs q, k, v; dout follows while it runs
     ok = in(wq, hq_ + qoff, Nq, Hq, q0, hq) && in(wk, hk_ + koff, Nk, Hkv, k0, hk) &&
          in(wv, hv_ + koff, Nk, Hkv, k0, hk);
@@ -508,15 +544,16 @@ extern "C" int fa_step_host(const void* q, const void* k, const void* v, const v
     ok = ok && out(hdq + qoff, wdq, Nq, Hq, q0, hq) && out(hdk + koff, wdk, Nk, Hkv, k0, hk) &&
          out(hdv + koff, wdv, Nk, Hkv, k0, hk);
   }
-  // the caller's stream waits for every copy stream, then frees the workspace
+  // the caller's stream waits for every copy stream, then releases the buffer
   for (int i = 0; i < 2 * kCopyLanes; ++i) {
-    cudaEvent_t e = ev[1 + per_c + i];
+    cudaEvent_t e = ev[per_c + i];
     if (e != nullptr && cudaEventRecord(e, cs[i]) == cudaSuccess) cudaStreamWaitEvent(s, e, 0);
   }
-  const bool freed = cudaFreeAsync(ws, s) == cudaSuccess;
+  const bool released = cudaEventRecord(slots.released[slot], s) == cudaSuccess;
+  slots.pending[slot] = released;
   for (auto& e : ev)
     if (e != nullptr) cudaEventDestroy(e);
-  if (!ok || !freed) {
+  if (!ok || !released) {
     cudaGetLastError();
     return FA_ERR_LAUNCH;
   }

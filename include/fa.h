@@ -150,12 +150,18 @@ int fa_bwd_window(const void* q, const void* k, const void* v, const void* o, co
  * Hkv is cut into two halves of its kv heads (each with its query heads),
  * copied as 2-D slices of the head dimension. The call only enqueues; `stream` is ordered after all
  * of it, so synchronise `stream` before reading the outputs, and keep every
- * host buffer alive (and the inputs unchanged) until then. Page-locked host
- * memory gives asynchronous, full-speed copies; pageable memory works but
- * the copies are staged by the driver.
- * Device memory: a copy of every tensor of the batch (about the size of
- * all inputs and outputs) from the same stream-ordered pool as fa_bwd,
- * freed on `stream` at the end, plus the backward's own workspace.
+ * host buffer alive (and the inputs unchanged) until then. The input copies
+ * do not wait for earlier work on `stream`: the host inputs must hold their
+ * values when the call is made. Consecutive calls therefore overlap: the
+ * inputs of one call are copied in while the previous call computes.
+ * Page-locked host memory gives asynchronous, full-speed copies; pageable
+ * memory works but the copies are staged by the driver.
+ * Device memory: two library-owned buffers per device, each a copy of every
+ * tensor of the batch (about the size of all inputs and outputs), used by
+ * alternate calls and kept (grown to the largest call) until the process
+ * exits; a call waits only for the call two before it to release its
+ * buffer. Calls from several host threads on one device are serialised
+ * while they enqueue. Plus the backward's own workspace from its pool.
  * Errors: a null pointer or a bad size gives FA_ERR_INVALID_ARG /
  * FA_ERR_UNSUPPORTED before anything is enqueued; FA_ERR_ALLOC if the device
  * copy cannot be allocated; FA_ERR_LAUNCH if a copy, launch or event call

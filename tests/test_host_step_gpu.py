@@ -78,3 +78,39 @@ def test_step_host_matches_device_calls(fa, case, pinned):
     # 2e-2: the bound grows with the value (assert_close_scaled)
     for name, ref in zip(("dq", "dk", "dv"), attn_ref.backward(*xs, scale, causal)):
         assert_close_scaled(f"{name} vs oracle", to64(outs[name]), ref)
+
+
+def test_step_host_back_to_back(fa):
+    """Consecutive calls overlap (the inputs of one call are copied in while
+    the previous one computes; the device buffers alternate between calls):
+    three calls enqueued without a synchronisation in between, each on its
+    own inputs and outputs, so that the third reuses the first one's device
+    buffer, all match the device calls on their inputs."""
+    B, Hq, Hkv, Nq, Nk, d, causal = 1, 8, 2, 700, 700, 128, True
+    args = (B, Hq, Hkv, Nq, Nk, d, 1.0 / math.sqrt(d), int(causal))
+    runs = []
+    for seed in (11, 12, 13):
+        x = workloads.make_inputs(B, Hq, Hkv, Nq, Nk, d, seed=seed, with_dout=True)
+        host = {n: x[n].pin_memory() for n in ("q", "k", "v", "do")}
+        outs = {n: torch.full(s, float("nan"), dtype=t, pin_memory=True)
+                for n, s, t in (("o", (B, Nq, Hq, d), torch.bfloat16), ("lse", (B, Hq, Nq), torch.float32),
+                                ("dq", (B, Nq, Hq, d), torch.bfloat16), ("dk", (B, Nk, Hkv, d), torch.bfloat16),
+                                ("dv", (B, Nk, Hkv, d), torch.bfloat16))}
+        runs.append((x, host, outs))
+    torch.cuda.synchronize()
+    for x, host, outs in runs:
+        assert fa.fa_step_host(host["q"], host["k"], host["v"], host["do"], outs["o"], outs["lse"], outs["dq"],
+                               outs["dk"], outs["dv"], *args) == 0
+    torch.cuda.synchronize()
+    assert fa.fa_get_status() == 0
+    for x, host, outs in runs:
+        q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
+        o, lse = torch.empty_like(q), torch.empty((B, Hq, Nq), device="cuda", dtype=torch.float32)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        assert fa.fa_fwd(q, k, v, o, lse, *args) == 0
+        assert fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, *args) == 0
+        torch.cuda.synchronize()
+        assert torch.equal(outs["o"], o.cpu())
+        assert torch.equal(outs["lse"], lse.cpu())
+        for name, ref in (("dq", dq), ("dk", dk), ("dv", dv)):
+            assert_close(name, to64(outs[name]), to64(ref.cpu()))
