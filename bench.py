@@ -481,19 +481,21 @@ def fp8_peak(peak_bf16: float):
 
 
 def fp8_config(fa, flush, peak):
-    """The e4m3 forward (incoherent transform on) of the two d = 128 forward
+    """The e4m3 forward (incoherent transform on) of the three d = 128 forward
     workloads: whole call (quantisation included) and the attention kernel
-    alone, against the measured dense e4m3 peak (fp8_peak)."""
+    alone, against the measured dense e4m3 peak (fp8_peak), beside the bf16
+    forward call on the same inputs."""
     import torch
     p8, p8_src = fp8_peak(peak)
     out = {"fp8_peak": {"tflops": round(p8, 1), "source": p8_src}}
-    for w in (workloads.WORKLOADS[1], workloads.WORKLOADS[2]):
+    for w in (workloads.WORKLOADS[1], workloads.WORKLOADS[2], workloads.WORKLOADS[3]):
         x = workloads.workload_inputs(w)
         q, k, v = (x[n].cuda() for n in ("q", "k", "v"))
         o = torch.empty_like(q)
         lse = torch.empty((w.B, w.Hq, w.Nq), device="cuda", dtype=torch.float32)
         a = (w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.d, w.scale, int(w.causal), 1)
         ms = time_one(lambda: fa.fa_fwd_fp8(q, k, v, o, lse, *a), flush)
+        ms16 = time_one(lambda: fa.fa_fwd(q, k, v, o, lse, *a[:-1]), flush)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(); e1.record()
         ks = []
@@ -507,6 +509,7 @@ def fp8_config(fa, flush, peak):
         kms = statistics.median(ks)
         fl = w.fwd_flops()
         out["fp8_" + w.name] = {"call_ms": round(ms, 4), "call_tflops": round(fl / ms / 1e9, 2),
+                                "bf16_call_ms": round(ms16, 4), "call_vs_bf16": round(ms16 / ms, 4),
                                 "kernel_ms": round(kms, 4), "kernel_tflops": round(fl / kms / 1e9, 2),
                                 "kernel_frac_of_fp8_peak": round(fl / kms / 1e9 / p8, 4)}
         del q, k, v, o, lse
