@@ -300,6 +300,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // launched while the pre-pass may still run: its LSE/D rows and the zeroed
+  // accumulator are read below
+  grid_dep_wait();
+  grid_dep_launch();
   const uint32_t tmem = ctl.tmem_base;
   uint8_t* sK = smem + C::kOffK;
   uint8_t* sV = smem + C::kOffV;
@@ -836,6 +840,7 @@ template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* o, const __nv_bfloat16* dout,
                                                       const float* lse, float* lse2, float* delta, float* dq_acc,
                                                       int B, int Hq, int Nq, int Nq_pad) {
+  grid_dep_launch();  // the main kernel may start its set-up meanwhile
   constexpr int TPR = D / 8;          // lanes per row, 8 elements (16 bytes) each
   constexpr int RPP = 32 / TPR;       // rows per pass of the warp
   constexpr int kRows = 16;           // rows per group
@@ -909,6 +914,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* o, co
 // reading 32 bytes and writing 16, four row pieces per thread in flight.
 __global__ void __launch_bounds__(256) bwd_post_rows_kernel(const float* dq_acc, __nv_bfloat16* dq, int B, int Hq,
                                                             int Nq, int Nq_pad, float scale) {
+  grid_dep_wait();  // launched while the main kernel may still run
   constexpr int D = 128, TPR = D / 8, U = 4;
   const long long n = 1LL * B * Hq * Nq * TPR;  // 8-element pieces
   const long long tid = 1LL * blockIdx.x * blockDim.x + threadIdx.x;
@@ -955,6 +961,7 @@ __global__ void __launch_bounds__(256) bwd_post_rows_kernel(const float* dq_acc,
 template <int D>
 __global__ void __launch_bounds__(256) bwd_post_kernel(const float* dq_acc, __nv_bfloat16* dq, int BH, int Hq, int Nq,
                                                        int Nq_pad, float scale) {
+  grid_dep_wait();  // launched while the main kernel may still run
   __shared__ float tile[D][65];
   const int nqt = Nq_pad / 64;
   const int bh = blockIdx.x / nqt, qt = blockIdx.x - bh * nqt;
@@ -1086,7 +1093,20 @@ cudaError_t launch_t(const Problem& pb, const void* o, const float* lse, const v
   p.n_units = int(units);
   const unsigned grid = unsigned(std::min<long long>(units, num_sms()));  // persistent CTAs, one per SM
   if (dc.ev_begin) cudaEventRecord(dc.ev_begin, stream);
-  kern<<<grid, kThreads, smem, stream>>>(mq, mk, mv, mdo, out, p);
+  // programmatic stream serialisation: the kernel may be scheduled while
+  // the pre-pass finishes (it waits for the pre-pass after its set-up)
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(grid);
+  lc.blockDim = dim3(kThreads);
+  lc.dynamicSmemBytes = smem;
+  lc.stream = stream;
+  lc.attrs = pdl;
+  lc.numAttrs = 1;
+  e = cudaLaunchKernelEx(&lc, kern, mq, mk, mv, mdo, out, p);
+  if (e != cudaSuccess) return e;
   e = cudaGetLastError();
   if (dc.ev_end) cudaEventRecord(dc.ev_end, stream);
   if (e != cudaSuccess) return e;
@@ -1094,12 +1114,20 @@ cudaError_t launch_t(const Problem& pb, const void* o, const float* lse, const v
     const long long pieces = 1LL * pb.B * pb.Hq * pb.Nq * (D / 8);
     long long blocks = (pieces + 4 * 256 - 1) / (4 * 256);
     if (blocks > 8LL * num_sms()) blocks = 8LL * num_sms();
-    bwd_post_rows_kernel<<<unsigned(blocks), 256, 0, stream>>>(dq_acc, static_cast<__nv_bfloat16*>(dq), pb.B, pb.Hq,
-                                                              pb.Nq, Nq_pad, pb.scale);
+    lc.gridDim = dim3(unsigned(blocks));
+    lc.blockDim = dim3(256);
+    lc.dynamicSmemBytes = 0;
+    e = cudaLaunchKernelEx(&lc, bwd_post_rows_kernel, dq_acc, static_cast<__nv_bfloat16*>(dq), pb.B, pb.Hq, pb.Nq,
+                           Nq_pad, pb.scale);
+    if (e != cudaSuccess) return e;
   } else {
     const long long blocks = 1LL * pb.B * pb.Hq * (Nq_pad / 64);
-    bwd_post_kernel<D><<<unsigned(blocks), 256, 0, stream>>>(
-        dq_acc, static_cast<__nv_bfloat16*>(dq), pb.B * pb.Hq, pb.Hq, pb.Nq, Nq_pad, pb.scale);
+    lc.gridDim = dim3(unsigned(blocks));
+    lc.blockDim = dim3(256);
+    lc.dynamicSmemBytes = 0;
+    e = cudaLaunchKernelEx(&lc, bwd_post_kernel<D>, dq_acc, static_cast<__nv_bfloat16*>(dq), pb.B * pb.Hq, pb.Hq,
+                           pb.Nq, Nq_pad, pb.scale);
+    if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
 }

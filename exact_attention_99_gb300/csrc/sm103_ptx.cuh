@@ -174,6 +174,14 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialisation may start while the previous kernel in the stream still
+// runs; grid_dep_wait() blocks until that kernel has completed and its
+// memory operations are visible (a no-op without the launch attribute).
+// grid_dep_launch() lets the next such kernel start launching.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Generic-proxy writes to shared memory that the tensor core (async proxy)
 // reads afterwards must be made visible with this fence.
 __device__ __forceinline__ void fence_proxy_async_smem() {
