@@ -18,7 +18,7 @@ import math
 import os
 
 __all__ = ["FAError", "lib", "fa_fwd", "fa_bwd", "fa_bwd_noalloc", "fa_get_status", "fa_status_string", "fa_debug_set",
-           "fa_debug_exp2", "fa_tune", "TUNE_EXP2_SPLIT", "TUNE_CTA_PAIRS", "fa_profile_events", "fa_trace", "forward", "backward", "STATUS"]
+           "fa_debug_exp2", "fa_tune", "TUNE_EXP2_SPLIT", "TUNE_CTA_PAIRS", "TUNE_BWD_SPLIT", "fa_profile_events", "fa_trace", "forward", "backward", "STATUS"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libfa.so")
@@ -194,13 +194,16 @@ def fa_trace(buf=None) -> int:
 
 TUNE_EXP2_SPLIT = 1
 TUNE_CTA_PAIRS = 2
+TUNE_BWD_SPLIT = 3
 
 
 def fa_tune(knob: int, value: int) -> int:
     """Process-wide tuning knob (see fa.h fa_tune); TUNE_EXP2_SPLIT: 0 = every
     forward exponential on the special-function unit, N in {1, 2, 4, 8} = one
     column pair in every N on the FMA-pipe polynomial; TUNE_CTA_PAIRS: 1 = the
-    d = 128 forward on pairs of CTAs (cta_group::2), 0 = one CTA per SM."""
+    d = 128 forward on pairs of CTAs (cta_group::2), 0 = one CTA per SM;
+    TUNE_BWD_SPLIT: -1 = the causal backward's split count from its model,
+    m >= 0 = that many pairs per kv head run as single tiles."""
     return lib().fa_tune(int(knob), int(value))
 
 

@@ -48,7 +48,7 @@ std::mutex g_step_mu;  // held for a whole fa_step_host enqueue
 StepSlots g_step[kMaxDevices];
 unsigned* g_status_ptr[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-DebugCfg g_debug = {kDefaultWaitNs, 0, nullptr, nullptr, nullptr, 0, 0};
+DebugCfg g_debug = {kDefaultWaitNs, 0, nullptr, nullptr, nullptr, 0, 0, -1};
 
 int current_device() {
   int dev = -1;
@@ -378,6 +378,12 @@ extern "C" int fa_tune(int knob, int value) {
     if (value != 0 && value != 1) return FA_ERR_INVALID_ARG;
     std::lock_guard<std::mutex> lk(g_mu);
     g_debug.cta_pairs = value;
+    return FA_OK;
+  }
+  if (knob == FA_TUNE_BWD_SPLIT) {
+    if (value < -1) return FA_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_debug.bwd_split = value;
     return FA_OK;
   }
   return FA_ERR_INVALID_ARG;

@@ -82,7 +82,10 @@ struct Item {
   int j;      // key tile
   int i0;     // first query tile that sees it
   int nq;     // query tiles per head
-  int steps;  // group * nq
+  int h0;     // first query head of the group that the item takes
+  int nh;     // query heads it takes: the whole group, or one (a tail piece)
+  int tt;     // tail tile index of a piece (its dK/dV are partial sums), else -1
+  int steps;  // nh * nq
 };
 struct Work {
   int b, kvh, n_items;
@@ -90,10 +93,11 @@ struct Work {
 };
 
 // The maps the dQ drain writes through, in one kernel parameter so that one
-// base address serves all three: the fp32 dQ accumulator (reductions), dK
-// and dV (stores).
+// base address serves them all: the fp32 dQ accumulator (reductions), dK
+// and dV (stores), and the fp32 partial dK/dV of tail pieces (stores).
 struct OutMaps {
   CUtensorMap acc, dk, dv;
+  CUtensorMap dkv;  // tail pieces: fp32 [B*Hkv*n_tail*group][2][128][D], boxes of 32 rows x 32 d
 };
 
 struct Cur {  // a warp's current item, kept in shared memory (see below)
@@ -124,6 +128,12 @@ struct Params {
   // head, the last n_split (those nearest the middle, both tiles about half
   // a pair's work) run as two single-tile CTAs each, after every whole pair
   int n_split;
+  // GQA tail pieces (d = 128): the single tiles are split further, one unit
+  // per query head of the group; such a unit stores its partial dK/dV in
+  // its own slot of the fp32 buffer [B*Hkv, n_tail, group, 2 (dV, dK), 128,
+  // D], which a last pass sums in a fixed order (so dK, dV stay
+  // deterministic). n_tail = 2 * n_split + (n_ktiles & 1) tiles per kv head.
+  int head_split, n_tail;
   // work units (a pair or a single key tile of one (batch, kv head)); the
   // CTAs are persistent: CTA c runs units c, c + gridDim.x, ...
   int n_units;
@@ -150,10 +160,16 @@ __device__ __forceinline__ int win_l(const Params& p) { return WIN ? p.wl : -1; 
 template <bool WIN>
 __device__ __forceinline__ int win_r(const Params& p) { return WIN ? p.wr : 0; }
 
-template <bool CAUSAL, bool WIN>
+template <bool CAUSAL, bool WIN, bool PIECES>
 __device__ __forceinline__ Work decode(const Params& p, int unit) {
   Work w;
   int r;
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    w.it[k].h0 = 0;
+    w.it[k].nh = p.group;
+    w.it[k].tt = -1;
+  }
   if (CAUSAL && win_l<WIN>(p) < 0) {
     // key tiles j and n-1-j share a CTA: the pair always has n+1 query-tile
     // steps (for Nq = Nk), so all these CTAs carry the same work; heads in a
@@ -170,12 +186,19 @@ __device__ __forceinline__ Work decode(const Params& p, int unit) {
       w.it[1].j = p.n_ktiles - 1 - pr;
       w.n_items = 2;
     } else {
-      const int per_head = 2 * p.n_split + (p.n_ktiles & 1);
+      const int hs = PIECES ? p.group : 1;  // units per tail tile
+      const int per_head = p.n_tail * hs;
       const int s = unit - whole;
       r = s / per_head;
       const int t = s - r * per_head;
-      const int pr = kept + (t >> 1);
-      w.it[0].j = t < 2 * p.n_split ? ((t & 1) ? p.n_ktiles - 1 - pr : pr) : half;
+      const int tt = t / hs;  // the query heads of one tile are consecutive units
+      const int pr = kept + (tt >> 1);
+      w.it[0].j = tt < 2 * p.n_split ? ((tt & 1) ? p.n_ktiles - 1 - pr : pr) : half;
+      if (PIECES) {
+        w.it[0].h0 = t - tt * hs;
+        w.it[0].nh = 1;
+        w.it[0].tt = tt;
+      }
       w.it[1].j = 0;
       w.n_items = 1;
     }
@@ -205,7 +228,7 @@ __device__ __forceinline__ Work decode(const Params& p, int unit) {
     }
     w.it[k].i0 = i0;
     w.it[k].nq = nq;
-    w.it[k].steps = nq * p.group;
+    w.it[k].steps = nq * w.it[k].nh;
   }
   return w;
 }
@@ -216,11 +239,11 @@ __device__ __forceinline__ Item pick(const Work& w, int k) { return k == 0 ? w.i
 // The k-th item of this (persistent) CTA: item k & 1 of unit blockIdx.x +
 // (k >> 1) * gridDim.x. Returns 0 past the last unit, 1 when the unit has no
 // such item (a single), 2 with I, b, kvh set.
-template <bool CAUSAL, bool WIN>
+template <bool CAUSAL, bool WIN, bool PIECES>
 __device__ __forceinline__ int item_at(const Params& p, int k, Item& I, int& b, int& kvh) {
   const int u = int(blockIdx.x) + (k >> 1) * int(gridDim.x);
   if (u >= p.n_units) return 0;
-  const Work w = decode<CAUSAL, WIN>(p, u);
+  const Work w = decode<CAUSAL, WIN, PIECES>(p, u);
   if ((k & 1) >= w.n_items) return 1;
   I = pick(w, k & 1);
   b = w.b;
@@ -250,7 +273,9 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
                : "memory");
 }
 
-template <int D, bool CAUSAL, bool WIN>
+// PIECES: the tail singles are split per query head (d = 128, GQA, paired
+// causal); without it no item is a piece and that code is compiled out.
+template <int D, bool CAUSAL, bool WIN, bool PIECES>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -335,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // warps have no registers to spare for it
         Item t;
         int tb, tk;
-        const int have = item_at<CAUSAL, WIN>(p, k, t, tb, tk);
+        const int have = item_at<CAUSAL, WIN, PIECES>(p, k, t, tb, tk);
         if (have == 0) break;
         if (have == 1) continue;
         __syncwarp();
@@ -466,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // warps have no registers to spare for it
         Item t;
         int tb, tk;
-        const int have = item_at<CAUSAL, WIN>(p, k, t, tb, tk);
+        const int have = item_at<CAUSAL, WIN, PIECES>(p, k, t, tb, tk);
         if (have == 0) break;
         if (have == 1) continue;
         __syncwarp();
@@ -478,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int& ikvh = ctl.cur[warp].kvh;
       for (int st = 0; st < I.steps && ok; ++st, ++g) {
         const int it = I.i0 + st % I.nq;
-        const int h = ikvh * p.group + st / I.nq;
+        const int h = ikvh * p.group + (PIECES ? I.h0 : 0) + st / I.nq;
         if (!mbar_wait_bounded(&ctl.dq_full, ph_dq, abort_flag, LIM)) { ok = false; break; }
         ph_dq ^= 1;
         if (threadIdx.x == 256) trace_stamp(p.trace, g, 10);
@@ -543,6 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       // epilogue of this item: dV, dK rows of its key tile (lane = key row)
       if (I.steps == 0) {
+        if (PIECES && I.tt >= 0) continue;  // a tail piece: the last pass writes the tile's zeros
         const int key = I.j * 128 + lr;
         __nv_bfloat16* dv = p.dv + ((size_t(ib) * p.Nk + key) * p.Hkv + ikvh) * D;
         __nv_bfloat16* dk = p.dk + ((size_t(ib) * p.Nk + key) * p.Hkv + ikvh) * D;
@@ -557,7 +583,52 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait_bounded(&ctl.acc_full, nacc & 1, abort_flag, LIM)) { ok = false; break; }
       ++nacc;
       tc_fence_after();
-      if (D == 128) {
+      if (D == 128 && PIECES && I.tt >= 0) {
+        // A tail piece (one query head of the group): its dV, then dK, are
+        // partial sums, stored in fp32 into the piece's own slot of the tail
+        // buffer with TMA stores, staged like dQ as [32 rows][32 d] boxes,
+        // two per half of d; a last pass sums the slots of each tile.
+        uint8_t* stg = smem + C::kOffStg + wq * 8192;
+        const int slot = ((ib * p.Hkv + ikvh) * p.n_tail + I.tt) * p.group + I.h0;
+#pragma unroll 1
+        for (int t = 0; t < 2; ++t) {
+          const uint32_t col = t == 0 ? C::kColDV : C::kColDK;
+          const float mul = t == 0 ? 1.0f : p.scale;
+#pragma unroll 1
+          for (int half = 0; half < 2; ++half) {
+            uint32_t v[64];
+            tmem_ld32(t_lane + col + half * 64, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+            tmem_ld32(t_lane + col + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+            tmem_wait_ld();
+            if (t == 1 && half == 1) {  // the next item's MMAs may overwrite the accumulators
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&ctl.acc_empty);
+            }
+            if (lane == 0) bulk_wait_read_all();  // earlier reductions and stores have read the quarter
+            __syncwarp();
+#pragma unroll
+            for (int b2 = 0; b2 < 2; ++b2) {
+              uint8_t* box = stg + b2 * 4096 + lane * 128;
+#pragma unroll
+              for (int u = 0; u < 8; ++u) {
+                const int c = b2 * 32 + 4 * u;
+                *reinterpret_cast<uint4*>(box + ((u ^ (lane & 7)) << 4)) =
+                    make_uint4(f2u(u2f(v[c]) * mul), f2u(u2f(v[c + 1]) * mul), f2u(u2f(v[c + 2]) * mul),
+                               f2u(u2f(v[c + 3]) * mul));
+              }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+#pragma unroll
+              for (int b2 = 0; b2 < 2; ++b2)
+                tma_store_4d(&out.dkv, stg + b2 * 4096, (half * 2 + b2) * 32, wq * 32, t, slot);
+              bulk_commit();
+            }
+          }
+        }
+      } else if (D == 128) {
         // Each warp stages its 32 key rows of dV, then of dK, as two
         // 128-byte-swizzled [32 rows][64 d] bf16 boxes in its quarter of the
         // dQ staging buffer and writes them with TMA stores (rows past Nk
@@ -646,7 +717,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         {
           Item t;
           int tb, tk;
-          const int have = item_at<CAUSAL, WIN>(p, k, t, tb, tk);
+          const int have = item_at<CAUSAL, WIN, PIECES>(p, k, t, tb, tk);
           if (have == 0) break;
           if (have == 1) continue;
           ctl.cur[warp] = Cur{t, tb, tk};  // one thread runs this role
@@ -665,15 +736,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int st = 0; st < I.steps && ok; ++st, ++g) {
           const int it = I.i0 + st % I.nq;
-          const int h = ikvh * p.group + st / I.nq;
+          const int h = ikvh * p.group + (PIECES ? I.h0 : 0) + st / I.nq;
           const int qs = g & 1;
           if (st == max(0, I.steps - kPrefetchSteps)) {
             // the next item's K and V into L2, so that its loads (issued
             // once this item's last GEMM has read K and V) hit L2
             Item N;
             int nb, nkvh;
-            int nh = item_at<CAUSAL, WIN>(p, k + 1, N, nb, nkvh);
-            if (nh == 1) nh = item_at<CAUSAL, WIN>(p, k + 2, N, nb, nkvh);
+            int nh = item_at<CAUSAL, WIN, PIECES>(p, k + 1, N, nb, nkvh);
+            if (nh == 1) nh = item_at<CAUSAL, WIN, PIECES>(p, k + 2, N, nb, nkvh);
             if (nh == 2 && N.steps > 0) {
 #pragma unroll
               for (int c = 0; c < D / 64; ++c) {
@@ -737,7 +808,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         {
           Item t;
           int tb, tk;
-          const int have = item_at<CAUSAL, WIN>(p, k, t, tb, tk);
+          const int have = item_at<CAUSAL, WIN, PIECES>(p, k, t, tb, tk);
           if (have == 0) break;
           if (have == 1) continue;
           ctl.cur[warp] = Cur{t, tb, tk};  // one thread runs this role
@@ -834,12 +905,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Work is split into groups of 16 consecutive query rows of one (batch,
 // head), one group per warp at a time: the warp loads the group's O and dO
 // rows (16 bytes per lane per row piece, all loads issued before any is
-// used), zeroes an equal share of the accumulator meanwhile, then writes the
-// group's 16 LSE/D values as one contiguous run.
+// used), zeroes an equal share of the dQ accumulator meanwhile, then
+// writes the group's 16 LSE/D values as one contiguous run.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* o, const __nv_bfloat16* dout,
                                                       const float* lse, float* lse2, float* delta, float* dq_acc,
-                                                      int B, int Hq, int Nq, int Nq_pad) {
+                                                      int B, int Hq, int Nq, int Nq_pad, long long zero4) {
   grid_dep_launch();  // the main kernel may start its set-up meanwhile
   constexpr int TPR = D / 8;          // lanes per row, 8 elements (16 bytes) each
   constexpr int RPP = 32 / TPR;       // rows per pass of the warp
@@ -851,7 +922,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* o, co
   const long long n_warps = (1LL * gridDim.x * blockDim.x) >> 5;
   const int gq = (Nq + kRows - 1) / kRows;  // groups per (batch, head)
   const long long n_groups = 1LL * B * Hq * gq;
-  const long long n4 = 1LL * B * Hq * D * Nq_pad / 4;  // accumulator, in float4
+  const long long n4 = zero4;  // the dQ accumulator, in float4
   const long long zc = (n4 + n_groups - 1) / n_groups;  // float4 zeroed per group
   float4* acc4 = reinterpret_cast<float4*>(dq_acc);
   for (long long grp = warp_id; grp < n_groups; grp += n_warps) {
@@ -953,6 +1024,52 @@ __global__ void __launch_bounds__(256) bwd_post_rows_kernel(const float* dq_acc,
   }
 }
 
+// d = 128 tail pieces: dV and dK rows of the tail tiles (their scale already
+// applied), the sum over the group's slots [B*Hkv][n_tail][group][2][128][D]
+// taken in slot order, to bf16 BSHD, 16 lanes per row; rows past Nk are
+// skipped, and a tile that no query row sees (its pieces stored nothing)
+// gets zeros. The tile of tail index tt is the one the main kernel's decode
+// gives it; wr is the kernel's right window bound (0 when causal).
+__global__ void __launch_bounds__(256) bwd_tail_kernel(const float* dkv, __nv_bfloat16* dk, __nv_bfloat16* dv, int B,
+                                                       int Hkv, int group, int Nq, int Nk, int wr, int n_ktiles,
+                                                       int n_split, int n_tail) {
+  grid_dep_wait();  // launched while the kernels before may still run
+  constexpr int D = 128, TPR = D / 8;
+  const long long n = 1LL * B * Hkv * n_tail * 2 * 128 * TPR;
+  const long long tid = 1LL * blockIdx.x * blockDim.x + threadIdx.x;
+  const long long nth = 1LL * gridDim.x * blockDim.x;
+  for (long long idx = tid; idx < n; idx += nth) {
+    const long long row = idx / TPR;  // ((r * n_tail + tt) * 2 + t) * 128 + rr
+    const int part = int(idx - row * TPR);
+    const int rr = int(row % 128);
+    long long x = row / 128;
+    const int t = int(x % 2);  // 0: dV, 1: dK
+    x /= 2;
+    const int tt = int(x % n_tail);
+    const long long r = x / n_tail;
+    const int b = int(r / Hkv), kvh = int(r - 1LL * b * Hkv);
+    const int half = n_ktiles / 2, kept = half - n_split, pr = kept + (tt >> 1);
+    const int j = tt < 2 * n_split ? ((tt & 1) ? n_ktiles - 1 - pr : pr) : half;
+    const int key = j * 128 + rr;
+    if (key >= Nk) continue;
+    // the first query row that sees key tile j is past the last one: no pieces ran
+    const bool empty = wr >= 0 && j * 128 - (Nk - Nq) - wr > Nq - 1;
+    float f[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    if (!empty) {
+      for (int g = 0; g < group; ++g) {
+        const float4* src =
+            reinterpret_cast<const float4*>(dkv + ((((r * n_tail + tt) * group + g) * 2 + t) * 128 + rr) * D + part * 8);
+        const float4 a = src[0], c = src[1];
+        f[0] += a.x; f[1] += a.y; f[2] += a.z; f[3] += a.w;
+        f[4] += c.x; f[5] += c.y; f[6] += c.z; f[7] += c.w;
+      }
+    }
+    __nv_bfloat16* dst = (t == 0 ? dv : dk) + ((size_t(b) * Nk + key) * Hkv + kvh) * D + part * 8;
+    *reinterpret_cast<uint4*>(dst) = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                                                pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+  }
+}
+
 // d = 64: dq[b, q, h, :] = bf16(scale * acc[b*Hq + h, :, q]), through a shared
 // tile: a block takes 64 queries of one (batch, head); each warp reads whole
 // 256-byte runs of accumulator rows (one d, 64 q), then every thread writes
@@ -991,26 +1108,28 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(const float* dq_acc, __nv
   }
 }
 
-// How many key-tile pairs per head (those nearest the middle) to run as two
+// How many key-tile pairs per kv head (those nearest the middle) to run as
 // single-tile units, for `heads` (batch, kv head) slices of n key tiles on G
-// persistent CTAs. Model, in units of half a pair's work: a whole pair takes
-// 2, a single 1. Units go to CTAs round robin in order (P pairs, then S
-// singles): with W = P / G and T = P mod G, CTA c runs W pairs (one more if
-// c < T) and then the singles u with (P + u) mod G = c. The finish time is
-// the largest CTA's total; the smallest split count reaching the least
-// finish time wins.
-int split_pairs(int heads, int n, int G) {
+// persistent CTAs, each single split further into `hs` units (one per query
+// head of the group, or hs = 1). Model, in units of one such piece (half a
+// pair's work for one head): a whole pair takes 2 * hs, a piece 1. Units go
+// to CTAs round robin in order (P pairs, then S pieces): with W = P / G and
+// T = P mod G, CTA c runs W pairs (one more if c < T) and then the pieces u
+// with (P + u) mod G = c. The finish time is the largest CTA's total; the
+// smallest split count reaching the least finish time wins.
+int split_pairs(int heads, int n, int G, int hs) {
   const int half = n / 2;
+  const long long cp = 2LL * hs;
   int best_m = 0;
   long long best_t = -1;
   for (int m = 0; m <= half; ++m) {
-    const long long P = 1LL * heads * (half - m), S = 1LL * heads * (2 * m + (n & 1));
+    const long long P = 1LL * heads * (half - m), S = 1LL * heads * (2 * m + (n & 1)) * hs;
     const long long W = P / G, T = P % G;
-    // CTAs c >= T take singles at positions c - T, those below T at
+    // CTAs c >= T take pieces at positions c - T, those below T at
     // c - T + G; each takes S / G, plus one at positions below S mod G
     const long long q = S / G, r = S % G;
-    long long t = 2 * W + q + (r > 0 ? 1 : 0);
-    if (T > 0) t = std::max(t, 2 * (W + 1) + q + (r > G - T ? 1 : 0));
+    long long t = cp * W + q + (r > 0 ? 1 : 0);
+    if (T > 0) t = std::max(t, cp * (W + 1) + q + (r > G - T ? 1 : 0));
     if (best_t < 0 || t < best_t) {
       best_t = t;
       best_m = m;
@@ -1019,13 +1138,41 @@ int split_pairs(int heads, int n, int G) {
   return best_m;
 }
 
+// The causal backward's work split: pairs of key tiles, n_split of them per
+// kv head run as single tiles, which for d = 128 with GQA are split once more
+// per query head (their dK/dV summed in the fp32 tail accumulator).
+struct TailPlan {
+  bool paired;
+  int n_split, head_split, n_tail;
+  size_t dkv_floats;  // size of the tail accumulator
+};
+TailPlan tail_plan(const Problem& pb) {
+  TailPlan t{};
+  const int n_ktiles = (pb.Nk + 127) / 128;
+  const int wl = normalize_window(pb.window_left, pb.Nq, pb.Nk);
+  t.paired = pb.masked() && wl < 0;  // pairs of key tiles only without a left bound
+  if (!t.paired) return t;
+  const int group = pb.Hq / pb.Hkv;
+  t.head_split = (pb.d == 128 && group > 1) ? 1 : 0;
+  const int forced = debug_cfg().bwd_split;
+  t.n_split = forced >= 0 ? std::min(forced, n_ktiles / 2)
+                          : split_pairs(pb.B * pb.Hkv, n_ktiles, num_sms(), t.head_split ? group : 1);
+  t.n_tail = 2 * t.n_split + (n_ktiles & 1);
+  if (t.head_split && t.n_tail > 0)
+    t.dkv_floats = size_t(pb.B) * pb.Hkv * t.n_tail * size_t(group) * 2 * 128 * size_t(pb.d);
+  if (t.dkv_floats == 0) t.head_split = 0;
+  return t;
+}
+
 template <int D, bool CAUSAL, bool WIN>
 cudaError_t launch_t(const Problem& pb, const void* o, const float* lse, const void* dout, void* dq, void* dk, void* dv,
                      float* ws, cudaStream_t stream) {
   const int Nq_pad = (pb.Nq + 127) / 128 * 128;
   const size_t acc_elems = size_t(pb.B) * pb.Hq * D * Nq_pad;
+  const TailPlan tp = tail_plan(pb);
   float* dq_acc = ws;
-  float* lse2 = ws + acc_elems;
+  float* dkv_acc = ws + acc_elems;  // tail pieces' partial dK/dV (d = 128, GQA), may be empty; not zeroed
+  float* lse2 = dkv_acc + tp.dkv_floats;
   float* delta = lse2 + size_t(pb.B) * pb.Hq * Nq_pad;
   {
     // 8 warps a block, one group of 16 query rows per warp at a time; at
@@ -1036,7 +1183,8 @@ cudaError_t launch_t(const Problem& pb, const void* o, const float* lse, const v
     if (blocks > maxb) blocks = maxb;
     bwd_pre_kernel<D><<<unsigned(blocks), 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(o),
                                                              static_cast<const __nv_bfloat16*>(dout), lse, lse2, delta,
-                                                             dq_acc, pb.B, pb.Hq, pb.Nq, Nq_pad);
+                                                             dq_acc, pb.B, pb.Hq, pb.Nq, Nq_pad,
+                                                             (long long)(acc_elems / 4));
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -1047,6 +1195,19 @@ cudaError_t launch_t(const Problem& pb, const void* o, const float* lse, const v
       !make_bshd_map(&mdo, dout, pb.B, pb.Nq, pb.Hq, D, 128) || !make_bshd_map(&out.dk, dk, pb.B, pb.Nk, pb.Hkv, D, 32) ||
       !make_bshd_map(&out.dv, dv, pb.B, pb.Nk, pb.Hkv, D, 32))
     return cudaErrorInvalidValue;
+  {
+    // out.dkv: the tail slots [B*Hkv*n_tail*group][2][128][D] fp32, boxes of
+    // 32 rows x 32 d (unused without tail pieces: then a map over the first
+    // rows of the dQ accumulator)
+    const uint64_t n2 = tp.dkv_floats ? 2 : 1;
+    const uint64_t nr = tp.dkv_floats ? uint64_t(pb.B) * pb.Hkv * tp.n_tail * (pb.Hq / pb.Hkv) : 1;
+    const uint64_t dims[4] = {uint64_t(D), 128, n2, nr};
+    const uint64_t strides[3] = {uint64_t(D) * 4, uint64_t(D) * 128 * 4, uint64_t(D) * 128 * 4 * n2};
+    const uint32_t box[4] = {32, 32, 1, 1};
+    if (!encode_tiled(&out.dkv, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, tp.dkv_floats ? dkv_acc : dq_acc, dims, strides,
+                      box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
   // out.acc (d = 128): the fp32 accumulator [B, Hq, Nq_pad, D], boxes of 32 q x 32 d
   {
     const uint64_t dims[4] = {uint64_t(D), uint64_t(Nq_pad), uint64_t(pb.Hq), uint64_t(pb.B)};
@@ -1082,13 +1243,19 @@ cudaError_t launch_t(const Problem& pb, const void* o, const float* lse, const v
   if (!p.status) return cudaErrorMemoryAllocation;
   using C = Cfg<D>;
   constexpr int smem = C::kOffCtl + int(sizeof(Ctl));
-  auto kern = bwd_main_kernel<D, CAUSAL, WIN>;
+  auto kern = bwd_main_kernel<D, CAUSAL, WIN, false>;
+  if constexpr (D == 128 && CAUSAL) {
+    if (tp.head_split) kern = bwd_main_kernel<D, CAUSAL, WIN, true>;
+  }
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const bool paired = CAUSAL && (WIN ? p.wl : -1) < 0;  // decode: pairs of key tiles only without a left bound
-  p.n_split = paired ? split_pairs(pb.B * pb.Hkv, p.n_ktiles, num_sms()) : 0;
-  const long long units = paired ? 1LL * pb.B * pb.Hkv * (p.n_ktiles / 2 + p.n_split + (p.n_ktiles & 1))
-                                 : 1LL * pb.B * pb.Hkv * p.n_ktiles;
+  const bool paired = tp.paired;  // decode: pairs of key tiles only without a left bound
+  p.n_split = tp.n_split;
+  p.head_split = tp.head_split;
+  p.n_tail = tp.n_tail;
+  const long long units =
+      paired ? 1LL * pb.B * pb.Hkv * (p.n_ktiles / 2 - p.n_split + 1LL * p.n_tail * (p.head_split ? p.group : 1))
+             : 1LL * pb.B * pb.Hkv * p.n_ktiles;
   if (units > (1LL << 31) - 1) return cudaErrorInvalidValue;
   p.n_units = int(units);
   const unsigned grid = unsigned(std::min<long long>(units, num_sms()));  // persistent CTAs, one per SM
@@ -1129,6 +1296,18 @@ cudaError_t launch_t(const Problem& pb, const void* o, const float* lse, const v
                            pb.Nq, Nq_pad, pb.scale);
     if (e != cudaSuccess) return e;
   }
+  if (D == 128 && tp.dkv_floats > 0) {  // dK/dV of the tail tiles, from their pieces' sums
+    const long long pieces = 1LL * pb.B * pb.Hkv * tp.n_tail * 2 * 128 * (D / 8);
+    long long blocks = (pieces + 255) / 256;
+    if (blocks > 8LL * num_sms()) blocks = 8LL * num_sms();
+    lc.gridDim = dim3(unsigned(blocks));
+    lc.blockDim = dim3(256);
+    lc.dynamicSmemBytes = 0;
+    e = cudaLaunchKernelEx(&lc, bwd_tail_kernel, static_cast<const float*>(dkv_acc), static_cast<__nv_bfloat16*>(dk),
+                           static_cast<__nv_bfloat16*>(dv), pb.B, pb.Hkv, p.group, pb.Nq, pb.Nk, p.wr, p.n_ktiles,
+                           p.n_split, p.n_tail);
+    if (e != cudaSuccess) return e;
+  }
   return cudaGetLastError();
 }
 
@@ -1136,7 +1315,8 @@ cudaError_t launch_t(const Problem& pb, const void* o, const float* lse, const v
 
 size_t bwd_workspace_bytes(const Problem& p) {
   const size_t Nq_pad = size_t(p.Nq + 127) / 128 * 128;
-  return sizeof(float) * size_t(p.B) * p.Hq * Nq_pad * size_t(p.d + 2);
+  // dQ accumulator and LSE/D rows, plus the tail pieces' partial dK/dV
+  return sizeof(float) * (size_t(p.B) * p.Hq * Nq_pad * size_t(p.d + 2) + bwd::tail_plan(p).dkv_floats);
 }
 
 cudaError_t launch_bwd(const Problem& p, const void* o, const float* lse, const void* dout, void* dq, void* dk,

@@ -32,6 +32,7 @@ struct DebugCfg {
   unsigned long long* trace;  // optional device trace buffer
   int poly_every;             // forward exp2 split (fa_tune FA_TUNE_EXP2_SPLIT)
   int cta_pairs;              // forward on CTA pairs (fa_tune FA_TUNE_CTA_PAIRS)
+  int bwd_split;              // causal backward split count, -1 = model (fa_tune FA_TUNE_BWD_SPLIT)
 };
 DebugCfg debug_cfg();
 

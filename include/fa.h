@@ -253,6 +253,20 @@ int fa_debug_exp2(const float* x, float* y, int n, int mode, void* stream);
  *     the order of floating-point additions.
  */
 #define FA_TUNE_CTA_PAIRS 2
+/*
+ *   FA_TUNE_BWD_SPLIT: the causal backward (no left window bound) runs key
+ *     tiles in pairs (j, n-1-j) of equal work; of each kv head's pairs, the
+ *     m nearest the middle run as single tiles to fill the last round of
+ *     the persistent CTAs, and with grouped-query heads at d = 128 each such
+ *     single is split further into one unit per query head, whose dK/dV are
+ *     partial sums kept in fp32 and summed in a fixed order by a last pass
+ *     (dK, dV stay deterministic). value -1
+ *     (the default): m from a model of the round-robin schedule on this
+ *     GPU's SM count; value m >= 0: that m (at most n/2). For tests of the
+ *     split paths on small shapes; results differ only in the order of
+ *     floating-point additions.
+ */
+#define FA_TUNE_BWD_SPLIT 3
 int fa_tune(int knob, int value);
 
 /*

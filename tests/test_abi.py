@@ -156,3 +156,6 @@ def test_tune_validates(fa):
         assert fa.fa_tune(fa.TUNE_CTA_PAIRS, v) == 1
     assert fa.fa_tune(fa.TUNE_CTA_PAIRS, 1) == 0
     assert fa.fa_tune(fa.TUNE_CTA_PAIRS, 0) == 0
+    assert fa.fa_tune(fa.TUNE_BWD_SPLIT, -2) == 1
+    for v in (5, 0, -1):
+        assert fa.fa_tune(fa.TUNE_BWD_SPLIT, v) == 0

@@ -274,3 +274,62 @@ def test_window_full_size_sampled_heads(fa):
         assert_close(f"dq[h{h}]", to64(dq[:, :, h:h + 1]), rdq)
         assert_close(f"dk[h{h}]", to64(dk[:, :, h:h + 1]), rdk)
         assert_close(f"dv[h{h}]", to64(dv[:, :, h:h + 1]), rdv)
+
+
+# The causal backward's split of its last round (fa_tune FA_TUNE_BWD_SPLIT
+# forces the count m of pairs per kv head that run as single tiles): with
+# GQA at d = 128 each single is split once more per query head, whose dK/dV
+# are partial sums kept in fp32 and summed by a last pass; otherwise
+# the singles take the whole group. Small shapes, forced m, against the
+# oracle element by element.
+SPLITS = [
+    # B, Hq, Hkv, Nq, Nk, d, m
+    (2, 8, 2, 1000, 1000, 128, 1),   # 8 key tiles, group 4: pieces per query head
+    (2, 8, 2, 1000, 1000, 128, 4),   # every pair split
+    (1, 4, 2, 1100, 1100, 128, 2),   # 9 key tiles: the middle tile is a tail tile too
+    (1, 4, 2, 1100, 1100, 128, 0),   # only the middle tile
+    (1, 6, 3, 600, 1000, 128, 2),    # Nq < Nk
+    (1, 4, 4, 900, 900, 128, 3),     # MHA: singles take the whole (one-head) group
+    (1, 4, 2, 700, 700, 64, 2),      # d = 64: singles take the whole group
+]
+
+
+@pytest.mark.parametrize("shape", SPLITS, ids=lambda s: "x".join(map(str, s)))
+def test_forced_split_matches_oracle(fa, shape):
+    B, Hq, Hkv, Nq, Nk, d, m = shape
+    x = workloads.make_inputs(B, Hq, Hkv, Nq, Nk, d, seed=sum(shape) + 7, with_dout=True)
+    scale = 1.0 / math.sqrt(d)
+    assert fa.fa_tune(fa.TUNE_BWD_SPLIT, m) == 0
+    try:
+        dq, dk, dv = gpu_grads(fa, x, True, scale)
+    finally:
+        fa.fa_tune(fa.TUNE_BWD_SPLIT, -1)
+    rdq, rdk, rdv = attn_ref.backward(*(x[n].double().numpy() for n in ("q", "k", "v", "do")), scale, True)
+    assert_close("dq", to64(dq), rdq)
+    # GQA dK/dV sum over the group's queries and pass |x| = 4, where output
+    # rounding alone can exceed 2e-2: the bound grows with the value
+    assert_close_scaled("dk", to64(dk), rdk)
+    assert_close_scaled("dv", to64(dv), rdv)
+
+
+def test_forced_split_agrees_with_model_split(fa):
+    """The same inputs with the split count from the model and with every
+    pair split into pieces: the gradients agree within the fp32 summation
+    order (dK/dV of a tile summed in TMEM over its heads, or in fp32 over
+    its pieces) and one bf16 rounding; and a second run with pieces gives
+    the same dK, dV bit for bit (the pieces are summed in a fixed order)."""
+    B, Hq, Hkv, N, d = 1, 8, 2, 1536, 128
+    x = workloads.make_inputs(B, Hq, Hkv, N, N, d, seed=91, with_dout=True)
+    scale = 1.0 / math.sqrt(d)
+    ref = gpu_grads(fa, x, True, scale)
+    assert fa.fa_tune(fa.TUNE_BWD_SPLIT, 6) == 0
+    try:
+        got = gpu_grads(fa, x, True, scale)
+        again = gpu_grads(fa, x, True, scale)
+    finally:
+        fa.fa_tune(fa.TUNE_BWD_SPLIT, -1)
+    assert torch.equal(got[1], again[1]) and torch.equal(got[2], again[2])
+    for name, a, b in zip(("dq", "dk", "dv"), got, ref):
+        a64, b64 = a.double(), b.double()
+        ulp = torch.maximum(a64.abs(), b64.abs()) * 2.0 ** -7 + 1e-6
+        assert ((a64 - b64).abs() <= ulp).all(), (name, (a64 - b64).abs().max().item())

@@ -76,8 +76,9 @@ def test_noalloc_rejects_workspace_beyond_the_array(fa):
 # Run in a fresh interpreter: the library's memory pool is still empty there,
 # so any allocation the call made (from the pool or elsewhere) would take new
 # device memory. A first call on a small problem loads the kernels and looks
-# up the array's address; the measured call uses the same kernels on a
-# problem whose workspace (about 40 MiB) is larger than the first one's.
+# up the array's address (a second, with the causal GQA split forced, loads
+# the kernels of that path); the measured call uses kernels already loaded
+# on a problem whose workspace (about 40 MiB) is larger than the first ones'.
 _CHILD = r"""
 import math, sys, torch
 sys.path.insert(0, ROOT)
@@ -100,6 +101,11 @@ def run(B, Hq, Hkv, N, d, seed):
     assert torch.isfinite(dq.float()).all()
     return free0 - free1
 run(1, 2, 2, 256, 128, 1)
+# the kernels of the causal GQA split (tail pieces and their last pass) load
+# on first use too: use them once before the measured call
+assert fa.fa_tune(fa.TUNE_BWD_SPLIT, 1) == 0
+run(1, 4, 2, 512, 128, 3)
+assert fa.fa_tune(fa.TUNE_BWD_SPLIT, -1) == 0
 taken = run(1, 8, 4, 9000, 128, 2)
 print("TAKEN", taken)
 """
