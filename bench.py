@@ -714,7 +714,9 @@ def run_ours(args):
                 "link_gbps": link["duplex_gbps"], "copy_ms_at_link": round(copy_ms, 4),
                 "bound_ms": round(bound_ms, 4), "frac_of_bound": round(bound_ms / e2e_ms, 4),
                 "copy_fraction_of_link": round((h2d + d2h) / (e2e_ms * 1e-3) / 1e9 / link["duplex_gbps"], 4)},
-        "gpu_launches": 4 * K,
+        # the forward and the backward's kernels (pre-pass, main, dQ
+        # conversion, and the pass over the GQA tail pieces when there are any)
+        "gpu_launches": (1 + fa.fa_bwd_launches(w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.d, int(w.causal))) * K,
         "configs": per_workload,
     }
     if world == 1:

@@ -17,7 +17,7 @@ import ctypes
 import math
 import os
 
-__all__ = ["FAError", "lib", "fa_fwd", "fa_bwd", "fa_bwd_noalloc", "fa_get_status", "fa_status_string", "fa_debug_set",
+__all__ = ["FAError", "lib", "fa_fwd", "fa_bwd", "fa_bwd_noalloc", "fa_bwd_launches", "fa_get_status", "fa_status_string", "fa_debug_set",
            "fa_debug_exp2", "fa_tune", "TUNE_EXP2_SPLIT", "TUNE_CTA_PAIRS", "TUNE_BWD_SPLIT", "fa_profile_events", "fa_trace", "forward", "backward", "STATUS"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -65,6 +65,8 @@ def lib() -> ctypes.CDLL:
         L.fa_bwd_window.restype = i
         L.fa_bwd_noalloc.argtypes = [vp] * 9 + [i, i, i, i, i, i, f, i, vp]
         L.fa_bwd_noalloc.restype = i
+        L.fa_bwd_launches.argtypes = [i] * 7
+        L.fa_bwd_launches.restype = i
         L.fa_get_status.argtypes = [vp]
         L.fa_get_status.restype = i
         L.fa_status_string.argtypes = [i]
@@ -156,6 +158,11 @@ def fa_bwd_window(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Nq, Nk, d, scal
     return lib().fa_bwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
                                _ptr(dv), B, Hq, Hkv, Nq, Nk, d, float(scale), int(window_left), int(window_right),
                                _stream(stream))
+
+
+def fa_bwd_launches(B, Hq, Hkv, Nq, Nk, d, causal) -> int:
+    """Kernels fa_bwd launches for this problem (see fa.h), or minus a status."""
+    return lib().fa_bwd_launches(int(B), int(Hq), int(Hkv), int(Nq), int(Nk), int(d), int(causal))
 
 
 def fa_bwd_noalloc(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Nq, Nk, d, scale, causal, stream=None) -> int:

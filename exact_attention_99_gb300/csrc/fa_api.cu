@@ -367,6 +367,13 @@ extern "C" int fa_debug_set(unsigned long long wait_limit_ns, int inject) {
   return FA_OK;
 }
 
+extern "C" int fa_bwd_launches(int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal) {
+  const int st = check_sizes(B, Hq, Hkv, Nq, Nk, d, 1.0f, causal);
+  if (st != FA_OK) return -st;
+  const Problem p{nullptr, nullptr, nullptr, B, Hq, Hkv, Nq, Nk, d, 1.0f, causal};
+  return bwd_launch_count(p);
+}
+
 extern "C" int fa_tune(int knob, int value) {
   if (knob == FA_TUNE_EXP2_SPLIT) {
     if (value != 0 && value != 1 && value != 2 && value != 4 && value != 8) return FA_ERR_INVALID_ARG;

@@ -1313,6 +1313,11 @@ cudaError_t launch_t(const Problem& pb, const void* o, const float* lse, const v
 
 }  // namespace bwd
 
+int bwd_launch_count(const Problem& p) {
+  // pre-pass, main kernel, dQ conversion, and the tail pieces' last pass
+  return 3 + (p.d == 128 && bwd::tail_plan(p).dkv_floats > 0 ? 1 : 0);
+}
+
 size_t bwd_workspace_bytes(const Problem& p) {
   const size_t Nq_pad = size_t(p.Nq + 127) / 128 * 128;
   // dQ accumulator and LSE/D rows, plus the tail pieces' partial dK/dV
@@ -1382,7 +1387,8 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
   float* ws = fa::noalloc_scratch();
   if (ws == nullptr) return FA_ERR_LAUNCH;
   // The preprocess kernel zeroes the dQ accumulator and rewrites every LSE/D
-  // row it reads, so nothing left in the array by an earlier call is used.
+  // row it reads, and every tail slot that the last pass reads is stored by
+  // this call, so nothing left in the array by an earlier call is used.
   return fa::launch_bwd(p, o, lse, dout, dq, dk, dv, ws, static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? FA_OK
              : FA_ERR_LAUNCH;

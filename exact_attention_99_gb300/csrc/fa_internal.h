@@ -79,6 +79,8 @@ int check_bwd_args(const void* q, const void* k, const void* v, const void* o, c
 
 // Backward workspace (fp32 dQ accumulator, padded LSE*log2e and D rows).
 size_t bwd_workspace_bytes(const Problem& p);
+// kernels fa_bwd launches for p
+int bwd_launch_count(const Problem& p);
 cudaError_t launch_bwd(const Problem& p, const void* o, const float* lse, const void* dout, void* dq, void* dk,
                        void* dv, float* ws, cudaStream_t stream);
 cudaError_t launch_debug_exp2(const float* x, float* y, int n, int mode, cudaStream_t stream);

@@ -181,7 +181,9 @@ int fa_step_host(const void* q, const void* k, const void* v, const void* dout, 
  *   Workspace: a file-scope device array of FA_BWD_NOALLOC_SCRATCH_BYTES
  *     (64 MiB) inside the library. Every device that loads the library holds
  *     it until the process exits. The call needs
- *       4 * B*Hq*ceil(Nq/128)*128 * (d + 2) bytes of it and returns
+ *       4 * B*Hq*ceil(Nq/128)*128 * (d + 2) bytes of it (plus, for the
+ *       causal GQA backward at d = 128 whose last round is split per query
+ *       head, 4 * 2 * 128 * d bytes per tail piece) and returns
  *     FA_ERR_UNSUPPORTED, without enqueuing anything, when that exceeds the
  *     array.
  *   No cudaMalloc, cudaFree or other allocating routine is called.
@@ -194,6 +196,16 @@ int fa_step_host(const void* q, const void* k, const void* v, const void* dout, 
  *     them) race on the array and give wrong results; order them.
  */
 #define FA_BWD_NOALLOC_SCRATCH_BYTES (64ull << 20)
+/*
+ * fa_bwd_launches — how many kernels fa_bwd (or fa_bwd_noalloc) launches
+ *   for this problem: the pre-pass, the main kernel and the dQ conversion,
+ *   plus, for the causal GQA backward at d = 128 whose last round is split
+ *   per query head, the pass that sums the pieces' dK/dV. With the split
+ *   count of the current fa_tune setting and this GPU's SM count. For
+ *   profiling and accounting; returns the count, or minus an fa_status for
+ *   sizes fa_bwd would reject.
+ */
+int fa_bwd_launches(int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal);
 int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
                    void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Nq, int Nk, int d, float scale,
                    int causal, void* stream);

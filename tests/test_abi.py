@@ -159,3 +159,19 @@ def test_tune_validates(fa):
     assert fa.fa_tune(fa.TUNE_BWD_SPLIT, -2) == 1
     for v in (5, 0, -1):
         assert fa.fa_tune(fa.TUNE_BWD_SPLIT, v) == 0
+
+
+def test_bwd_launches_counts(fa):
+    # pre-pass, main kernel, dQ conversion; the GQA tail's last pass only when
+    # the causal GQA split at d = 128 makes pieces (forced here: one pair per kv head)
+    assert fa.fa_bwd_launches(1, 4, 4, 1000, 1000, 128, 1) == 3  # MHA
+    assert fa.fa_bwd_launches(2, 8, 2, 1000, 1000, 128, 0) == 3
+    assert fa.fa_bwd_launches(2, 8, 2, 1000, 1000, 64, 1) == 3
+    assert fa.fa_tune(fa.TUNE_BWD_SPLIT, 1) == 0
+    try:
+        assert fa.fa_bwd_launches(2, 8, 2, 1000, 1000, 128, 1) == 4
+        assert fa.fa_bwd_launches(2, 8, 8, 1000, 1000, 128, 1) == 3  # MHA: no pieces
+    finally:
+        fa.fa_tune(fa.TUNE_BWD_SPLIT, -1)
+    assert fa.fa_bwd_launches(1, 3, 2, 64, 64, 128, 1) == -1  # Hq not a multiple of Hkv
+    assert fa.fa_bwd_launches(1, 2, 2, 64, 64, 96, 1) < 0     # unsupported head dim
