@@ -1161,6 +1161,15 @@ TailPlan tail_plan(const Problem& pb) {
   if (t.head_split && t.n_tail > 0)
     t.dkv_floats = size_t(pb.B) * pb.Hkv * t.n_tail * size_t(group) * 2 * 128 * size_t(pb.d);
   if (t.dkv_floats == 0) t.head_split = 0;
+  const size_t base = sizeof(float) * size_t(pb.B) * pb.Hq * ((size_t(pb.Nq) + 127) / 128 * 128) * size_t(pb.d + 2);
+  if (t.head_split && pb.ws_cap > 0 && base + sizeof(float) * t.dkv_floats > pb.ws_cap) {
+    // the slots do not fit the caller's workspace: whole single tiles, as
+    // many as the model wants for them
+    if (forced < 0) t.n_split = split_pairs(pb.B * pb.Hkv, n_ktiles, num_sms(), 1);
+    t.n_tail = 2 * t.n_split + (n_ktiles & 1);
+    t.head_split = 0;
+    t.dkv_floats = 0;
+  }
   return t;
 }
 
@@ -1387,7 +1396,8 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
                               int d, float scale, int causal, void* stream) {
   const int st = fa::check_bwd_args(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Nq, Nk, d, scale, causal);
   if (st != FA_OK) return st;
-  const fa::Problem p{q, k, v, B, Hq, Hkv, Nq, Nk, d, scale, causal};
+  fa::Problem p{q, k, v, B, Hq, Hkv, Nq, Nk, d, scale, causal};
+  p.ws_cap = FA_BWD_NOALLOC_SCRATCH_BYTES;  // tail pieces only where their slots fit too
   if (fa::bwd_workspace_bytes(p) > FA_BWD_NOALLOC_SCRATCH_BYTES) return FA_ERR_UNSUPPORTED;
   float* ws = fa::noalloc_scratch();
   if (ws == nullptr) return FA_ERR_LAUNCH;

@@ -19,6 +19,9 @@ struct Problem {
   // sliding window: key j visible to query i iff i + off - window_left <= j
   // <= i + off + window_right (off = Nk - Nq); -1 = no limit on that side
   int window_left = -1, window_right = -1;
+  // backward: largest workspace the call may use (0: any); the tail pieces
+  // fall back to whole single tiles when their slots would not fit
+  size_t ws_cap = 0;
   bool masked() const { return causal || window_left >= 0 || window_right >= 0; }
   // the causal mask and nothing else (window bounds already normalised)
   bool plain_causal() const { return window_left < 0 && (causal || window_right == 0); }

@@ -181,11 +181,12 @@ int fa_step_host(const void* q, const void* k, const void* v, const void* dout, 
  *   Workspace: a file-scope device array of FA_BWD_NOALLOC_SCRATCH_BYTES
  *     (64 MiB) inside the library. Every device that loads the library holds
  *     it until the process exits. The call needs
- *       4 * B*Hq*ceil(Nq/128)*128 * (d + 2) bytes of it (plus, for the
- *       causal GQA backward at d = 128 whose last round is split per query
- *       head, 4 * 2 * 128 * d bytes per tail piece) and returns
+ *       4 * B*Hq*ceil(Nq/128)*128 * (d + 2) bytes of it and returns
  *     FA_ERR_UNSUPPORTED, without enqueuing anything, when that exceeds the
- *     array.
+ *     array. The causal GQA backward at d = 128 splits its last round per
+ *     query head only where the pieces' fp32 slots (4 * 2 * 128 * d bytes
+ *     each) fit in the rest of the array; otherwise that round runs whole
+ *     single tiles (same results up to the order of fp32 additions).
  *   No cudaMalloc, cudaFree or other allocating routine is called.
  *   Set-up: the first call on each device looks up the array's device
  *     address on that device (cudaGetSymbolAddress); make that first call
@@ -197,8 +198,9 @@ int fa_step_host(const void* q, const void* k, const void* v, const void* dout, 
  */
 #define FA_BWD_NOALLOC_SCRATCH_BYTES (64ull << 20)
 /*
- * fa_bwd_launches — how many kernels fa_bwd (or fa_bwd_noalloc) launches
- *   for this problem: the pre-pass, the main kernel and the dQ conversion,
+ * fa_bwd_launches — how many kernels fa_bwd launches for this problem
+ *   (fa_bwd_noalloc: the same, or one fewer where the tail slots would not
+ *   fit its array): the pre-pass, the main kernel and the dQ conversion,
  *   plus, for the causal GQA backward at d = 128 whose last round is split
  *   per query head, the pass that sums the pieces' dK/dV. With the split
  *   count of the current fa_tune setting and this GPU's SM count. For

@@ -73,6 +73,38 @@ def test_noalloc_rejects_workspace_beyond_the_array(fa):
     assert fa.fa_get_status() == 0
 
 
+def test_noalloc_runs_whole_tiles_where_tail_slots_do_not_fit(fa):
+    # causal GQA at d = 128 with every pair split (16 tail tiles x 16 query
+    # heads of fp32 slots, 67 MB) next to a 34 MB dQ accumulator: more than
+    # the 64 MiB array, so the last round runs whole tiles instead of
+    # returning FA_ERR_UNSUPPORTED; fa_bwd (its own workspace) keeps the
+    # pieces. Same sums grouped differently: within two bf16 ulps of the
+    # element plus 2^-12 of the tensor's largest magnitude.
+    B, Hq, Hkv, N, d = 1, 32, 2, 2048, 128
+    x = workloads.make_inputs(B, Hq, Hkv, N, N, d, 41, with_dout=True)
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
+    scale = 1.0 / math.sqrt(d)
+    o, lse = fa.forward(q, k, v, causal=True, scale=scale)
+    args = (B, Hq, Hkv, N, N, d, scale, 1)
+    assert fa.fa_tune(fa.TUNE_BWD_SPLIT, 8) == 0
+    try:
+        assert fa.fa_bwd_launches(B, Hq, Hkv, N, N, d, 1) == 4  # fa_bwd: with the pieces' last pass
+        ref = [torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)]
+        assert fa.fa_bwd(q, k, v, o, lse, do, *ref, *args) == 0
+        got = [torch.full_like(q, float("nan")), torch.full_like(k, float("nan")), torch.full_like(v, float("nan"))]
+        assert fa.fa_bwd_noalloc(q, k, v, o, lse, do, *got, *args) == 0
+        torch.cuda.synchronize()
+    finally:
+        fa.fa_tune(fa.TUNE_BWD_SPLIT, -1)
+    assert fa.fa_get_status() == 0
+    for name, a, b in zip(("dq", "dk", "dv"), got, ref):
+        a64, b64 = a.double(), b.double()
+        assert torch.isfinite(a64).all(), name
+        top = torch.maximum(a64.abs().max(), b64.abs().max())
+        bound = torch.maximum(a64.abs(), b64.abs()) * 2.0 ** -6 + top * 2.0 ** -12
+        assert ((a64 - b64).abs() <= bound).all(), (name, (a64 - b64).abs().max().item())
+
+
 # Run in a fresh interpreter: the library's memory pool is still empty there,
 # so any allocation the call made (from the pool or elsewhere) would take new
 # device memory. A first call on a small problem loads the kernels and looks
@@ -113,7 +145,10 @@ print("TAKEN", taken)
 
 def test_noalloc_takes_no_device_memory():
     code = "ROOT = " + repr(ROOT) + "\n" + _CHILD
-    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True, timeout=600)
+    # eager module loading: every kernel is loaded when the library loads,
+    # so a kernel variant first used by the measured call takes no memory
+    env = dict(os.environ, CUDA_MODULE_LOADING="EAGER")
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True, timeout=600, env=env)
     assert r.returncode == 0, r.stderr[-2000:]
     taken = int(r.stdout.strip().splitlines()[-1].split()[1])
     assert taken == 0, f"the call took {taken} bytes of device memory"
