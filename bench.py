@@ -630,24 +630,27 @@ def run_ours(args):
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
     d2h = sum(t.numel() * t.element_size() for t in host_out.values())
     ke = min(K, 10)
-    ee0, ee1 = [ev() for _ in range(ke)], [ev() for _ in range(ke)]
+    ee0, ee1 = ev(), ev()
     torch.cuda.synchronize()
     host_args = [host_in[n] for n in ("q", "k", "v", "do")] + [host_out[n] for n in ("o", "lse", "dq", "dk", "dv")]
     if fa.fa_step_host(*host_args, *args_f):  # untimed: creates the copy streams, grows the pool
         raise RuntimeError("fa_step_host failed")
+    torch.cuda.synchronize()
+    # no L2 flush between calls: the calls overlap (below), and each one
+    # copies all its inputs in, more bytes than L2 holds
+    ee0.record()
     for i in range(ke):
-        flush.zero_()
-        ee0[i].record()
         # one call: inputs in, forward + backward, results out, pipelined over chunks of heads
         if fa.fa_step_host(*host_args, *args_f):
             raise RuntimeError("fa_step_host failed")
-        ee1[i].record()
+    ee1.record()
     torch.cuda.synchronize()
     if fa.fa_get_status() != 0:
         raise RuntimeError("device status not OK after fa_step_host")
     # consecutive calls overlap (a call's input copies run while the previous
-    # one computes), so the step time is the whole loop's device time per call
-    e2e_ms = ee0[0].elapsed_time(ee1[-1]) / ke
+    # one computes, and its kernels while the previous one's results go
+    # out), so the step time is the whole loop's device time per call
+    e2e_ms = ee0.elapsed_time(ee1) / ke
     e2e_value = world * step_flops(w) / (e2e_ms * 1e-3) / 1e12
     link = link_bandwidth()
     # the step cannot take less than its device time nor than its copies at
@@ -710,7 +713,8 @@ def run_ours(args):
         "rooflines": rooflines,
         "clocks": clocks,
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4), "link": link,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4), "calls": ke,
+                "l2": f"not flushed: each call copies {h2d / 1e6:.0f} MB of inputs in (L2: 129 MB)", "link": link,
                 "link_gbps": link["duplex_gbps"], "copy_ms_at_link": round(copy_ms, 4),
                 "bound_ms": round(bound_ms, 4), "frac_of_bound": round(bound_ms / e2e_ms, 4),
                 "copy_fraction_of_link": round((h2d + d2h) / (e2e_ms * 1e-3) / 1e9 / link["duplex_gbps"], 4)},

@@ -28,11 +28,12 @@ std::mutex g_mu;
 int g_sms[kMaxDevices];
 cudaMemPool_t g_pool[kMaxDevices];
 // fa_step_host: copy streams per device, kCopyLanes for each direction
-// (host to device: even indices, device to host: odd). One lane per
-// direction measured fastest: splitting each copy over two streams per
-// direction made the end-to-end step slower (1.44 instead of 1.19 ms).
+// (host to device: even indices, device to host: odd), then one compute
+// stream. One lane per direction measured fastest: splitting each copy over
+// two streams per direction made the end-to-end step slower (1.44 instead
+// of 1.19 ms).
 constexpr int kCopyLanes = 1;
-cudaStream_t g_copy[kMaxDevices][2 * kCopyLanes];
+cudaStream_t g_copy[kMaxDevices][2 * kCopyLanes + 1];
 // fa_step_host: two device buffers per device, used by alternate calls, so
 // that a call's input copies can run while the previous call computes. A
 // buffer is released (event on the caller's stream) once its call's last
@@ -59,11 +60,11 @@ int current_device() {
 bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // the copy streams of the current device, created on first use
-bool copy_streams(cudaStream_t (&out)[2 * kCopyLanes]) {
+bool copy_streams(cudaStream_t (&out)[2 * kCopyLanes + 1]) {
   const int dev = current_device();
   if (dev < 0) return false;
   std::lock_guard<std::mutex> lk(g_mu);
-  for (int i = 0; i < 2 * kCopyLanes; ++i) {
+  for (int i = 0; i < 2 * kCopyLanes + 1; ++i) {
     if (g_copy[dev][i] == nullptr && cudaStreamCreateWithFlags(&g_copy[dev][i], cudaStreamNonBlocking) != cudaSuccess) {
       g_copy[dev][i] = nullptr;
       return false;
@@ -431,19 +432,32 @@ extern "C" int fa_step_host(const void* q, const void* k, const void* v, const v
   st = check_device();
   if (st != FA_OK) return st;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaStream_t cs[2 * kCopyLanes];
+  cudaStream_t cs[2 * kCopyLanes + 1];
   if (!copy_streams(cs)) return FA_ERR_LAUNCH;
+  // the kernels run on the library's compute stream: they read and write
+  // only the library's buffers, so they wait for their input copies and not
+  // for `stream`, which the previous call left waiting for its last copies
+  // out; this call's compute then runs while those copies drain
+  const cudaStream_t sc = cs[2 * kCopyLanes];
   // Chunks: one batch element each; a batch of one element is cut into two
-  // halves of its kv heads (each with its query heads) when Hkv is even, so
-  // that copies and compute still overlap. A chunk is a problem of its own
-  // (B = 1, hq query heads, hk kv heads) in contiguous device buffers.
+  // halves of its kv heads (each with its query heads) when Hkv is even.
+  // On the device every tensor is stored chunk after chunk, [chunk][rows]
+  // [hq or hk heads][d] (LSE [chunk][hq][Nq]), i.e. as a batch of n_chunks
+  // elements with hq query and hk kv heads: the same attention problem,
+  // since (batch, head) pairs are independent. The forward runs in two
+  // launches over halves of the chunks, so that it starts once the first
+  // half's inputs are in and the first half's O goes out while the second
+  // computes; the backward runs as one launch over all chunks (per-chunk
+  // backward launches left the persistent kernel's last round half empty:
+  // 6.3 instead of 5.9 ms per call on the causal GQA N16384 step), and its
+  // results go out after it.
   const int C = (B == 1 && Hkv % 2 == 0) ? 2 : 1;  // kv-head slices per batch element
   const int hk = Hkv / C, hq = Hq / C;
   const size_t e2 = 2;  // bf16
   const size_t bq = size_t(Nq) * hq * d * e2, bk = size_t(Nk) * hk * d * e2, nl = size_t(hq) * Nq;
-  const size_t bl = (nl * 4 + 15) & ~size_t(15);
-  const size_t per = 4 * bq + 4 * bk + bl;
   const int n_chunks = B * C;
+  const int F = n_chunks >= 2 ? 2 : 1;  // forward launches
+  const size_t per = 4 * bq + 4 * bk + nl * 4;
   const int dev = current_device();
   if (dev < 0) return FA_ERR_LAUNCH;
   std::lock_guard<std::mutex> step_lock(g_step_mu);
@@ -471,12 +485,14 @@ extern "C" int fa_step_host(const void* q, const void* k, const void* v, const v
     slots.cap[slot] = need;
   }
   void* ws = slots.buf[slot];
-  // events: one set per chunk, reused for every chunk (each record is
-  // waited on before it is recorded again): per copy lane "q, k, v in" and
-  // "dout in", then "forward done" and "backward done"; then one "done" per
-  // copy stream
-  const size_t per_c = 2 * kCopyLanes + 2;
-  std::vector<cudaEvent_t> ev(per_c + 2 * kCopyLanes, nullptr);
+  // events, per copy lane: "q, k, v of forward group f in" (f < 2) and
+  // "dout in"; then "forward f done" (f < 2) and "backward done"; then one
+  // "done" per copy stream and one for the compute stream
+  const auto ev_qkv = [](int f, int l) { return size_t(f) * kCopyLanes + l; };
+  const auto ev_do = [](int l) { return size_t(2) * kCopyLanes + l; };
+  const auto ev_fwd = [](int f) { return size_t(3) * kCopyLanes + f; };
+  const size_t ev_bwd = 3 * kCopyLanes + 2, per_c = 3 * kCopyLanes + 3;
+  std::vector<cudaEvent_t> ev(per_c + 2 * kCopyLanes + 1, nullptr);
   bool ok = true;
   for (auto& e : ev) ok = ok && cudaEventCreateWithFlags(&e, cudaEventDisableTiming) == cudaSuccess;
   // the copies wait only for the previous user of this buffer (two calls
@@ -523,42 +539,57 @@ extern "C" int fa_step_host(const void* q, const void* k, const void* v, const v
   auto out = [&](uint8_t* host, uint8_t* dev, int rows, int H, int h0, int h) {
     return copy_heads(dev, host, rows, H, h0, h, d2h, 1);
   };
-  // chunk c: its inputs go in while chunk c-1 computes on the caller's
-  // stream and the results of chunk c-2 come back
-  for (int c = 0; c < n_chunks && ok; ++c) {
-    const int b = c / C, g = c - b * C;
-    const int q0 = g * hq, k0 = g * hk;  // first query / kv head of the chunk
-    uint8_t* w = static_cast<uint8_t*>(ws) + per * size_t(c);
-    uint8_t *wq = w, *wdo = w + bq, *wo = w + 2 * bq, *wdq = w + 3 * bq;
-    uint8_t *wk = w + 4 * bq, *wv = wk + bk, *wdk = wk + 2 * bk, *wdv = wk + 3 * bk;
-    float* wl = reinterpret_cast<float*>(wk + 4 * bk);
-    const size_t qoff = size_t(b) * Nq * Hq * d * e2, koff = size_t(b) * Nk * Hkv * d * e2;
-    cudaEvent_t* ec = ev.data();
-    // the forward needs q, k, v; dout follows while it runs
-    ok = in(wq, hq_ + qoff, Nq, Hq, q0, hq) && in(wk, hk_ + koff, Nk, Hkv, k0, hk) &&
-         in(wv, hv_ + koff, Nk, Hkv, k0, hk);
-    for (int l = 0; l < kCopyLanes && ok; ++l)
-      ok = cudaEventRecord(ec[l], cs[2 * l]) == cudaSuccess && cudaStreamWaitEvent(s, ec[l], 0) == cudaSuccess;
-    ok = ok && in(wdo, hdo + qoff, Nq, Hq, q0, hq);
-    for (int l = 0; l < kCopyLanes && ok; ++l) ok = cudaEventRecord(ec[kCopyLanes + l], cs[2 * l]) == cudaSuccess;
-    if (!ok) break;
-    const Problem p{wq, wk, wv, 1, hq, hk, Nq, Nk, d, scale, causal};
-    ok = launch_fwd(p, wo, wl, s) == cudaSuccess && cudaEventRecord(ec[2 * kCopyLanes], s) == cudaSuccess;
-    // o and lse go out while the backward runs
-    for (int l = 0; l < kCopyLanes && ok; ++l)
-      ok = cudaStreamWaitEvent(cs[2 * l + 1], ec[2 * kCopyLanes], 0) == cudaSuccess;
-    ok = ok && out(ho + qoff, wo, Nq, Hq, q0, hq) &&
-         cudaMemcpyAsync(hl + (size_t(b) * Hq + q0) * Nq * 4, wl, nl * 4, d2h, cs[1]) == cudaSuccess;
-    for (int l = 0; l < kCopyLanes && ok; ++l) ok = cudaStreamWaitEvent(s, ec[kCopyLanes + l], 0) == cudaSuccess;
-    ok = ok && bwd_pooled(p, wo, wl, wdo, wdq, wdk, wdv, stream) == FA_OK &&
-         cudaEventRecord(ec[2 * kCopyLanes + 1], s) == cudaSuccess;
-    for (int l = 0; l < kCopyLanes && ok; ++l)
-      ok = cudaStreamWaitEvent(cs[2 * l + 1], ec[2 * kCopyLanes + 1], 0) == cudaSuccess;
-    ok = ok && out(hdq + qoff, wdq, Nq, Hq, q0, hq) && out(hdk + koff, wdk, Nk, Hkv, k0, hk) &&
-         out(hdv + koff, wdv, Nk, Hkv, k0, hk);
+  uint8_t* const base = static_cast<uint8_t*>(ws);
+  uint8_t *const Rq = base, *const Rdo = Rq + n_chunks * bq, *const Ro = Rdo + n_chunks * bq;
+  uint8_t *const Rdq = Ro + n_chunks * bq, *const Rk = Rdq + n_chunks * bq, *const Rv = Rk + n_chunks * bk;
+  uint8_t *const Rdk = Rv + n_chunks * bk, *const Rdv = Rdk + n_chunks * bk;
+  float* const Rl = reinterpret_cast<float*>(Rdv + n_chunks * bk);
+  // chunk c = (batch element b, kv-head slice g): its host offsets
+  const auto qoff = [&](int c) { return size_t(c / C) * Nq * Hq * d * e2; };
+  const auto koff = [&](int c) { return size_t(c / C) * Nk * Hkv * d * e2; };
+  const auto first = [&](int f) { return n_chunks * f / F; };  // first chunk of forward group f
+  // inputs: q, k, v of the first forward group, then of the second, then
+  // dout (needed by the backward only)
+  for (int f = 0; f < F && ok; ++f) {
+    for (int c = first(f); c < first(f + 1) && ok; ++c) {
+      const int g = c % C;
+      ok = in(Rq + c * bq, hq_ + qoff(c), Nq, Hq, g * hq, hq) && in(Rk + c * bk, hk_ + koff(c), Nk, Hkv, g * hk, hk) &&
+           in(Rv + c * bk, hv_ + koff(c), Nk, Hkv, g * hk, hk);
+    }
+    for (int l = 0; l < kCopyLanes && ok; ++l) ok = cudaEventRecord(ev[ev_qkv(f, l)], cs[2 * l]) == cudaSuccess;
   }
-  // the caller's stream waits for every copy stream, then releases the buffer
-  for (int i = 0; i < 2 * kCopyLanes; ++i) {
+  for (int c = 0; c < n_chunks && ok; ++c) ok = in(Rdo + c * bq, hdo + qoff(c), Nq, Hq, (c % C) * hq, hq);
+  for (int l = 0; l < kCopyLanes && ok; ++l) ok = cudaEventRecord(ev[ev_do(l)], cs[2 * l]) == cudaSuccess;
+  // forward group f on the compute stream; its O and LSE go out while the
+  // next group (or the backward) runs. Host LSE [B][Hq][Nq] holds the chunks
+  // in chunk order, so a group's LSE is one contiguous copy.
+  for (int f = 0; f < F && ok; ++f) {
+    const int c0 = first(f), nc = first(f + 1) - c0;
+    for (int l = 0; l < kCopyLanes && ok; ++l) ok = cudaStreamWaitEvent(sc, ev[ev_qkv(f, l)], 0) == cudaSuccess;
+    if (!ok) break;
+    const Problem pf{Rq + c0 * bq, Rk + c0 * bk, Rv + c0 * bk, nc, hq, hk, Nq, Nk, d, scale, causal};
+    ok = launch_fwd(pf, Ro + c0 * bq, Rl + c0 * nl, sc) == cudaSuccess &&
+         cudaEventRecord(ev[ev_fwd(f)], sc) == cudaSuccess;
+    for (int l = 0; l < kCopyLanes && ok; ++l)
+      ok = cudaStreamWaitEvent(cs[2 * l + 1], ev[ev_fwd(f)], 0) == cudaSuccess;
+    for (int c = c0; c < c0 + nc && ok; ++c) ok = out(ho + qoff(c), Ro + c * bq, Nq, Hq, (c % C) * hq, hq);
+    ok = ok && cudaMemcpyAsync(hl + size_t(c0) * nl * 4, Rl + c0 * nl, nc * nl * 4, d2h, cs[1]) == cudaSuccess;
+  }
+  // the backward over all chunks, then its results out
+  for (int l = 0; l < kCopyLanes && ok; ++l) ok = cudaStreamWaitEvent(sc, ev[ev_do(l)], 0) == cudaSuccess;
+  if (ok) {
+    const Problem pb{Rq, Rk, Rv, n_chunks, hq, hk, Nq, Nk, d, scale, causal};
+    ok = bwd_pooled(pb, Ro, Rl, Rdo, Rdq, Rdk, Rdv, sc) == FA_OK && cudaEventRecord(ev[ev_bwd], sc) == cudaSuccess;
+  }
+  for (int l = 0; l < kCopyLanes && ok; ++l) ok = cudaStreamWaitEvent(cs[2 * l + 1], ev[ev_bwd], 0) == cudaSuccess;
+  for (int c = 0; c < n_chunks && ok; ++c) {
+    const int g = c % C;
+    ok = out(hdq + qoff(c), Rdq + c * bq, Nq, Hq, g * hq, hq) && out(hdk + koff(c), Rdk + c * bk, Nk, Hkv, g * hk, hk) &&
+         out(hdv + koff(c), Rdv + c * bk, Nk, Hkv, g * hk, hk);
+  }
+  // the caller's stream waits for every copy stream and the compute stream,
+  // then releases the buffer
+  for (int i = 0; i < 2 * kCopyLanes + 1; ++i) {
     cudaEvent_t e = ev[per_c + i];
     if (e != nullptr && cudaEventRecord(e, cs[i]) == cudaSuccess) cudaStreamWaitEvent(s, e, 0);
   }

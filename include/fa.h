@@ -143,17 +143,23 @@ int fa_bwd_window(const void* q, const void* k, const void* v, const void* o, co
  * and results), with every pointer a host address:
  *   in : q [B,Nq,Hq,d], k, v [B,Nk,Hkv,d], dout [B,Nq,Hq,d] (bf16)
  *   out: o [B,Nq,Hq,d] (bf16), lse [B,Hq,Nq] (fp32), dq, dk, dv (bf16).
- * The batch is processed in chunks and pipelined: the inputs of chunk c are
- * copied in on a library-owned copy stream while chunk c-1 computes on
- * `stream` and the results of chunk c-2 are copied out on a second copy
- * stream. A chunk is one batch element; a batch of one element with an even
- * Hkv is cut into two halves of its kv heads (each with its query heads),
- * copied as 2-D slices of the head dimension. The call only enqueues; `stream` is ordered after all
- * of it, so synchronise `stream` before reading the outputs, and keep every
- * host buffer alive (and the inputs unchanged) until then. The input copies
- * do not wait for earlier work on `stream`: the host inputs must hold their
- * values when the call is made. Consecutive calls therefore overlap: the
- * inputs of one call are copied in while the previous call computes.
+ * The batch is processed in chunks and pipelined over library-owned
+ * streams (one copy stream each way, one compute stream): a chunk is one
+ * batch element, or, for a batch of one element with an even Hkv, one half
+ * of its kv heads with their query heads (copied as 2-D slices of the head
+ * dimension). The forward runs as two launches over halves of the chunks:
+ * the first starts once its half's q, k, v are in, and its O and LSE go
+ * out while the second runs; dout is copied in meanwhile. The backward runs
+ * as one launch over all chunks, and dq, dk, dv go out after it.
+ * The call only enqueues; `stream` is ordered after all of it, so
+ * synchronise `stream` before reading the outputs, and keep every host
+ * buffer alive (and the inputs unchanged) until then. Nothing of the
+ * call waits for earlier work on `stream` (the copies and kernels touch only
+ * the host buffers and the library's device buffers): the host inputs must
+ * hold their values when the call is made. Consecutive calls therefore
+ * overlap: the inputs of one call are copied in while the previous call
+ * computes, and its kernels start while the previous call's last results
+ * are still being copied out.
  * Page-locked host memory gives asynchronous, full-speed copies; pageable
  * memory works but the copies are staged by the driver.
  * Device memory: two library-owned buffers per device, each a copy of every

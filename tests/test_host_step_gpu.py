@@ -1,7 +1,8 @@
 """fa_step_host: forward + backward on host buffers, pipelined over the
-batch (inputs in on one copy stream, compute on the caller's stream,
-results out on another; a one-element batch is cut into two halves of its
-kv heads). Checked through the C ABI element by element
+batch (inputs in on one copy stream, compute on a library stream, results
+out on another; a one-element batch is cut into two halves of its kv
+heads; the forward runs over two groups of these chunks, uneven for an odd
+count, the backward over all of them at once). Checked through the C ABI element by element
 against the fp64 oracle (O, LSE within the parity tolerances; dQ, dK, dV
 within them plus half a bf16 ulp of the value, as these GQA gradients
 exceed |x| = 4),
@@ -82,7 +83,8 @@ def test_step_host_matches_device_calls(fa, case, pinned):
 
 def test_step_host_back_to_back(fa):
     """Consecutive calls overlap (the inputs of one call are copied in while
-    the previous one computes; the device buffers alternate between calls):
+    the previous one computes, and its kernels run while the previous one's
+    results go out; the device buffers alternate between calls):
     three calls enqueued without a synchronisation in between, each on its
     own inputs and outputs, so that the third reuses the first one's device
     buffer, all match the device calls on their inputs."""
@@ -114,3 +116,41 @@ def test_step_host_back_to_back(fa):
         assert torch.equal(outs["lse"], lse.cpu())
         for name, ref in (("dq", dq), ("dk", dk), ("dv", dv)):
             assert_close(name, to64(outs[name]), to64(ref.cpu()))
+
+
+def test_step_host_stream_ordered_after_call(fa):
+    """The kernels run on a library stream, but the caller's stream is
+    ordered after every copy and kernel of the call: synchronising that
+    stream alone (not the device) is enough to read the host results, and
+    work enqueued on it afterwards sees them. Two calls on a side stream,
+    the second enqueued right after the first."""
+    B, Hq, Hkv, Nq, Nk, d, causal = 1, 8, 2, 1000, 1000, 128, True
+    args = (B, Hq, Hkv, Nq, Nk, d, 1.0 / math.sqrt(d), int(causal))
+    x = workloads.make_inputs(B, Hq, Hkv, Nq, Nk, d, seed=21, with_dout=True)
+    host = {n: x[n].pin_memory() for n in ("q", "k", "v", "do")}
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
+    o, lse = torch.empty_like(q), torch.empty((B, Hq, Nq), device="cuda", dtype=torch.float32)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    assert fa.fa_fwd(q, k, v, o, lse, *args) == 0
+    assert fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, *args) == 0
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    outs = []
+    for _ in range(2):
+        outs.append({n: torch.full(t.shape, float("nan"), dtype=t.dtype, pin_memory=True)
+                     for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))})
+        assert fa.fa_step_host(host["q"], host["k"], host["v"], host["do"], outs[-1]["o"], outs[-1]["lse"],
+                               outs[-1]["dq"], outs[-1]["dk"], outs[-1]["dv"], *args, stream=side) == 0
+    # a device copy of the second call's dK enqueued on the side stream
+    with torch.cuda.stream(side):
+        dk_dev = torch.empty_like(dk)
+        dk_dev.copy_(outs[1]["dk"], non_blocking=True)
+    side.synchronize()
+    for out in outs:
+        assert torch.equal(out["o"], o.cpu())
+        assert torch.equal(out["lse"], lse.cpu())
+        for name, ref in (("dq", dq), ("dk", dk), ("dv", dv)):
+            assert_close(name, to64(out[name]), to64(ref.cpu()))
+    assert torch.equal(dk_dev.cpu(), outs[1]["dk"])
+    torch.cuda.synchronize()
+    assert fa.fa_get_status() == 0
