@@ -21,6 +21,8 @@
 //                       from shared memory; P of each stage is staged as an
 //                       e4m3 tile [128 rows x 128 keys] with the 128-byte
 //                       swizzle.
+#include <algorithm>
+
 #include "fa_fwd_pipeline.cuh"
 
 namespace fa {
@@ -77,18 +79,32 @@ __device__ __forceinline__ float had_sign(int i) {
   return ((2654435769u * uint32_t(i + 1)) >> 31) ? -1.0f : 1.0f;
 }
 
+// the signs of the 32 elements lane ql of a quad holds, as bits: bit j set
+// where sign_{32 ql + j} = -1
+__device__ __forceinline__ uint32_t had_sign_bits(int ql) {
+  uint32_t bits = 0;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) bits |= (had_sign(ql * 32 + j) < 0.0f ? 1u : 0u) << j;
+  return bits;
+}
+
+// x with its sign flipped where bit j of `bits` is set (exact)
+__device__ __forceinline__ float flip_sign(float x, uint32_t bits, int j) {
+  return __uint_as_float(__float_as_uint(x) ^ (((bits >> j) & 1u) << 31));
+}
+
 // Rows of 128 values are handled by quads of lanes: lane ql = lane & 3 of a
 // quad holds elements 32 ql .. 32 ql + 31 of its row. quad_transform
 // multiplies the row by diag(signs) H_128 (the 1/sqrt(128) is left to the
 // caller): a butterfly over the seven index bits, five inside the lane
-// (bit 0 fused with the signs sg[j] = sign_{32 ql + j}) and two across the
-// quad.
-__device__ __forceinline__ void quad_transform(float (&x)[32], const float (&sg)[32], int ql) {
+// (bit 0 fused with the signs, `sgn` = had_sign_bits(ql)) and two across
+// the quad.
+__device__ __forceinline__ void quad_transform(float (&x)[32], uint32_t sgn, int ql) {
 #pragma unroll
   for (int j = 0; j < 32; j += 2) {
-    const float a = x[j] * sg[j];
-    x[j] = fmaf(x[j + 1], sg[j + 1], a);
-    x[j + 1] = fmaf(-x[j + 1], sg[j + 1], a);
+    const float a = flip_sign(x[j], sgn, j), c = flip_sign(x[j + 1], sgn, j + 1);
+    x[j] = a + c;
+    x[j + 1] = a - c;
   }
 #pragma unroll
   for (int m = 2; m < 32; m <<= 1) {
@@ -158,35 +174,42 @@ __device__ __forceinline__ void quant_v_tile(const __nv_bfloat16* v, int Nk, int
 
 constexpr float kInvSqrt128 = 0.08838834764831845f;
 
-// Row pass over Q, K (and V when !QUANT) of one batch (blockIdx.z), tensor
-// t = blockIdx.y (0 = Q, 1 = K, 2 = V), rows [B, N, H] of 128 values:
+// Row pass over Q, K (and V when !QUANT) of one batch (blockIdx.z), rows
+// [B, N, H] of 128 values:
 //   !QUANT: per (batch, head) max |x M| (M the incoherent transform when
 //           had; V untransformed), gathered per head in shared memory and
 //           merged with one atomicMax on the (non-negative) float bits per
 //           head and block; the maxima start at zero.
-//   QUANT:  x M rounded to e4m3 with its head's scale, [rows x 128] bytes.
-// A warp takes 8 rows (a quad each) and loads its next group of rows before
-// transforming the current one; the grid strides over the batch's rows.
+//   QUANT:  x M rounded to e4m3 with its head's scale, [rows x 128] bytes;
+//           V rounded and transposed by the V blocks.
+// Blocks [0, nbq) of a batch take Q, [nbq, nbq + nbk) K and the rest V (the
+// host splits them in proportion to the tensors' rows, so that every block
+// has about the same bytes to move). A warp takes 8 rows (a quad each)
+// and keeps the loads of its next two groups of rows in flight while it
+// transforms the current one; each tensor's blocks stride over its rows.
 template <bool QUANT>
 __global__ void __launch_bounds__(256, 2) fp8_rows_kernel(const __nv_bfloat16* q, const __nv_bfloat16* k,
                                                        const __nv_bfloat16* v, int Nq, int Nk, int Hq, int Hkv,
                                                        int had, unsigned* amax_q, unsigned* amax_k,
                                                        unsigned* amax_v, uint8_t* q8, uint8_t* k8, int Nk_pad,
-                                                       uint8_t* vt8) {
+                                                       uint8_t* vt8, int nbq, int nbk) {
   extern __shared__ float head_sm[];  // QUANT: 1 / (scale sqrt(128)) per head; else max bits per head
-  if (QUANT && blockIdx.y == 2) {
-    // the V transpose runs in the same launch: blockIdx.y = 2 strides over
-    // the (key tile, kv head) tiles of batch blockIdx.z
-    const int b = blockIdx.z, nkt = Nk_pad / 128;
-    for (int t = blockIdx.x; t < nkt * Hkv; t += gridDim.x) {
-      const int kvh = t / nkt, kt = t - kvh * nkt;
+  const int bi = blockIdx.x;
+  const int t = bi < nbq ? 0 : (bi < nbq + nbk ? 1 : 2);
+  const int bx = bi - (t == 0 ? 0 : (t == 1 ? nbq : nbq + nbk));
+  const int nbx = t == 0 ? nbq : (t == 1 ? nbk : int(gridDim.x) - nbq - nbk);
+  const int b = blockIdx.z;
+  if (QUANT && t == 2) {
+    // the V blocks stride over the (key tile, kv head) tiles of the batch
+    const int nkt = Nk_pad / 128;
+    for (int i = bx; i < nkt * Hkv; i += nbx) {
+      const int kvh = i / nkt, kt = i - kvh * nkt;
       quant_v_tile(v, Nk, Hkv, Nk_pad, 1.0f / amax_scale(amax_v[b * Hkv + kvh]), vt8, kt, kvh, b);
     }
     return;
   }
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   const int ql = lane & 3, quad = lane >> 2;
-  const int t = blockIdx.y, b = blockIdx.z;
   const int H = t == 0 ? Hq : Hkv, N = t == 0 ? Nq : Nk;
   const __nv_bfloat16* x_b = (t == 0 ? q : (t == 1 ? k : v)) + size_t(b) * N * H * 128;
   unsigned* amax = (t == 0 ? amax_q : (t == 1 ? amax_k : amax_v)) + b * H;
@@ -196,21 +219,22 @@ __global__ void __launch_bounds__(256, 2) fp8_rows_kernel(const __nv_bfloat16* q
     if (QUANT) head_sm[h] = (tr ? kInvSqrt128 : 1.0f) / amax_scale(amax[h]);
     else reinterpret_cast<unsigned*>(head_sm)[h] = 0u;
   }
-  float sg[32];
-#pragma unroll
-  for (int j = 0; j < 32; ++j) sg[j] = had_sign(ql * 32 + j);
+  const uint32_t sgn = had_sign_bits(ql);
   __syncthreads();
   const int R = N * H;
-  const int step = gridDim.x * nwarps;
-  int g = blockIdx.x * nwarps + warp;
-  uint4 u[4];
+  const int step = nbx * nwarps;
+  int g = bx * nwarps + warp;
+  uint4 u[4], un[4];
   load_quad_row(x_b + size_t(g * 8 + quad) * 128, ql, g * 8 + quad < R, u);
+  load_quad_row(x_b + size_t((g + step) * 8 + quad) * 128, ql, (g + step) * 8 + quad < R, un);
   for (; g * 8 < R; g += step) {
-    const int r = g * 8 + quad, rn = r + step * 8;
+    const int r = g * 8 + quad, rn = r + 2 * step * 8;
     float x[32];
     unpack_quad_row(u, x);
-    load_quad_row(x_b + size_t(rn) * 128, ql, rn < R, u);  // the next group's row, in flight meanwhile
-    if (tr) quad_transform(x, sg, ql);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) u[c] = un[c];
+    load_quad_row(x_b + size_t(rn) * 128, ql, rn < R, un);  // the group after next, in flight meanwhile
+    if (tr) quad_transform(x, sgn, ql);
     const int h = r % H;
     if (QUANT) {
       const float inv = r < R ? head_sm[h] : 0.0f;
@@ -412,17 +436,22 @@ cudaError_t launch_t(const Problem& pb, void* o, float* lse, int incoherent, cud
   }
   if (e == cudaSuccess) e = cudaMemsetAsync(amax_q, 0, n_amax * 4, stream);
   if (e == cudaSuccess) {
-    // about two resident blocks per SM over all (tensor, batch) columns
+    // about two resident blocks per SM, split between Q, K and V of each
+    // batch element in proportion to their rows (at least one block each)
     const int Hmax = pb.Hq > pb.Hkv ? pb.Hq : pb.Hkv;
     const size_t hs = size_t(Hmax) * 4;
-    const int bx_a = (2 * G + 3 * pb.B - 1) / (3 * pb.B), bx_q = (2 * G + 2 * pb.B - 1) / (2 * pb.B);
+    const int per_b = std::max(3, (2 * G + pb.B - 1) / pb.B);
+    const double rq = double(pb.Nq) * pb.Hq, rk = double(pb.Nk) * pb.Hkv, rall = rq + 2.0 * rk;
+    const int nbq = std::max(1, int(per_b * rq / rall + 0.5)), nbk = std::max(1, int(per_b * rk / rall + 0.5));
+    const int nbv = std::max(1, per_b - nbq - nbk);
+    const dim3 grid(unsigned(nbq + nbk + nbv), 1, unsigned(pb.B));
     const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(pb.q);
     const __nv_bfloat16* k = static_cast<const __nv_bfloat16*>(pb.k);
     const __nv_bfloat16* v = static_cast<const __nv_bfloat16*>(pb.v);
-    fp8_rows_kernel<false><<<dim3(bx_a, 3, pb.B), 256, hs, stream>>>(q, k, v, pb.Nq, pb.Nk, pb.Hq, pb.Hkv, incoherent,
-                                                                      amax_q, amax_k, amax_v, q8, k8, Nk_pad, vt8);
-    fp8_rows_kernel<true><<<dim3(bx_q, 3, pb.B), 256, hs, stream>>>(q, k, v, pb.Nq, pb.Nk, pb.Hq, pb.Hkv, incoherent,
-                                                                     amax_q, amax_k, amax_v, q8, k8, Nk_pad, vt8);
+    fp8_rows_kernel<false><<<grid, 256, hs, stream>>>(q, k, v, pb.Nq, pb.Nk, pb.Hq, pb.Hkv, incoherent, amax_q, amax_k,
+                                                      amax_v, q8, k8, Nk_pad, vt8, nbq, nbk);
+    fp8_rows_kernel<true><<<grid, 256, hs, stream>>>(q, k, v, pb.Nq, pb.Nk, pb.Hq, pb.Hkv, incoherent, amax_q, amax_k,
+                                                     amax_v, q8, k8, Nk_pad, vt8, nbq, nbk);
     e = cudaGetLastError();
   }
   if (e == cudaSuccess) {
