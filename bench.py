@@ -44,7 +44,8 @@ MAIN = workloads.BY_NAME["fwd_causal_gqa_b1_hq32_hkv8_n16384_d128"]
 METRIC = "attention fwd/bwd TFLOP/s at 1 GB300 and fraction of dense BF16 tensor peak"
 FLUSH_BYTES = 256 << 20
 KERNEL_SOURCES = {"fa_fwd_kernel": ("fa_fwd.cu", "fa_fwd_pipeline.cuh"), "bwd_main_kernel": ("fa_bwd.cu",),
-                  "fa_fwd8_kernel": ("fa_fwd8.cu", "fa_fwd_pipeline.cuh")}
+                  "fa_fwd8_kernel": ("fa_fwd8.cu", "fa_fwd_pipeline.cuh"),
+                  "fa_fwd_pair_kernel": ("fa_fwd.cu", "fa_fwd_pipeline.cuh")}
 PANEL = 1024  # query rows of one oracle sample
 
 
